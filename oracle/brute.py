@@ -1,0 +1,89 @@
+"""Scalar brute force for tiny inputs: a pin for the vectorised oracle.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Written separately from ``formats`` / ``nvfp4`` / ``indexer``: formats are
+decoded from their bit fields with ``math.ldexp`` (no value tables), bytes
+are walked one element at a time, dot products are plain Python float
+(float64) loops, and the selection is a full sort of (-score, id) pairs.
+Pure Python: only for a handful of pages and heads.
+"""
+from __future__ import annotations
+
+import math
+
+
+def e2m1(code: int) -> float:
+    """E2M1 from its fields: sign | 2-bit exponent (bias 1) | 1-bit mantissa."""
+    s = -1.0 if code & 8 else 1.0
+    e = (code >> 1) & 3
+    m = code & 1
+    if e == 0:
+        return s * math.ldexp(m, -1)          # subnormal: m * 2^(1-1) * 1/2
+    return s * math.ldexp(1.0 + m / 2.0, e - 1)
+
+
+def e4m3(byte: int) -> float:
+    """E4M3fn from its fields: sign | 4-bit exponent (bias 7) | 3-bit mantissa."""
+    s = -1.0 if byte & 0x80 else 1.0
+    e = (byte >> 3) & 0xF
+    m = byte & 7
+    if e == 15 and m == 7:
+        return math.nan
+    if e == 0:
+        return s * math.ldexp(m, -9)           # m/8 * 2^-6
+    return s * math.ldexp(8 + m, e - 10)       # (1 + m/8) * 2^(e-7)
+
+
+def key_element(row: bytes, e: int) -> float:
+    b = row[e // 2]
+    code = (b >> 4) if (e & 1) else (b & 0xF)
+    return e2m1(code) * e4m3(row[64 + e // 16])
+
+
+def score(q_bytes, page_rows) -> tuple:
+    """(max_t q.k_t, max_t sum |q_d k_td|) over the 128 rows of one page."""
+    q = [e4m3(int(b)) for b in q_bytes]
+    best = -math.inf
+    best_abs = -math.inf
+    for row in page_rows:
+        row = bytes(int(x) for x in row)
+        acc = 0.0
+        acc_abs = 0.0
+        for d in range(128):
+            p = q[d] * key_element(row, d)
+            acc += p
+            acc_abs += abs(p)
+        best = max(best, acc)
+        best_abs = max(best_abs, acc_abs)
+    return best, best_abs
+
+
+def indexer_rows(q, kv_pages, page_table, seq_lens, qlens, num_heads):
+    """Ids [rows][H][16] and scores {(row, h, page): S} by brute force."""
+    out = []
+    scores = {}
+    row = 0
+    for r, (seq, ql) in enumerate(zip(seq_lens, qlens)):
+        for i in range(int(ql)):
+            pos = int(seq) - int(ql) + i
+            per_head = []
+            for h in range(num_heads):
+                if pos < 0:
+                    per_head.append([-1] * 16)
+                    continue
+                L = pos // 128
+                cand = []
+                for j in range(L):
+                    phys = int(page_table[r][j])
+                    s, a = score(q[row][h], kv_pages[phys])
+                    scores[(row, h, j)] = (s, a)
+                    cand.append((-s, j))
+                cand.sort()
+                ids = [j for _, j in cand[:15]]
+                ids.append(L)
+                ids += [-1] * (16 - len(ids))
+                per_head.append(ids)
+            out.append(per_head)
+            row += 1
+    return out, scores
