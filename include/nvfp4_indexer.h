@@ -1,0 +1,175 @@
+/*
+ * nvfp4_indexer.h -- C ABI of the GB300 (sm_103a) NVFP4 lightning indexer.
+ *
+ * The indexer selects, for every query token and every index head, the 16
+ * pages of the paged KV cache that block-sparse attention will read: the 15
+ * history pages whose best token scores highest against the query, then the
+ * query's own (local) page, then -1.  Source pages:
+ *   vllm.models.minimax_m3.nvidia.indexer_nvfp4 (module description; class
+ *   MiniMaxM3IndexerNvfp4Impl, __init__ / forward / _prefill; class
+ *   MiniMaxM3IndexerNvfp4MetadataBuilder, build / _build_prefill_chunks) and
+ *   vllm.models.minimax_m3.nvidia.indexer_flashinfer (forward; builder build).
+ *
+ * Fixed configuration (MiniMaxM3IndexerNvfp4Impl.__init__ rejects anything
+ * else): 128-token pages, index head dim 128, top-k 16, init_blocks 0,
+ * local_blocks 1, "max" scoring.
+ *
+ * Data formats (indexer_nvfp4, module description):
+ *   kv_pages  uint8 [num_blocks][128 tokens][72 B]; per token 64 B of E2M1
+ *             codes (element e in byte e/2, low nibble for even e) then 8 E4M3
+ *             scales, scale j for elements 16j..16j+15; no global scale.
+ *   q         E4M3 bytes [rows][H][128], row-major.
+ *   out       int32 [rows][H][16] logical page ids: up to 15 history pages by
+ *             score (descending; equal scores: lower id first), the local page
+ *             pos/128, then -1.  A row whose position is negative (a padding
+ *             request) is all -1.
+ *   page_table int32 [num_reqs][pt_stride] logical -> physical page.
+ *   seq_lens  int32 [num_reqs], every token of the request including the
+ *             queries; queries sit at the last positions (right-aligned).
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers unless stated; the caller owns
+ *     them.  Calls never allocate, never synchronise the stream (except
+ *     indexer_get_status) and read seq_lens / page_table / cu_seqlens_q in
+ *     place, so indexer_decode can be captured in a CUDA graph.
+ *   - kv_pages and q must be 16-byte aligned; out 16-byte aligned.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns IDX_EINVAL / IDX_EUNSUPPORTED and launches nothing.  The text of
+ *     the last error of the calling thread is in indexer_last_error().
+ *   - Device-side bad data (a page id outside [0, num_blocks), a history that
+ *     does not fit pt_stride) never traps: the affected request's rows are
+ *     written as -1 and the plan's status word records it (indexer_get_status).
+ *   - A CUDA launch error returns IDX_ECUDA.
+ */
+#ifndef NVFP4_INDEXER_H
+#define NVFP4_INDEXER_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  IDX_OK = 0,
+  IDX_EINVAL = -1,         /* bad pointer, size, alignment or stride           */
+  IDX_EUNSUPPORTED = -2,   /* head count or query length outside the kernels   */
+  IDX_ECUDA = -3,          /* CUDA runtime error                              */
+  IDX_ENOSPACE = -4,       /* call exceeds the sizes the plan was made for     */
+  IDX_EDEVICE = -5         /* a device-side check fired (indexer_get_status)   */
+};
+
+/* Status bits of the device status word. */
+enum {
+  IDX_STATUS_BAD_PAGE = 1,     /* a page id outside the cache; rows set to -1  */
+  IDX_STATUS_BAD_TABLE = 2,    /* history wider than pt_stride; rows set to -1 */
+  IDX_STATUS_TIMEOUT = 4,      /* a bounded wait gave up; outputs undefined    */
+  IDX_STATUS_BAD_SLOT = 8      /* nvfp4_insert skipped a slot past the cache    */
+};
+
+typedef struct indexer_plan_s* indexer_plan_t;
+
+/*
+ * indexer_plan -- create a plan on the current CUDA device.
+ * Owns the device scratch of the decode split-merge (per-split top-15
+ * candidates, per-request bookkeeping) and the status word; sized here and
+ * never resized.  Mirrors MiniMaxM3IndexerNvfp4MetadataBuilder.__init__,
+ * which sizes one decode score buffer for the largest batch and context.
+ *   num_heads          index heads H; one of 1, 2, 4, 8 (the builder's
+ *                      DECODE_NUM_HEADS check; read here as {1,2,4,8})
+ *   max_reqs           largest num_reqs of any indexer_decode call
+ *   max_query_len      largest decode query_len, 1..8 (the builder rejects
+ *                      more than 8 decode queries per request)
+ *   max_pages_per_req  largest page-table width a call may pass as pt_stride
+ *   max_prefill_tokens largest total_q of any indexer_prefill call
+ *   max_prefill_reqs   largest num_reqs of any indexer_prefill call
+ * Returns IDX_OK and *plan, or an error (nothing allocated).
+ */
+int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_query_len,
+                 int max_pages_per_req, int max_prefill_tokens, int max_prefill_reqs);
+
+/* Free the plan's device memory.  The caller must not have work using the
+ * plan in flight.  NULL is accepted. */
+int indexer_plan_destroy(indexer_plan_t plan);
+
+/*
+ * indexer_decode -- top-k pages for uniform decode batches
+ * (MiniMaxM3IndexerNvfp4Impl.forward, decode branch; the Q8KV4 indexer reads
+ * the 1..8 queries of each request in place and writes straight to out).
+ *   q          E4M3 [num_reqs * query_len][H][128]; row r*query_len+i is query
+ *              i of request r, at position seq_lens[r] - query_len + i
+ *   kv_pages   [num_blocks][128][72]
+ *   page_table [num_reqs][pt_stride], pt_stride <= plan max_pages_per_req
+ *   seq_lens   [num_reqs]; a request with seq_lens < query_len pads a graph
+ *              batch, its rows with negative position are all -1
+ *   num_reqs   1..plan max_reqs (host scalar, fixed in a captured graph)
+ *   query_len  1..plan max_query_len
+ *   out        int32 [num_reqs * query_len][H][16]
+ *   scores_dbg NULL, or fp32 [num_reqs * query_len][H][dbg_stride]: page
+ *              scores of every history page j < pos/128 of the row (other
+ *              entries untouched); dbg_stride >= pt_stride
+ *   stream     the stream all work is queued on
+ * Work: each history page is read from HBM once for all queries and heads of
+ * its request, scored on the tensor cores, top-15 kept per row; requests
+ * split across CTAs are merged by a second small kernel.
+ */
+int indexer_decode(indexer_plan_t plan, const uint8_t* q, const uint8_t* kv_pages, int num_blocks,
+                   const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
+                   int num_reqs, int query_len, int32_t* out, float* scores_dbg, int dbg_stride,
+                   cudaStream_t stream);
+
+/*
+ * indexer_prefill -- top-k pages for ragged prefill rows (MiniMaxM3Indexer-
+ * Nvfp4Impl._prefill; per-token causal clamp = pos/128 + 1 valid pages, as
+ * the flashinfer builder's num_valid_pages).  Scores the NVFP4 pages
+ * directly (exact fp16 dequantisation in shared memory), without the pages'
+ * FP8 gather workspace.
+ *   q            E4M3 [total_q][H][128]
+ *   cu_seqlens_q int32 [num_reqs + 1], cu[0] = 0, cu[num_reqs] = total_q;
+ *                request r owns rows cu[r] .. cu[r+1]-1 at positions
+ *                seq_lens[r] - (cu[r+1]-cu[r]) + i (context first)
+ *   num_reqs     1..plan max_prefill_reqs;  total_q <= plan max_prefill_tokens
+ *   max_seqlen_q host upper bound of cu[r+1]-cu[r] (sizes the grid)
+ *   out          int32 [total_q][H][16] (pass decode out + num_decode_rows*H*16
+ *                for a mixed step; decode rows come first, as in forward)
+ *   scores_dbg   NULL, or fp32 [total_q][H][dbg_stride], dbg_stride >= pt_stride
+ */
+int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seqlens_q,
+                    int num_reqs, int total_q, int max_seqlen_q, const uint8_t* kv_pages,
+                    int num_blocks, const int32_t* page_table, int pt_stride,
+                    const int32_t* seq_lens, int32_t* out, float* scores_dbg, int dbg_stride,
+                    cudaStream_t stream);
+
+/*
+ * nvfp4_insert -- quantise bf16 index keys and write them into the pages
+ * (the quantise-and-scatter half of the fused qk-norm/rope insert named in
+ * the indexer_nvfp4 module description).  Per token and 16-element group:
+ * scale byte = E4M3 round-to-nearest-even of amax/6 (saturating at 448);
+ * code = E2M1 round-to-nearest-even of x/scale (saturating at 6, sign kept,
+ * sign-only zero codes when the scale is 0).
+ *   k_bf16       [n][128] bf16 bit patterns, 16-byte aligned
+ *   slot_mapping int64 [n]: page * 128 + row; negative = skip
+ *   n            tokens (0 is a no-op)
+ *   kv_pages     [num_blocks][128][72]
+ *   status       NULL, or a device int32 that gets IDX_STATUS_BAD_SLOT OR-ed
+ *                in when a slot >= num_blocks*128 was skipped
+ */
+int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* kv_pages,
+                 int num_blocks, int32_t* status, cudaStream_t stream);
+
+/* Synchronise `stream`, read and clear the plan's device status word.
+ * Returns IDX_OK, or IDX_EDEVICE with the IDX_STATUS_* bits in *bits. */
+int indexer_get_status(indexer_plan_t plan, cudaStream_t stream, int32_t* bits);
+
+/* Text of the calling thread's last error ("" if none). */
+const char* indexer_last_error(void);
+
+/* Library version string. */
+const char* indexer_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_INDEXER_H */

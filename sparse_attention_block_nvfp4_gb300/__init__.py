@@ -1,0 +1,198 @@
+"""GB300 (sm_103a) NVFP4 lightning indexer -- Python binding.
+
+A thin ctypes layer over ``libnvfp4_indexer.so`` (C ABI declared in
+``include/nvfp4_indexer.h``).  It only marshals arguments: checks dtypes,
+shapes, devices and contiguity of torch tensors, passes raw device pointers
+and the current CUDA stream, and turns non-zero status codes into
+``IndexerError``.  Every step of the indexer runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback.  If the library has not been
+built, importing the functions below raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+__all__ = ["Plan", "insert", "IndexerError", "load_library", "library_path", "declared_symbols",
+           "STATUS_BAD_PAGE", "STATUS_BAD_TABLE", "STATUS_TIMEOUT", "STATUS_BAD_SLOT", "TOPK", "PAGE"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_LIB_PATH = os.path.join(_HERE, "libnvfp4_indexer.so")
+_HEADER = os.path.join(_ROOT, "include", "nvfp4_indexer.h")
+
+PAGE = 128
+TOPK = 16
+STATUS_BAD_PAGE, STATUS_BAD_TABLE, STATUS_TIMEOUT, STATUS_BAD_SLOT = 1, 2, 4, 8
+IDX_OK, IDX_EINVAL, IDX_EUNSUPPORTED, IDX_ECUDA, IDX_ENOSPACE, IDX_EDEVICE = 0, -1, -2, -3, -4, -5
+
+_lib = None
+
+
+class IndexerError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def declared_symbols() -> list:
+    """Function names declared in include/nvfp4_indexer.h."""
+    text = open(_HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)
+
+
+def load_library():
+    """Load the built library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.indexer_plan.argtypes = [ctypes.POINTER(P), I, I, I, I, I, I]
+    lib.indexer_plan_destroy.argtypes = [P]
+    lib.indexer_decode.argtypes = [P, P, P, I, P, I, P, I, I, P, P, I, P]
+    lib.indexer_prefill.argtypes = [P, P, P, I, I, I, P, I, P, I, P, P, P, I, P]
+    lib.nvfp4_insert.argtypes = [P, P, I, P, I, P, P]
+    lib.indexer_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.indexer_last_error.restype = ctypes.c_char_p
+    lib.indexer_version.restype = ctypes.c_char_p
+    for name in ("indexer_plan", "indexer_plan_destroy", "indexer_decode", "indexer_prefill",
+                 "nvfp4_insert", "indexer_get_status"):
+        getattr(lib, name).restype = I
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != IDX_OK:
+        raise IndexerError(rc, load_library().indexer_last_error().decode())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t, dtype, name, ndim=None):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+class Plan:
+    """Owns the indexer's device scratch for calls up to the given sizes
+    (``indexer_plan``).  ``num_heads`` in {1, 2, 4, 8}; ``max_query_len`` 1..8."""
+
+    def __init__(self, num_heads: int, max_reqs: int, max_query_len: int, max_pages_per_req: int,
+                 max_prefill_tokens: int = 0, max_prefill_reqs: int = 0):
+        lib = load_library()
+        h = ctypes.c_void_p()
+        _check(lib.indexer_plan(ctypes.byref(h), num_heads, max_reqs, max_query_len,
+                                max_pages_per_req, max_prefill_tokens, max_prefill_reqs))
+        self._h = h
+        self.num_heads = num_heads
+        self.max_pages_per_req = max_pages_per_req
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load_library().indexer_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def decode(self, q, kv_pages, page_table, seq_lens, query_len: int, out=None, scores_dbg=None,
+               stream=None):
+        """Top-k pages of a uniform decode batch; returns ``out`` int32 [rows, H, 16]."""
+        import torch
+        H = self.num_heads
+        if q.dim() != 3 or q.shape[1] != H or q.shape[2] != 128:
+            raise ValueError(f"q: expected [rows, {H}, 128], got {tuple(q.shape)}")
+        num_reqs = int(seq_lens.shape[0])
+        if q.shape[0] != num_reqs * query_len:
+            raise ValueError("q rows != num_reqs * query_len")
+        if out is None:
+            out = torch.empty((q.shape[0], H, TOPK), dtype=torch.int32, device=q.device)
+        dbg_stride = 0
+        if scores_dbg is not None:
+            dbg_stride = int(scores_dbg.shape[-1])
+        _check(load_library().indexer_decode(
+            self._h, _ptr(q, torch.uint8, "q"), _ptr(kv_pages, torch.uint8, "kv_pages", 3),
+            int(kv_pages.shape[0]), _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
+            _ptr(seq_lens, torch.int32, "seq_lens", 1), num_reqs, int(query_len),
+            _ptr(out, torch.int32, "out"), _ptr(scores_dbg, torch.float32, "scores_dbg"), dbg_stride,
+            _stream_ptr(stream)))
+        return out
+
+    def prefill(self, q, cu_seqlens_q, kv_pages, page_table, seq_lens, max_seqlen_q: int, out=None,
+                scores_dbg=None, stream=None):
+        """Top-k pages of ragged prefill rows; returns ``out`` int32 [total_q, H, 16]."""
+        import torch
+        H = self.num_heads
+        if q.dim() != 3 or q.shape[1] != H or q.shape[2] != 128:
+            raise ValueError(f"q: expected [total_q, {H}, 128], got {tuple(q.shape)}")
+        num_reqs = int(seq_lens.shape[0])
+        if cu_seqlens_q.shape[0] != num_reqs + 1:
+            raise ValueError("cu_seqlens_q must have num_reqs + 1 entries")
+        total_q = int(q.shape[0])
+        if out is None:
+            out = torch.empty((total_q, H, TOPK), dtype=torch.int32, device=q.device)
+        dbg_stride = int(scores_dbg.shape[-1]) if scores_dbg is not None else 0
+        _check(load_library().indexer_prefill(
+            self._h, _ptr(q, torch.uint8, "q"), _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1),
+            num_reqs, total_q, int(max_seqlen_q), _ptr(kv_pages, torch.uint8, "kv_pages", 3),
+            int(kv_pages.shape[0]), _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
+            _ptr(seq_lens, torch.int32, "seq_lens", 1), _ptr(out, torch.int32, "out"),
+            _ptr(scores_dbg, torch.float32, "scores_dbg"), dbg_stride, _stream_ptr(stream)))
+        return out
+
+    def status(self, stream=None) -> int:
+        """Synchronise, read and clear the device status word (IDX_STATUS_* bits)."""
+        bits = ctypes.c_int32(0)
+        rc = load_library().indexer_get_status(self._h, _stream_ptr(stream), ctypes.byref(bits))
+        if rc not in (IDX_OK, IDX_EDEVICE):
+            _check(rc)
+        return int(bits.value)
+
+
+def insert(k_bf16, slot_mapping, kv_pages, status=None, stream=None):
+    """Quantise bf16 keys [n, 128] to NVFP4 and write them at ``slot_mapping``."""
+    import torch
+    if k_bf16.dim() != 2 or k_bf16.shape[1] != 128:
+        raise ValueError("k_bf16: expected [n, 128]")
+    kb = k_bf16.view(torch.int16) if k_bf16.dtype == torch.bfloat16 else k_bf16
+    n = int(kb.shape[0])
+    if slot_mapping.shape[0] != n:
+        raise ValueError("slot_mapping must have one entry per key")
+    _check(load_library().nvfp4_insert(
+        _ptr(kb, torch.int16, "k_bf16"), _ptr(slot_mapping, torch.int64, "slot_mapping", 1), n,
+        _ptr(kv_pages, torch.uint8, "kv_pages", 3), int(kv_pages.shape[0]),
+        _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
+    return kv_pages

@@ -1,0 +1,249 @@
+// api.cu -- the C ABI (include/nvfp4_indexer.h): argument checks, the plan
+// object and its device scratch, launches on the caller's stream.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4_indexer.h"
+#include "internal.h"
+
+using namespace nvfp4idx;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int set_err(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_err(cudaError_t e, const char* what) {
+  return set_err(IDX_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_heads(int h) { return h == 1 || h == 2 || h == 4 || h == 8; }
+
+}  // namespace
+
+struct indexer_plan_s {
+  int device = 0;
+  int num_sms = 0;
+  int num_heads = 0, max_reqs = 0, max_query_len = 0, max_pages = 0;
+  int max_prefill_tokens = 0, max_prefill_reqs = 0;
+  int decode_grid = 0;
+  float2* cand = nullptr;      // [(decode_grid + max_reqs)][64][15]
+  int32_t* slot_bad = nullptr; // [decode_grid + max_reqs]
+  int2* req_info = nullptr;    // [max_reqs]
+  int32_t* status = nullptr;   // 1 word
+};
+
+extern "C" {
+
+const char* indexer_version(void) { return "nvfp4_indexer 0.1 sm_103a"; }
+
+const char* indexer_last_error(void) { return g_last_error.c_str(); }
+
+int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_query_len,
+                 int max_pages_per_req, int max_prefill_tokens, int max_prefill_reqs) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "indexer_plan: plan is NULL");
+  *plan = nullptr;
+  if (!valid_heads(num_heads))
+    return set_err(IDX_EUNSUPPORTED, "indexer_plan: num_heads=%d, supported 1, 2, 4, 8", num_heads);
+  if (max_query_len < 1 || max_query_len > 8)
+    return set_err(IDX_EUNSUPPORTED, "indexer_plan: max_query_len=%d, supported 1..8", max_query_len);
+  if (max_reqs < 0 || max_reqs > kMaxDecodeReqs)
+    return set_err(IDX_EINVAL, "indexer_plan: max_reqs=%d outside 0..%d", max_reqs, kMaxDecodeReqs);
+  if (max_pages_per_req < 1 || max_pages_per_req > (1 << 20))
+    return set_err(IDX_EINVAL, "indexer_plan: max_pages_per_req=%d outside 1..2^20", max_pages_per_req);
+  if (max_prefill_tokens < 0 || max_prefill_reqs < 0 || max_prefill_reqs > (1 << 16))
+    return set_err(IDX_EINVAL, "indexer_plan: bad prefill limits (%d tokens, %d requests)",
+                   max_prefill_tokens, max_prefill_reqs);
+
+  indexer_plan_s* pl = new indexer_plan_s();
+  cudaError_t e = cudaGetDevice(&pl->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device);
+  if (e != cudaSuccess) {
+    delete pl;
+    return cuda_err(e, "indexer_plan: device query");
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, pl->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, pl->device);
+  if (major != 10 || minor != 3) {
+    delete pl;
+    return set_err(IDX_EUNSUPPORTED, "indexer_plan: device is sm_%d%d, the kernels are built for sm_103a",
+                   major, minor);
+  }
+  pl->num_heads = num_heads;
+  pl->max_reqs = max_reqs;
+  pl->max_query_len = max_query_len;
+  pl->max_pages = max_pages_per_req;
+  pl->max_prefill_tokens = max_prefill_tokens;
+  pl->max_prefill_reqs = max_prefill_reqs;
+  pl->decode_grid = 2 * pl->num_sms;
+  const size_t slots = (size_t)pl->decode_grid + (size_t)max_reqs;
+  e = cudaMalloc(&pl->cand, slots * kMaxRows * kHistK * sizeof(float2));
+  if (e == cudaSuccess) e = cudaMalloc(&pl->slot_bad, slots * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&pl->req_info, (size_t)(max_reqs > 0 ? max_reqs : 1) * sizeof(int2));
+  if (e == cudaSuccess) e = cudaMalloc(&pl->status, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(pl->status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(pl->slot_bad, 0, slots * sizeof(int32_t));
+  if (e != cudaSuccess) {
+    indexer_plan_destroy(pl);
+    return cuda_err(e, "indexer_plan: allocation");
+  }
+  *plan = pl;
+  return IDX_OK;
+}
+
+int indexer_plan_destroy(indexer_plan_t plan) {
+  if (!plan) return IDX_OK;
+  cudaFree(plan->cand);
+  cudaFree(plan->slot_bad);
+  cudaFree(plan->req_info);
+  cudaFree(plan->status);
+  delete plan;
+  return IDX_OK;
+}
+
+int indexer_decode(indexer_plan_t plan, const uint8_t* q, const uint8_t* kv_pages, int num_blocks,
+                   const int32_t* page_table, int pt_stride, const int32_t* seq_lens, int num_reqs,
+                   int query_len, int32_t* out, float* scores_dbg, int dbg_stride, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "indexer_decode: plan is NULL");
+  if (!q || !kv_pages || !page_table || !seq_lens || !out)
+    return set_err(IDX_EINVAL, "indexer_decode: NULL array argument");
+  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
+    return set_err(IDX_EINVAL, "indexer_decode: q, kv_pages and out must be 16-byte aligned");
+  if (query_len < 1 || query_len > 8)
+    return set_err(IDX_EUNSUPPORTED, "indexer_decode: query_len=%d, supported 1..8", query_len);
+  if (query_len > plan->max_query_len)
+    return set_err(IDX_ENOSPACE, "indexer_decode: query_len=%d > plan max %d", query_len, plan->max_query_len);
+  if (num_reqs < 1 || num_reqs > plan->max_reqs)
+    return set_err(IDX_ENOSPACE, "indexer_decode: num_reqs=%d outside 1..%d", num_reqs, plan->max_reqs);
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "indexer_decode: num_blocks=%d", num_blocks);
+  if (pt_stride < 1 || pt_stride > plan->max_pages)
+    return set_err(IDX_ENOSPACE, "indexer_decode: pt_stride=%d outside 1..%d", pt_stride, plan->max_pages);
+  if (scores_dbg && dbg_stride < pt_stride)
+    return set_err(IDX_EINVAL, "indexer_decode: dbg_stride=%d < pt_stride=%d", dbg_stride, pt_stride);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != plan->device)
+    return set_err(IDX_EINVAL, "indexer_decode: current device %d, plan made on %d", dev, plan->device);
+
+  DecodeParams p{};
+  p.q = q;
+  p.kv = kv_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.scores_dbg = scores_dbg;
+  p.cand = plan->cand;
+  p.slot_bad = plan->slot_bad;
+  p.req_info = plan->req_info;
+  p.status = plan->status;
+  p.num_blocks = num_blocks;
+  p.pt_stride = pt_stride;
+  p.num_reqs = num_reqs;
+  p.qlen = query_len;
+  p.H = plan->num_heads;
+  p.R = query_len * plan->num_heads;
+  p.dbg_stride = dbg_stride;
+  cudaError_t e = launch_decode(p, plan->decode_grid, stream);
+  if (e != cudaSuccess) return cuda_err(e, "indexer_decode: launch");
+  return IDX_OK;
+}
+
+int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seqlens_q, int num_reqs,
+                    int total_q, int max_seqlen_q, const uint8_t* kv_pages, int num_blocks,
+                    const int32_t* page_table, int pt_stride, const int32_t* seq_lens, int32_t* out,
+                    float* scores_dbg, int dbg_stride, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "indexer_prefill: plan is NULL");
+  if (!q || !cu_seqlens_q || !kv_pages || !page_table || !seq_lens || !out)
+    return set_err(IDX_EINVAL, "indexer_prefill: NULL array argument");
+  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
+    return set_err(IDX_EINVAL, "indexer_prefill: q, kv_pages and out must be 16-byte aligned");
+  if (num_reqs < 1 || num_reqs > plan->max_prefill_reqs)
+    return set_err(IDX_ENOSPACE, "indexer_prefill: num_reqs=%d outside 1..%d", num_reqs, plan->max_prefill_reqs);
+  if (total_q < 0 || total_q > plan->max_prefill_tokens)
+    return set_err(IDX_ENOSPACE, "indexer_prefill: total_q=%d outside 0..%d", total_q, plan->max_prefill_tokens);
+  if (max_seqlen_q < 0 || max_seqlen_q > total_q)
+    return set_err(IDX_EINVAL, "indexer_prefill: max_seqlen_q=%d outside 0..total_q", max_seqlen_q);
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "indexer_prefill: num_blocks=%d", num_blocks);
+  if (pt_stride < 1 || pt_stride > plan->max_pages)
+    return set_err(IDX_ENOSPACE, "indexer_prefill: pt_stride=%d outside 1..%d", pt_stride, plan->max_pages);
+  if (scores_dbg && dbg_stride < pt_stride)
+    return set_err(IDX_EINVAL, "indexer_prefill: dbg_stride=%d < pt_stride=%d", dbg_stride, pt_stride);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != plan->device)
+    return set_err(IDX_EINVAL, "indexer_prefill: current device %d, plan made on %d", dev, plan->device);
+  if (total_q == 0) return IDX_OK;
+
+  PrefillParams p{};
+  p.q = q;
+  p.kv = kv_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.out = out;
+  p.scores_dbg = scores_dbg;
+  p.status = plan->status;
+  p.num_blocks = num_blocks;
+  p.pt_stride = pt_stride;
+  p.num_reqs = num_reqs;
+  p.total_q = total_q;
+  p.H = plan->num_heads;
+  p.dbg_stride = dbg_stride;
+  const int tq = 128 / plan->num_heads;
+  const int64_t tiles_bound = (int64_t)total_q / tq + num_reqs;
+  int grid = 2 * plan->num_sms;
+  if (tiles_bound < grid) grid = (int)tiles_bound;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch_prefill(p, grid, stream);
+  if (e != cudaSuccess) return cuda_err(e, "indexer_prefill: launch");
+  return IDX_OK;
+}
+
+int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* kv_pages,
+                 int num_blocks, int32_t* status, cudaStream_t stream) {
+  g_last_error.clear();
+  if (n < 0) return set_err(IDX_EINVAL, "nvfp4_insert: n=%d", n);
+  if (n == 0) return IDX_OK;
+  if (!k_bf16 || !slot_mapping || !kv_pages)
+    return set_err(IDX_EINVAL, "nvfp4_insert: NULL array argument");
+  if (!aligned16(k_bf16) || !aligned16(kv_pages) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return set_err(IDX_EINVAL, "nvfp4_insert: k_bf16 and kv_pages must be 16-byte aligned, slot_mapping 8");
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "nvfp4_insert: num_blocks=%d", num_blocks);
+  cudaError_t e = launch_insert(k_bf16, slot_mapping, n, kv_pages, num_blocks, status, stream);
+  if (e != cudaSuccess) return cuda_err(e, "nvfp4_insert: launch");
+  return IDX_OK;
+}
+
+int indexer_get_status(indexer_plan_t plan, cudaStream_t stream, int32_t* bits) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "indexer_get_status: plan is NULL");
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, plan->status, sizeof(v), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(plan->status, 0, sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_err(e, "indexer_get_status");
+  if (bits) *bits = v;
+  if (v != 0) return set_err(IDX_EDEVICE, "device status bits 0x%x", v);
+  return IDX_OK;
+}
+
+}  // extern "C"

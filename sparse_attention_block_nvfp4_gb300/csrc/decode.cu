@@ -1,0 +1,465 @@
+// decode.cu -- decode indexer: page scores on the tensor cores + fused top-15.
+//
+// Follows MiniMaxM3IndexerNvfp4Impl.forward (decode branch) of
+// vllm.models.minimax_m3.nvidia.indexer_nvfp4: each request's 1..8 queries are
+// read in place, every history page of the request is read ONCE for all of
+// its queries and heads, and the top-k goes straight into the output buffer.
+//
+// Work split.  The history pages of all requests (page j < (seq_len-1)/128 of
+// request r) form one list of T pages; CTA c of G takes the contiguous range
+// [c*T/G, (c+1)*T/G).  A CTA walks its range as segments (one per request it
+// touches).  Per page:
+//   * the TMA unit copies the 9216-byte page into a shared-memory stage
+//     (cp.async.bulk, 7-stage ring, mbarrier completion);
+//   * thread t (of 128) reads token t's 72-byte row and dequantises it exactly
+//     to fp16 in registers (E2M1 x E4M3 fits fp16), then stores it into its
+//     own tensor-memory lane (tcgen05.st): the page becomes the MMA's A
+//     operand in tensor memory, M = 128 tokens, K = 128;
+//   * one thread issues 8 tcgen05.mma (K = 16 each) against the request's
+//     queries, B = [NQ rows x 128] fp16 in shared memory (E4M3 widened
+//     exactly), accumulating D[token][row] in fp32 in tensor memory;
+//   * the epilogue of the previous page (overlapping this page's MMA) loads
+//     D, reduces max over the 128 token lanes (butterfly across the warp,
+//     then across the 4 warps through shared memory) and inserts the page's
+//     score into the row's running top-15 (thread = row).
+// A request covered by one CTA is finalised in place; otherwise each segment
+// leaves its 15 candidates per row in scratch and decode_merge_kernel merges
+// them (and writes the rows of requests with no history page).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "codec.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace nvfp4idx {
+
+constexpr int kDecStages = 7;
+constexpr int kDecThreads = 128;
+constexpr uint32_t kDecTmemCols = 256;   // A0 [0,64) A1 [64,128) D0 [128,192) D1 [192,256)
+
+template <int NQ>
+struct DecLayout {
+  static constexpr uint32_t kQBytes = NQ * 256;                   // fp16 [2][NQ][64], SW128
+  static constexpr uint32_t kStageOff = kQBytes;                   // multiple of 1024
+  static constexpr uint32_t kRedOff = kStageOff + kDecStages * kPageBytes;
+  static constexpr uint32_t kPreOff = kRedOff + 4 * NQ * 4;
+  // at least 80 KB so that no more than two CTAs share an SM: each holds 256
+  // of the SM's 512 tensor-memory columns
+  static size_t bytes(int num_reqs) {
+    const size_t b = 1024 + kPreOff + (size_t)(num_reqs + 1) * 4;
+    return b < 80 * 1024 ? 80 * 1024 : b;
+  }
+};
+
+__device__ __forceinline__ int hist_pages(int seq_len, int pt_stride) {
+  const int h = seq_len >= 1 ? (seq_len - 1) >> 7 : 0;
+  return h > pt_stride ? 0 : h;   // a history wider than the table is finalised as bad by the merge
+}
+
+// CTA owning global page x when T pages are split over G CTAs.
+__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
+  return (int)(((x + 1) * G - 1) / T);
+}
+
+// Butterfly reduce-scatter of per-lane row vectors: after it, lane l holds
+// in v[0 .. NQ/32-1] the max over the warp's 32 lanes of columns
+// l*NQ/32 + i (NQ >= 32), or of column l/2 (NQ == 16).
+template <int NQ>
+__device__ __forceinline__ void warp_colmax(float (&v)[NQ], int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int off = 16 >> lvl;
+    const int cnt = NQ >> (lvl + 1);
+    if (cnt >= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < cnt; ++i) {
+        const float send = upper ? v[i] : v[i + cnt];
+        const float keep = upper ? v[i + cnt] : v[i];
+        v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+      }
+    } else {
+      v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+    }
+  }
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const DecodeParams p) {
+  using Lay = DecLayout<NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kDecStages];
+  __shared__ __align__(8) uint64_t mma_bar[2];
+  __shared__ int stage_bad[kDecStages];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  __shared__ int warp_sum[4];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* const base = smem_raw + (sbase - raw_u32);
+  float* const red = reinterpret_cast<float*>(base + Lay::kRedOff);
+  int32_t* const pre = reinterpret_cast<int32_t*>(base + Lay::kPreOff);
+
+  const int NR = p.num_reqs, R = p.R, G = gridDim.x, c = blockIdx.x;
+
+  // ---- 1. history pages per request -> exclusive prefix sums in smem
+  {
+    const int per = (NR + kDecThreads - 1) / kDecThreads;
+    const int r0 = tid * per, r1 = min(NR, r0 + per);
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) sum += hist_pages(__ldg(p.seq_lens + r), p.pt_stride);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int off = 0;
+    for (int w = 0; w < warp; ++w) off += warp_sum[w];
+    int run = off + incl - sum;
+    for (int r = r0; r < r1; ++r) {
+      pre[r] = run;
+      run += hist_pages(__ldg(p.seq_lens + r), p.pt_stride);
+    }
+    if (tid == kDecThreads - 1) pre[NR] = off + incl;
+    __syncthreads();
+  }
+  const int64_t T = pre[NR];
+  if (c == 0) {
+    for (int r = tid; r < NR; r += kDecThreads) {
+      const int h = pre[r + 1] - pre[r];
+      int2 info = make_int2(0, 0);
+      if (h > 0) {
+        const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+        info = make_int2(cf, cl - cf + 1);
+      }
+      p.req_info[r] = info;
+    }
+  }
+  const int64_t x0 = (int64_t)c * T / G, x1 = (int64_t)(c + 1) * T / G;
+  if (x0 >= x1) return;
+  const int64_t n = x1 - x0;
+
+  // ---- 2. tensor memory, barriers
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base_s), kDecTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kDecStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    mbar_init(smem_u32(&mma_bar[0]), 1);
+    mbar_init(smem_u32(&mma_bar[1]), 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  // first request of the range: largest r with pre[r] <= x0 and a history page
+  int r_start = 0;
+  {
+    int lo = 0, hi = NR - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= x0) lo = mid; else hi = mid - 1;
+    }
+    r_start = lo;
+    while (pre[r_start + 1] - pre[r_start] == 0) ++r_start;   // x0 < T, so this stops
+  }
+
+  // ---- producer state (thread 0)
+  int pr = r_start, pj = (int)(x0 - pre[r_start]);
+  int64_t issued = 0;
+  auto produce = [&]() {
+    const int stage = (int)(issued % kDecStages);
+    const uint32_t fb = smem_u32(&full_bar[stage]);
+    const int phys = __ldg(p.page_table + (int64_t)pr * p.pt_stride + pj);
+    if (phys < 0 || phys >= p.num_blocks) {
+      stage_bad[stage] = 1;
+      atomicOr(p.status, kStatusBadPage);
+      mbar_arrive(fb);
+    } else {
+      stage_bad[stage] = 0;
+      mbar_arrive_expect_tx(fb, kPageBytes);
+      bulk_g2s(sbase + Lay::kStageOff + stage * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+               kPageBytes, fb);
+    }
+    ++issued;
+    ++pj;
+    while (pr < NR && pj >= pre[pr + 1] - pre[pr]) { ++pr; pj = 0; }
+  };
+  if (tid == 0) {
+    const int64_t first = n < kDecStages ? n : kDecStages;
+    for (int64_t g = 0; g < first; ++g) produce();
+  }
+
+  constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
+  bool ok = true;
+  auto fail = [&]() {
+    if (ok) {
+      ok = false;
+      abort_s = 1;
+      atomicOr(p.status, kStatusTimeout);
+    }
+  };
+
+  TopK15 top;
+  int64_t g = 0;            // pages consumed by this CTA
+  int64_t mma_issued = 0;   // tcgen05.commit count (thread 0)
+  int r = r_start;
+  int j = (int)(x0 - pre[r_start]);
+
+  // epilogue of page `jp` consumed at step `gp`
+  int seq_r = 0;
+  auto epilogue = [&](int64_t gp, int jp) {
+    const int b = (int)(gp & 1);
+    if (ok && !abort_s) {
+      if (!mbar_wait(smem_u32(&mma_bar[b]), (uint32_t)((gp >> 1) & 1))) fail();
+    }
+    tc_fence_after();
+    float v[NQ];
+    tmem_ld_row<NQ>(tbase + lane_base + 128 + b * 64, v);
+    tmem_wait_ld();
+    tc_fence_before();
+    warp_colmax<NQ>(v, lane);
+    if constexpr (NQ >= 32) {
+#pragma unroll
+      for (int i = 0; i < NQ / 32; ++i) red[warp * NQ + lane * (NQ / 32) + i] = v[i];
+    } else {
+      if ((lane & 1) == 0) red[warp * NQ + (lane >> 1)] = v[0];
+    }
+    named_bar_sync(1, kDecThreads);
+    if (tid < R) {
+      const float s = canon_zero(fmaxf(fmaxf(red[tid], red[NQ + tid]),
+                                       fmaxf(red[2 * NQ + tid], red[3 * NQ + tid])));
+      const int pos = seq_r - p.qlen + tid / p.H;
+      const int L = pos >= 0 ? (pos >> 7) : -1;
+      if (jp < L) {
+        top.insert(s, jp);
+        if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + tid) * p.dbg_stride + jp] = s;
+      }
+    }
+  };
+
+  while (g < n) {
+    const int hist = pre[r + 1] - pre[r];
+    const int j_end = (int)min((int64_t)hist, (int64_t)j + (n - g));
+    const int j_begin = j;
+    seq_r = __ldg(p.seq_lens + r);
+
+    // ---- segment start: the request's queries -> fp16 B operand (SW128)
+    for (int it = tid; it < NQ * 16; it += kDecThreads) {
+      const int row = it >> 4, c8 = it & 15;
+      uint4 o = make_uint4(0, 0, 0, 0);
+      if (row < R) {
+        const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.q + ((int64_t)r * R + row) * 128 + c8 * 8));
+        o.x = e4m3x2_to_f16x2(e.x & 0xFFFFu);
+        o.y = e4m3x2_to_f16x2(e.x >> 16);
+        o.z = e4m3x2_to_f16x2(e.y & 0xFFFFu);
+        o.w = e4m3x2_to_f16x2(e.y >> 16);
+      }
+      *reinterpret_cast<uint4*>(base + (c8 >> 3) * (NQ * 128) + sw128_offset(row, c8 & 7)) = o;
+    }
+    fence_proxy_async_smem();
+    top.reset();
+    int seg_bad = 0;
+
+    for (int jj = j_begin; jj < j_end; ++jj, ++g) {
+      const int stage = (int)(g % kDecStages);
+      if (ok && !abort_s) {
+        if (!mbar_wait(smem_u32(&full_bar[stage]), (uint32_t)((g / kDecStages) & 1))) fail();
+      }
+      seg_bad |= stage_bad[stage];
+      uint32_t w[18];
+      {
+        const uint2* src = reinterpret_cast<const uint2*>(base + Lay::kStageOff + stage * kPageBytes + tid * kRowBytes);
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+          const uint2 t2 = src[i];
+          w[2 * i] = t2.x;
+          w[2 * i + 1] = t2.y;
+        }
+      }
+      named_bar_sync(1, kDecThreads);                    // stage consumed by all
+      if (tid == 0 && issued < n && !abort_s) produce();
+
+      // dequantise token `tid` of the page into its tensor-memory lane
+      uint32_t a[64];
+      {
+        const uint32_t sc01 = e4m3x2_to_f16x2(w[16] & 0xFFFFu), sc23 = e4m3x2_to_f16x2(w[16] >> 16);
+        const uint32_t sc45 = e4m3x2_to_f16x2(w[17] & 0xFFFFu), sc67 = e4m3x2_to_f16x2(w[17] >> 16);
+        const uint32_t sc[4] = {sc01, sc23, sc45, sc67};
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
+          dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
+        }
+      }
+      const int b = (int)(g & 1);
+      tmem_st_32x32b_x64(tbase + lane_base + b * 64, a);
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(1, kDecThreads);                    // A operand and B operand ready
+      if (tid == 0 && !abort_s) {
+        tc_fence_after();
+        const uint32_t d_t = tbase + 128 + b * 64;
+        const uint32_t a_t = tbase + b * 64;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(sbase + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
+          mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&mma_bar[b]));
+        ++mma_issued;
+      }
+      if (jj > j_begin) epilogue(g - 1, jj - 1);
+    }
+    epilogue(g - 1, j_end - 1);
+
+    // ---- finalise the segment
+    const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+    if (tid < R) {
+      if (cf == cl) {
+        const int pos = seq_r - p.qlen + tid / p.H;
+        const int L = pos >= 0 ? (pos >> 7) : -1;
+        write_out_row(p.out + ((int64_t)r * R + tid) * kTopK, top.id, L, seg_bad != 0);
+      } else {
+        float2* dst = p.cand + ((int64_t)(c + r) * R + tid) * kHistK;
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+      }
+    }
+    if (tid == 0 && cf != cl) p.slot_bad[c + r] = seg_bad;
+
+    // next request with history pages
+    ++r;
+    while (r < NR && pre[r + 1] - pre[r] == 0) ++r;
+    j = 0;
+    named_bar_sync(1, kDecThreads);    // Q smem free for the next segment
+  }
+
+  // ---- drain after a timeout, then free tensor memory
+  __syncthreads();
+  if (tid == 0 && abort_s) {
+    for (int64_t k = (issued > kDecStages ? issued - kDecStages : 0); k < issued; ++k)
+      mbar_wait(smem_u32(&full_bar[k % kDecStages]), (uint32_t)((k / kDecStages) & 1));
+    for (int64_t k = (mma_issued > 2 ? mma_issued - 2 : 0); k < mma_issued; ++k)
+      mbar_wait(smem_u32(&mma_bar[k & 1]), (uint32_t)((k >> 1) & 1));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, kDecTmemCols);
+}
+
+// One warp per (request, row): merge the per-segment top-15 lists of split
+// requests; write rows of requests with no history page or an unreadable one.
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  __shared__ float2 lists[8][32][kHistK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * 8 + warp;
+  if (gw >= (int64_t)p.num_reqs * p.R) return;
+  const int r = (int)(gw / p.R), n = (int)(gw % p.R);
+  const int seq = __ldg(p.seq_lens + r);
+  const int pos = seq - p.qlen + n / p.H;
+  const int L = pos >= 0 ? (pos >> 7) : -1;
+  const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
+  int32_t* out_row = p.out + gw * kTopK;
+  const int none[1] = {-1};
+  if (hist > p.pt_stride) {
+    if (lane == 0) {
+      write_out_row(out_row, none, L, true);
+      atomicOr(p.status, kStatusBadTable);
+    }
+    return;
+  }
+  const int2 info = p.req_info[r];
+  const int nseg = info.y;
+  if (nseg == 1) return;                      // finalised by the scoring kernel
+  if (nseg == 0) {                            // no history page: local page only
+    if (lane == 0) write_out_row(out_row, none, L, false);
+    return;
+  }
+  const int slot0 = info.x + r;
+  int bad = 0;
+  for (int k = lane; k < nseg; k += 32) bad |= p.slot_bad[slot0 + k];
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) write_out_row(out_row, none, L, true);
+    return;
+  }
+  // lane-local sorted list: list `lane` when nseg <= 32, else a top-15 of
+  // lists lane, lane+32, ... (visited in ascending page order)
+  float2(&mine)[kHistK] = lists[warp][lane];
+  if (nseg <= 32) {
+    if (lane < nseg) {
+      const float2* src = p.cand + ((int64_t)(slot0 + lane) * p.R + n) * kHistK;
+#pragma unroll
+      for (int k = 0; k < kHistK; ++k) mine[k] = src[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(0.0f, __int_as_float(-1));
+    }
+  } else {
+    TopK15 t;
+    t.reset();
+    for (int k = lane; k < nseg; k += 32) {
+      const float2* src = p.cand + ((int64_t)(slot0 + k) * p.R + n) * kHistK;
+      float2 e[kHistK];
+#pragma unroll
+      for (int i = 0; i < kHistK; ++i) e[i] = src[i];
+#pragma unroll
+      for (int i = 0; i < kHistK; ++i)
+        if (__float_as_int(e[i].y) >= 0) t.insert(e[i].x, __float_as_int(e[i].y));
+    }
+#pragma unroll
+    for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(t.s[k], __int_as_float(t.id[k]));
+  }
+  __syncwarp();
+  int res[kHistK];
+  int cur = 0;
+#pragma unroll
+  for (int k = 0; k < kHistK; ++k) {
+    float2 e = make_float2(0.0f, __int_as_float(-1));
+    if (cur < kHistK) e = lists[warp][lane][cur];
+    const int id = __float_as_int(e.y);
+    const uint32_t key = id >= 0 ? order_key(e.x) : 0u;
+    const uint32_t kmax = warp_max_u32(key);
+    const uint32_t idmin = warp_min_u32(key == kmax && kmax != 0u ? (uint32_t)id : 0xFFFFFFFFu);
+    if (kmax != 0u && key == kmax && (uint32_t)id == idmin) ++cur;
+    res[k] = kmax != 0u ? (int)idmin : -1;
+  }
+  if (lane == 0) write_out_row(out_row, res, L, false);
+}
+
+template <int NQ>
+static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = DecLayout<NQ>::bytes(p.num_reqs);
+  cudaError_t e = cudaFuncSetAttribute(decode_score_kernel<NQ>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_score_kernel<NQ><<<grid, kDecThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t warps = (int64_t)p.num_reqs * p.R;
+  decode_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
+  switch (decode_nq(p.R)) {
+    case 16: return launch_decode_nq<16>(p, grid, stream);
+    case 32: return launch_decode_nq<32>(p, grid, stream);
+    default: return launch_decode_nq<64>(p, grid, stream);
+  }
+}
+
+}  // namespace nvfp4idx

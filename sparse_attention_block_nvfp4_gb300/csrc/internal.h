@@ -1,0 +1,57 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4idx {
+
+constexpr int kPage = 128;        // tokens per page
+constexpr int kDim = 128;         // index head dim
+constexpr int kRowBytes = 72;     // 64 B codes + 8 B scales
+constexpr int kPageBytes = kPage * kRowBytes;   // 9216
+constexpr int kTopK = 16;
+constexpr int kHistK = 15;        // score-ranked history pages per row
+constexpr int kMaxRows = 64;      // query_len (<= 8) x heads (<= 8) per request
+constexpr int kMaxDecodeReqs = 4096;
+
+// device status bits (mirror IDX_STATUS_* in include/nvfp4_indexer.h)
+constexpr int32_t kStatusBadPage = 1;
+constexpr int32_t kStatusBadTable = 2;
+constexpr int32_t kStatusTimeout = 4;
+constexpr int32_t kStatusBadSlot = 8;
+
+struct DecodeParams {
+  const uint8_t* q;            // [num_reqs * qlen][H][128] e4m3
+  const uint8_t* kv;           // [num_blocks][128][72]
+  const int32_t* page_table;   // [num_reqs][pt_stride]
+  const int32_t* seq_lens;     // [num_reqs]
+  int32_t* out;                // [rows][H][16]
+  float* scores_dbg;           // nullable
+  float2* cand;                // [(grid + num_reqs) slots][R][15] (score, id bits)
+  int32_t* slot_bad;           // [(grid + num_reqs)]
+  int2* req_info;              // [num_reqs] (first CTA, number of segments)
+  int32_t* status;
+  int num_blocks, pt_stride, num_reqs, qlen, H, R, dbg_stride;
+};
+
+struct PrefillParams {
+  const uint8_t* q;            // [total_q][H][128]
+  const uint8_t* kv;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* cu_seqlens_q; // [num_reqs + 1]
+  int32_t* out;                // [total_q][H][16]
+  float* scores_dbg;
+  int32_t* status;
+  int num_blocks, pt_stride, num_reqs, total_q, H, dbg_stride;
+};
+
+cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
+                          int num_blocks, int32_t* status, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream);
+
+// smallest power-of-two >= 16 that holds R rows (the MMA N dimension)
+inline int decode_nq(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
+
+}  // namespace nvfp4idx

@@ -1,0 +1,87 @@
+// topk.cuh -- per-row running top-15 in registers, and the ordering helpers.
+//
+// Selection rule (vllm.models.minimax_m3.nvidia.indexer_nvfp4, module
+// description: 15 score-ranked history pages, local page last): pages ranked
+// by score, descending; equal scores rank the lower page id first.  Callers
+// feed pages in ascending id order, so "strictly greater" comparisons give
+// exactly that total order.
+#pragma once
+#include <cstdint>
+#include <math_constants.h>
+
+namespace nvfp4idx {
+
+struct TopK15 {
+  float s[15];
+  int id[15];
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < 15; ++i) {
+      s[i] = -CUDART_INF_F;
+      id[i] = -1;
+    }
+  }
+
+  // Insert (v, j); j must exceed every id inserted before with the same score.
+  __device__ __forceinline__ void insert(float v, int j) {
+    if (v > s[14]) {
+      s[14] = v;
+      id[14] = j;
+#pragma unroll
+      for (int i = 14; i > 0; --i) {
+        const bool up = s[i] > s[i - 1];
+        const float ts = s[i], tu = s[i - 1];
+        const int ti = id[i], tj = id[i - 1];
+        s[i - 1] = up ? ts : tu;
+        s[i] = up ? tu : ts;
+        id[i - 1] = up ? ti : tj;
+        id[i] = up ? tj : ti;
+      }
+    }
+  }
+};
+
+// -0.0 -> +0.0 so that equal scores compare equal in the integer key below.
+__device__ __forceinline__ float canon_zero(float v) { return v + 0.0f; }
+
+// Monotone map of finite floats (and -inf) to unsigned keys; 0 = "none".
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// Write one output row: m = min(15, L) ranked ids, then L, then -1.
+// L < 0 or `bad` -> all -1.
+__device__ __forceinline__ void write_out_row(int32_t* row, const int* ids, int L, bool bad) {
+  int v[16];
+  const int m = L < 15 ? L : 15;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    int x = -1;
+    if (!bad && L >= 0) {
+      if (k < m) x = ids[k];
+      else if (k == m) x = L;
+    }
+    v[k] = x;
+  }
+  int4* o = reinterpret_cast<int4*>(row);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) o[k] = make_int4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+
+}  // namespace nvfp4idx
