@@ -1,0 +1,531 @@
+"""Benchmark of the NVFP4 lightning indexer step on GB300.
+
+One step = the whole hot path over one batch: NVFP4 insert of the step's new
+keys, the decode indexer over every decode request, the prefill indexer over
+every prefill chunk.  Default workload: the long-context mixed step (16
+decode requests at a 131072-token context with 8 queries each, plus 2 prefill
+chunks of 8192 new tokens on 65536-token histories, 8 index heads), the only
+named configuration that runs every step of the path; the cache holds all
+2.24 M keys, written once before timing.
+
+Metric: indexer pages scored per second = sum over (query row, head) of the
+history pages scored, per second of step time.  Timing: CUDA events on the
+launching stream around each step (and around each kernel, for the roofline),
+L2 flushed (a 2 x L2 write) between steps, W warm-up steps first.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--sweep]
+
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own full
+batch (weak scaling, no data-path collective); value = all ranks' pages /
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_INDEX = {"tiny_decode": 0, "decode_batch": 1, "spec_decode": 2, "ragged_prefill": 3, "long_mixed": 4}
+KERNEL_SOURCES = ["csrc/prefill.cu", "csrc/decode.cu", "csrc/insert.cu", "csrc/ptx.cuh", "csrc/codec.cuh",
+                  "csrc/topk.cuh", "csrc/internal.h"]
+
+
+# ----------------------------------------------------------------------------- host-side logic
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "sparse_attention_block_nvfp4_gb300", rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == cur:
+            return float(parts[3])
+    return None
+
+
+def work_counts(w: workloads.Workload) -> dict:
+    """Algorithmic work of one step (history pages only; the local page is not scored)."""
+    H = w.num_heads
+    out = {}
+    # decode
+    seq = w.dec_seq_lens.astype(np.int64)
+    ql = w.query_len
+    if w.num_decode_reqs:
+        pos = seq[:, None] - ql + np.arange(ql)[None, :]
+        hist_rows = np.where(pos >= 0, pos // 128, 0)                  # pages per (row)
+        req_pages = np.where(seq >= 1, (seq - 1) // 128, 0)           # pages read per request
+        R = ql * H
+        out["dec_pages_scored"] = int(hist_rows.sum()) * H
+        out["dec_bytes"] = int(req_pages.sum()) * (9216 + 4) + w.num_decode_reqs * (R * 128 + R * 64 + 4)
+        out["dec_flops"] = int(req_pages.sum()) * 2 * 128 * 128 * R
+    else:
+        out.update(dec_pages_scored=0, dec_bytes=0, dec_flops=0)
+    # prefill
+    if w.num_prefill_reqs:
+        tot = 0
+        for s, q in zip(w.pre_seq_lens.astype(np.int64), w.pre_query_lens.astype(np.int64)):
+            pos = s - q + np.arange(q)
+            tot += int(np.where(pos >= 0, pos // 128, 0).sum())
+        out["pre_pages_scored"] = tot * H
+        out["pre_flops"] = tot * H * 2 * 128 * 128
+    else:
+        out.update(pre_pages_scored=0, pre_flops=0)
+    out["pages_scored"] = out["dec_pages_scored"] + out["pre_pages_scored"]
+    return out
+
+
+def step_new_tokens(w: workloads.Workload) -> np.ndarray:
+    """Indices (into w.k_bf16) of the keys a step inserts: the decode queries'
+    own tokens and the prefill chunks' new tokens (the rest is history)."""
+    seq = w.seq_lens.astype(np.int64)
+    start = np.concatenate([[0], np.cumsum(np.maximum(seq, 0))])
+    idx = []
+    for r in range(w.num_decode_reqs):
+        idx.append(np.arange(start[r + 1] - min(w.query_len, seq[r]), start[r + 1]))
+    for k in range(w.num_prefill_reqs):
+        r = w.num_decode_reqs + k
+        idx.append(np.arange(start[r + 1] - w.pre_query_lens[k], start[r + 1]))
+    return np.concatenate(idx) if idx else np.zeros(0, np.int64)
+
+
+def aggregate(per_rank_pages, per_rank_seconds) -> float:
+    """Whole-job throughput: all ranks' work over the slowest rank's time."""
+    return float(sum(per_rank_pages)) / float(max(per_rank_seconds))
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (all ranks get it); identity for one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 100 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class GpuStep:
+    """Device-resident inputs of one workload and the three library calls."""
+
+    def __init__(self, w, device):
+        import torch
+        import sparse_attention_block_nvfp4_gb300 as idx
+        self.idx, self.torch, self.w, self.dev = idx, torch, w, device
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.kv = torch.zeros((w.num_blocks, 128, 72), dtype=torch.uint8, device=device)
+        # the history: every cached key inserted once, outside the timed region
+        idx.insert(up(w.k_bf16.view(np.int16)), up(w.slot_mapping), self.kv)
+        new = step_new_tokens(w)
+        self.h_k_new = w.k_bf16[new].view(np.int16)
+        self.h_slot_new = w.slot_mapping[new]
+        self.k_new, self.slot_new = up(self.h_k_new), up(self.h_slot_new)
+        self.plan = idx.Plan(num_heads=w.num_heads, max_reqs=max(1, w.num_decode_reqs),
+                             max_query_len=max(1, w.query_len), max_pages_per_req=w.page_table.shape[1],
+                             max_prefill_tokens=max(1, w.total_prefill_q),
+                             max_prefill_reqs=max(1, w.num_prefill_reqs))
+        self.h = dict(q_dec=w.q_decode, q_pre=w.q_prefill, dec_table=w.dec_page_table,
+                      pre_table=w.pre_page_table, dec_seq=w.dec_seq_lens, pre_seq=w.pre_seq_lens,
+                      cu=w.cu_seqlens_q)
+        self.d = {k: up(v) for k, v in self.h.items()}
+        rows = w.num_decode_rows + w.total_prefill_q
+        self.out = torch.empty((rows, w.num_heads, 16), dtype=torch.int32, device=device)
+        self.nd = w.num_decode_rows
+        self.max_q = int(w.pre_query_lens.max()) if w.num_prefill_reqs else 0
+        self.launches_per_step = (1 if len(new) else 0) + (2 if w.num_decode_reqs else 0) + \
+            (1 if w.num_prefill_reqs else 0)
+
+    def run(self, stream, d=None, events=None, k_new=None, slot_new=None):
+        """Enqueue one step; events: dict name -> (start, end) recorded around each kernel."""
+        d = d or self.d
+        k_new = self.k_new if k_new is None else k_new
+        slot_new = self.slot_new if slot_new is None else slot_new
+        w = self.w
+
+        def rec(name, i):
+            if events is not None:
+                events[name][i].record(stream)
+        if k_new.shape[0]:
+            rec("insert", 0)
+            self.idx.insert(k_new, slot_new, self.kv, stream=stream)
+            rec("insert", 1)
+        if w.num_decode_reqs:
+            rec("decode", 0)
+            self.plan.decode(d["q_dec"], self.kv, d["dec_table"], d["dec_seq"], w.query_len,
+                             out=self.out[: self.nd], stream=stream)
+            rec("decode", 1)
+        if w.num_prefill_reqs:
+            rec("prefill", 0)
+            self.plan.prefill(d["q_pre"], d["cu"], self.kv, d["pre_table"], d["pre_seq"], self.max_q,
+                              out=self.out[self.nd:], stream=stream)
+            rec("prefill", 1)
+
+
+def gpu_arm(args, w, rank, world, local):
+    import torch
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    st = GpuStep(w, dev)
+    work = work_counts(w)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) if args.flush else 1, dtype=torch.uint8, device=dev)
+    names = ["insert", "decode", "prefill"]
+
+    def new_events():
+        return {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        st.run(stream)
+    torch.cuda.synchronize()
+    if st.plan.status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+    step_ev, kern_ev = [], []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1)                                   # L2 flush between timed steps
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev = new_events()
+            s0.record(stream)
+            st.run(stream, events=ev)
+            s1.record(stream)
+            step_ev.append((s0, s1))
+            kern_ev.append(ev)
+        torch.cuda.synchronize()
+    if world > 1:
+        tdist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    ran = {"insert": st.k_new.shape[0] > 0, "decode": w.num_decode_reqs > 0, "prefill": w.num_prefill_reqs > 0}
+    kern_ms = {n: [e[n][0].elapsed_time(e[n][1]) for e in kern_ev] for n in names if ran[n]}
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    status = st.plan.status()
+
+    # ---- end to end: host buffers in, ids out, through the same C ABI calls
+    e2e = None
+    if args.e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        hin = {k: pin(v) for k, v in st.h.items()}
+        hk, hs = pin(st.h_k_new), pin(st.h_slot_new)
+        dbuf = {k: torch.empty_like(v) for k, v in st.d.items()}
+        dk, ds = torch.empty_like(st.k_new), torch.empty_like(st.slot_new)
+        hout = torch.empty(st.out.shape, dtype=torch.int32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in hin.values()) + hk.numel() * 2 + hs.numel() * 8
+        d2h = hout.numel() * 4
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in hin:
+                dbuf[k].copy_(hin[k], non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+            st.run(stream, d=dbuf, k_new=dk, slot_new=ds)
+            hout.copy_(st.out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                times.append(a.elapsed_time(b))
+        e2e_s = max_over_ranks(sum(times) / 1e3, world, dev)
+        e2e = {"value": work["pages_scored"] * args.steps * world / e2e_s, "unit": "pages/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    return dict(st=st, work=work, step_ms=step_ms, kern_ms=kern_ms, total_s=total_s, clk=clk.summary(),
+                e2e=e2e, status=status)
+
+
+def roofline_block(res, w, wname, peaks, peak_kind):
+    work, km = res["work"], res["kern_ms"]
+    avg = {n: (sum(v) / len(v) if v else 0.0) for n, v in km.items()}
+    avg = {n: avg.get(n, 0.0) for n in ("insert", "decode", "prefill")}
+    n_new = res["st"].k_new.shape[0]
+    kernels = {}
+    if avg.get("prefill"):
+        tf = work["pre_flops"] / (avg["prefill"] / 1e3) / 1e12
+        kernels["prefill"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                              "frac": tf / peaks["bf16_tflops"], "ms": avg["prefill"],
+                              "traffic": recorded_traffic("prefill", wname)}
+    if avg.get("decode"):
+        gb = work["dec_bytes"] / (avg["decode"] / 1e3) / 1e9
+        kernels["decode"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gb / peaks["hbm_gbs"], "ms": avg["decode"],
+                             "tensor_tflops": work["dec_flops"] / (avg["decode"] / 1e3) / 1e12,
+                             "traffic": recorded_traffic("decode", wname)}
+    if avg.get("insert"):
+        gb = n_new * (256 + 8 + 72) / (avg["insert"] / 1e3) / 1e9
+        kernels["insert"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gb / peaks["hbm_gbs"], "ms": avg["insert"],
+                             "traffic": recorded_traffic("insert", wname)}
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    rl = dict(kernels[dom])
+    rl.pop("ms", None)
+    rl.pop("tensor_tflops", None)
+    rl["kernel"] = dom
+    rl["peak_source"] = f"{peak_kind} ({'bf16 dense burst; fp16 has the same dense rate' if rl['unit'] == 'TFLOP/s' else 'copy bandwidth'})"
+    return rl, kernels
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(w, budget_s: float, rng_seed: int = 0):
+    """Time the CPU oracle on a bounded sample of the workload's step: the
+    step's new keys of the sampled requests quantised, then a sample of decode
+    and prefill rows scored and selected.  Returns (pages_scored, seconds, text)."""
+    from oracle import indexer as oidx, nvfp4 as onvfp4
+    rng = np.random.Generator(np.random.PCG64(rng_seed))
+    seq = w.seq_lens.astype(np.int64)
+    start = np.concatenate([[0], np.cumsum(np.maximum(seq, 0))])
+    pages, secs, parts = 0, 0.0, []
+    kv = np.zeros((w.num_blocks, 128, 72), np.uint8)
+    # history of the sampled requests (resident cache: not timed)
+    dr = [int(rng.integers(w.num_decode_reqs))] if w.num_decode_reqs else []
+    pr = [int(rng.integers(w.num_prefill_reqs))] if w.num_prefill_reqs else []
+    for r in dr + [w.num_decode_reqs + k for k in pr]:
+        a, b = int(start[r]), int(start[r + 1])
+        onvfp4.insert(w.k_bf16[a:b], w.slot_mapping[a:b], kv)
+    H = w.num_heads
+    t_end = time.perf_counter() + budget_s
+    while time.perf_counter() < t_end:
+        if dr:
+            r = dr[0]
+            rows = np.arange(r * w.query_len, (r + 1) * w.query_len)
+            t0 = time.perf_counter()
+            a = int(start[r + 1]) - w.query_len
+            onvfp4.insert(w.k_bf16[a:int(start[r + 1])], w.slot_mapping[a:int(start[r + 1])], kv)
+            res = oidx.decode(w.q_decode, kv, w.dec_page_table, w.dec_seq_lens, w.query_len, H, rows=rows)
+            secs += time.perf_counter() - t0
+            pages += int(np.nansum(~np.isnan(res.S)))
+            parts.append(f"decode request {r}: {len(rows)} rows x {H} heads")
+        if pr and time.perf_counter() < t_end:
+            k = pr[0]
+            cu = w.cu_seqlens_q
+            rows = np.sort(rng.choice(np.arange(cu[k], cu[k + 1]), size=min(32, int(cu[k + 1] - cu[k])),
+                                      replace=False))
+            t0 = time.perf_counter()
+            r = w.num_decode_reqs + k
+            toks = int(start[r]) + (int(seq[r]) - int(w.pre_query_lens[k])) + (rows - cu[k])
+            onvfp4.insert(w.k_bf16[toks], w.slot_mapping[toks], kv)
+            res = oidx.prefill(w.q_prefill, cu, kv, w.pre_page_table, w.pre_seq_lens, H, rows=rows)
+            secs += time.perf_counter() - t0
+            pages += int(np.count_nonzero(~np.isnan(res.S)))
+            parts.append(f"prefill chunk {k}: {len(rows)} rows x {H} heads")
+    uniq = sorted(set(parts))
+    return pages, secs, "; ".join(uniq)
+
+
+def cpu_block(w, budget_s):
+    pages, secs, what = oracle_sample(w, budget_s)
+    return {"value": pages / secs if secs else None, "unit": "pages/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"{what}; {pages} (row, head, page) scores in {secs:.1f} s, "
+                                        f"NumPy float64, BLAS on all host cores"}
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_mixed", choices=list(WORKLOAD_INDEX))
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--sweep", action="store_true", help="one line per named workload (no e2e / cpu)")
+    ap.add_argument("--no-flush", dest="flush", action="store_false",
+                    help="skip the L2 flush (profiling runs only; the timed numbers then see a warm L2)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = workloads.config(WORKLOAD_INDEX[args.workload])
+        per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+        for _ in range(args.warmup):
+            oracle_sample(w, per_step)
+        pages, secs = 0, 0.0
+        what = ""
+        for _ in range(args.steps):
+            p, s, what = oracle_sample(w, per_step)
+            pages += p
+            secs += s
+        v = pages / secs
+        line = {"impl": "reference", "metric": "indexer pages scored/s", "value": v, "unit": "pages/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload},
+                "cpu_baseline": {"value": v, "unit": "pages/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"each step: {what}; NumPy float64 CPU oracle on the host cores"},
+                "e2e": {"value": v, "unit": "pages/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    names = list(WORKLOAD_INDEX) if args.sweep else [args.workload]
+    peaks, peak_kind = load_peaks()
+    for wname in names:
+        w = workloads.config(WORKLOAD_INDEX[wname])
+        if world > 1:
+            # weak scaling: every rank its own batch of the same shape
+            w = workloads.config(WORKLOAD_INDEX[wname]) if rank == 0 else _reseeded(wname, rank)
+        sweep_args = argparse.Namespace(**vars(args))
+        if args.sweep:
+            sweep_args.e2e = False
+        res = gpu_arm(sweep_args, w, rank, world, local)
+        work = res["work"]
+        value = work["pages_scored"] * args.steps * world / res["total_s"]
+        rl, kernels = roofline_block(res, w, wname, peaks, peak_kind)
+        line = {
+            "metric": "indexer pages scored/s", "value": value, "unit": "pages/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["total_s"] * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
+            "config": {"workload": wname, "shape": w.notes or _describe(w), "num_heads": w.num_heads,
+                       "l2": "flushed between timed steps (2 x L2 write)" if args.flush else "not flushed",
+                       "pages_scored_per_step": work["pages_scored"]},
+            "roofline": rl,
+            "kernels": kernels,
+            "gpu_launches": res["st"].launches_per_step * args.steps,
+            "clocks": res["clk"],
+            "device_status": res["status"],
+        }
+        if res["e2e"] is not None:
+            line["e2e"] = res["e2e"]
+        if rank == 0 and world == 1 and args.cpu_baseline and not args.sweep:
+            line["cpu_baseline"] = cpu_block(w, args.cpu_budget)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.destroy_process_group()
+
+
+def _describe(w):
+    parts = []
+    if w.num_decode_reqs:
+        parts.append(f"{w.num_decode_reqs} decode req, seq {int(w.dec_seq_lens.min())}..{int(w.dec_seq_lens.max())}, "
+                     f"query_len {w.query_len}")
+    if w.num_prefill_reqs:
+        parts.append(f"{w.num_prefill_reqs} prefill req, new {w.pre_query_lens.tolist()}, "
+                     f"seq {w.pre_seq_lens.tolist()}")
+    return "; ".join(parts) + f"; H={w.num_heads}, head_dim 128, 128-token NVFP4 pages"
+
+
+def _reseeded(wname, rank):
+    """The same workload shape with another seed (another rank's batch)."""
+    import workloads as wl
+    w = wl.config(WORKLOAD_INDEX[wname])
+    rng = np.random.Generator(np.random.PCG64(1000 + rank))
+    q = wl.random_q(w.q_e4m3.shape[0], w.num_heads, rng)
+    w.q_e4m3 = q
+    return w
+
+
+if __name__ == "__main__":
+    main()
