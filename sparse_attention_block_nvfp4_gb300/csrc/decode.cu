@@ -6,9 +6,9 @@
 // its queries and heads, and the top-k goes straight into the output buffer.
 //
 // Work split.  The history pages of all requests (page j < (seq_len-1)/128 of
-// request r) form one list of T pages; CTA c of G takes the contiguous range
-// [c*T/G, (c+1)*T/G).  A CTA walks its range as segments (one per request it
-// touches).  Per page:
+// request r) form one list of T pages; CTA c of G = min(grid, T) takes the
+// contiguous range [c*T/G, (c+1)*T/G), never empty.  A CTA walks its range
+// as segments (one per request it touches).  Per page:
 //   * the TMA unit copies the 9216-byte page into a shared-memory stage
 //     (cp.async.bulk, 7-stage ring, mbarrier completion);
 //   * thread t (of 128) reads token t's 72-byte row and dequantises it exactly
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
   float* const red = reinterpret_cast<float*>(base + Lay::kRedOff);
   int32_t* const pre = reinterpret_cast<int32_t*>(base + Lay::kPreOff);
 
-  const int NR = p.num_reqs, R = p.R, G = gridDim.x, c = blockIdx.x;
+  const int NR = p.num_reqs, R = p.R, c = blockIdx.x;
 
   // ---- 1. history pages per request -> exclusive prefix sums in smem
   {
@@ -131,6 +131,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
     __syncthreads();
   }
   const int64_t T = pre[NR];
+  // Split the T pages over G_eff = min(G, T) CTAs: every one of them then
+  // owns at least one page, so every CTA between a request's first and last
+  // owner holds a segment of it (and writes the slot the merge reads).
+  const int G = (int)min((int64_t)gridDim.x, T);
   if (c == 0) {
     for (int r = tid; r < NR; r += kDecThreads) {
       const int h = pre[r + 1] - pre[r];
@@ -142,8 +146,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
       p.req_info[r] = info;
     }
   }
+  if (c >= G) return;
   const int64_t x0 = (int64_t)c * T / G, x1 = (int64_t)(c + 1) * T / G;
-  if (x0 >= x1) return;
   const int64_t n = x1 - x0;
 
   // ---- 2. tensor memory, barriers

@@ -192,3 +192,22 @@ def test_decode_full_size_sampled(idx):
             o = out[t, h]
             assert o[m[t]] == L[t] and np.all(o[m[t] + 1:] == -1)
             assert len(set(o[:m[t]].tolist())) == m[t] and np.all(o[:m[t]] < L[t]) and np.all(o[:m[t]] >= 0)
+
+
+def test_decode_small_batch_after_wide_batch_same_plan():
+    """A batch with fewer history pages than CTAs, run on a plan whose scratch
+    still holds a previous, wider batch's candidates: every candidate slot the
+    merge reads must have been written by the current call."""
+    rng = np.random.Generator(np.random.PCG64(36))
+    wide = workloads.make_workload(name="wide", seed=36, rng=rng, num_heads=8,
+                                   dec_seq_lens=rng.integers(3000, 9000, size=16), query_len=8)
+    small = workloads.make_workload(name="small", seed=37, rng=np.random.Generator(np.random.PCG64(37)),
+                                    num_heads=8, dec_seq_lens=[2000, 3100, 700, 129, 4000], query_len=2)
+    import sparse_attention_block_nvfp4_gb300 as idx
+    plan = idx.Plan(num_heads=8, max_reqs=16, max_query_len=8,
+                    max_pages_per_req=max(wide.page_table.shape[1], small.page_table.shape[1]))
+    for w in (wide, small, wide, small):
+        out, _ = run_decode(plan, w, gpu_cache(w))
+        ref = oidx.decode(w.q_decode, oracle_cache(w), w.dec_page_table, w.dec_seq_lens, w.query_len, 8)
+        assert_ids(out, ref, w.name)
+    assert plan.status() == 0
