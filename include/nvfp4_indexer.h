@@ -158,6 +158,36 @@ int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seq
 int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* kv_pages,
                  int num_blocks, int32_t* status, cudaStream_t stream);
 
+/*
+ * indexer_decode_noalloc -- indexer_decode for callers that cannot allocate
+ * device memory.  (No counterpart in the source pages: an addition of this
+ * library.)
+ * Creating a plan calls cudaMalloc.  Some callers cannot do that: a custom-op
+ * hook inside a serving engine that is handed only its input and output
+ * buffers while the engine owns all device memory, or a latency-critical loop
+ * that must never call cudaMalloc, which can synchronise the device.  This
+ * call takes no plan and allocates nothing; it runs the same kernels as
+ * indexer_decode with their scratch in a fixed 4 MiB array compiled into the
+ * library (held on every device that loads the library until the process
+ * exits).
+ *   Arguments as indexer_decode, plus
+ *   num_heads  H, one of 1, 2, 4, 8
+ *   status     NULL, or a device int32 that gets IDX_STATUS_* bits OR-ed in
+ *   (no scores_dbg output)
+ * Limit: the call needs 256-byte-aligned pieces of roughly
+ * 8*num_reqs + (2*SMs + num_reqs) * (4 + 120*query_len*num_heads) bytes; a
+ * call that needs more than 4 MiB returns IDX_ENOSPACE and launches nothing
+ * (about 240 requests at query_len*num_heads = 64 on a 152-SM GPU).
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (once per device, that device current): make that
+ * first call before any stream capture.  All calls share the array, so calls
+ * whose kernels overlap on the GPU race and must be serialised by the caller.
+ */
+int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages, int num_blocks,
+                           const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
+                           int num_reqs, int query_len, int num_heads, int32_t* out,
+                           int32_t* status, cudaStream_t stream);
+
 /* Synchronise `stream`, read and clear the plan's device status word.
  * Returns IDX_OK, or IDX_EDEVICE with the IDX_STATUS_* bits in *bits. */
 int indexer_get_status(indexer_plan_t plan, cudaStream_t stream, int32_t* bits);

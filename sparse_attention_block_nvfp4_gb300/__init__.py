@@ -17,7 +17,7 @@ import os
 import re
 from typing import Optional
 
-__all__ = ["Plan", "insert", "IndexerError", "load_library", "library_path", "declared_symbols",
+__all__ = ["Plan", "insert", "decode_noalloc", "IndexerError", "load_library", "library_path", "declared_symbols",
            "STATUS_BAD_PAGE", "STATUS_BAD_TABLE", "STATUS_TIMEOUT", "STATUS_BAD_SLOT", "TOPK", "PAGE"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -196,3 +196,26 @@ def insert(k_bf16, slot_mapping, kv_pages, status=None, stream=None):
         _ptr(kv_pages, torch.uint8, "kv_pages", 3), int(kv_pages.shape[0]),
         _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
     return kv_pages
+
+
+def decode_noalloc(q, kv_pages, page_table, seq_lens, query_len: int, num_heads: int, out=None,
+                   status=None, stream=None):
+    """``indexer_decode_noalloc``: the decode indexer for callers that cannot
+    allocate device memory (no plan; scratch in a fixed array inside the
+    library).  Calls that overlap on the GPU share that array and race."""
+    import torch
+    lib = load_library()
+    fn = lib.indexer_decode_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [P, P, I, P, I, P, I, I, I, P, P, P]
+    fn.restype = I
+    num_reqs = int(seq_lens.shape[0])
+    if q.dim() != 3 or q.shape[0] != num_reqs * query_len or q.shape[1] != num_heads or q.shape[2] != 128:
+        raise ValueError(f"q: expected [{num_reqs * query_len}, {num_heads}, 128], got {tuple(q.shape)}")
+    if out is None:
+        out = torch.empty((q.shape[0], num_heads, TOPK), dtype=torch.int32, device=q.device)
+    _check(fn(_ptr(q, torch.uint8, "q"), _ptr(kv_pages, torch.uint8, "kv_pages", 3), int(kv_pages.shape[0]),
+              _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
+              _ptr(seq_lens, torch.int32, "seq_lens", 1), num_reqs, int(query_len), int(num_heads),
+              _ptr(out, torch.int32, "out"), _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
+    return out

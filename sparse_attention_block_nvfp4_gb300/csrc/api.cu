@@ -35,6 +35,11 @@ bool valid_heads(int h) { return h == 1 || h == 2 || h == 4 || h == 8; }
 
 }  // namespace
 
+namespace nvfp4idx {
+// Error text for entry points defined in other translation units.
+void set_last_error_text(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace nvfp4idx
+
 struct indexer_plan_s {
   int device = 0;
   int num_sms = 0;

@@ -1,0 +1,80 @@
+"""indexer_decode_noalloc: the decode entry point for callers that cannot
+allocate device memory.
+
+A caller such as a custom-op hook inside a serving engine (handed only its
+input and output buffers, the engine owning all device memory) or a
+latency-critical loop that must never call cudaMalloc cannot create a plan,
+because the plan allocates its scratch.  indexer_decode_noalloc runs the same
+kernels with their scratch in a fixed array inside the library.  These tests
+call it through the C ABI (ctypes, no binding helper) and compare it with
+indexer_decode on the same inputs, on two calls in a row, so a call that
+depends on what the previous call left in the shared array would show up.
+The file is named to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import indexer as oidx
+from gpu_util import assert_ids, gpu_cache, make_plan, oracle_cache, torch_dev, up
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    import sparse_attention_block_nvfp4_gb300 as idx
+    __graft_entry__.build()
+    L = idx.load_library()
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.indexer_decode_noalloc.argtypes = [P, P, I, P, I, P, I, I, I, P, P, P]
+    L.indexer_decode_noalloc.restype = I
+    return L
+
+
+def _call(lib, w, kv, out, status):
+    import torch
+    q, table, seq = up(w.q_decode), up(w.dec_page_table), up(w.dec_seq_lens)
+    stream = torch.cuda.current_stream()
+    rc = lib.indexer_decode_noalloc(q.data_ptr(), kv.data_ptr(), int(kv.shape[0]), table.data_ptr(),
+                                    int(table.shape[1]), seq.data_ptr(), w.num_decode_reqs, w.query_len,
+                                    w.num_heads, out.data_ptr(), status.data_ptr(), stream.cuda_stream)
+    torch.cuda.synchronize()
+    return rc
+
+
+def test_noalloc_matches_indexer_decode_on_two_calls_in_a_row(lib):
+    import torch
+    cases = [workloads.config(2, small=True),                       # 8 heads x 4 queries, split requests
+             workloads.config(1, small=True)]                       # 4 heads x 1 query
+    for w in cases:
+        kv = gpu_cache(w)
+        plan = make_plan(w)
+        want = plan.decode(up(w.q_decode), kv, up(w.dec_page_table), up(w.dec_seq_lens), w.query_len)
+        torch.cuda.synchronize()
+        out = torch.full((w.num_decode_rows, w.num_heads, 16), -77, dtype=torch.int32, device=torch_dev())
+        status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+        assert _call(lib, w, kv, out, status) == 0, lib.indexer_last_error()
+        assert int(status.item()) == 0
+        got = out.cpu().numpy()
+        assert np.array_equal(got, want.cpu().numpy()), f"{w.name}: differs from indexer_decode"
+        ref = oidx.decode(w.q_decode, oracle_cache(w), w.dec_page_table, w.dec_seq_lens, w.query_len,
+                          w.num_heads)
+        assert_ids(got, ref, w.name)
+        plan.close()
+
+
+def test_noalloc_rejects_calls_beyond_its_fixed_scratch(lib):
+    import torch
+    rng = np.random.Generator(np.random.PCG64(77))
+    w = workloads.make_workload(name="too_many", seed=77, rng=rng, num_heads=8,
+                                dec_seq_lens=[300] * 600, query_len=8)
+    kv = torch.zeros((w.num_blocks, 128, 72), dtype=torch.uint8, device=torch_dev())
+    out = torch.zeros((w.num_decode_rows, 8, 16), dtype=torch.int32, device=torch_dev())
+    status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+    import sparse_attention_block_nvfp4_gb300 as idx
+    assert _call(lib, w, kv, out, status) == idx.IDX_ENOSPACE
+    assert b"scratch" in lib.indexer_last_error()
