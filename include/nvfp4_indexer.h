@@ -175,9 +175,9 @@ int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uin
  *   status     NULL, or a device int32 that gets IDX_STATUS_* bits OR-ed in
  *   (no scores_dbg output)
  * Limit: the call needs 256-byte-aligned pieces of roughly
- * 8*num_reqs + (2*SMs + num_reqs) * (4 + 120*query_len*num_heads) bytes; a
+ * 8*num_reqs + (SMs + num_reqs) * (4 + 120*query_len*num_heads) bytes; a
  * call that needs more than 4 MiB returns IDX_ENOSPACE and launches nothing
- * (about 240 requests at query_len*num_heads = 64 on a 152-SM GPU).
+ * (about 390 requests at query_len*num_heads = 64 on a 152-SM GPU).
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (once per device, that device current): make that
  * first call before any stream capture.  All calls share the array, so calls

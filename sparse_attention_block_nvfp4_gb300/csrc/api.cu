@@ -46,7 +46,7 @@ struct indexer_plan_s {
   int num_heads = 0, max_reqs = 0, max_query_len = 0, max_pages = 0;
   int max_prefill_tokens = 0, max_prefill_reqs = 0;
   int decode_grid = 0;
-  float2* cand = nullptr;      // [(decode_grid + max_reqs)][64][15]
+  float2* cand = nullptr;      // [(decode_grid + max_reqs)][<= 64 rows][15]
   int32_t* slot_bad = nullptr; // [decode_grid + max_reqs]
   int2* req_info = nullptr;    // [max_reqs]
   int32_t* status = nullptr;   // 1 word
@@ -71,7 +71,7 @@ int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_quer
     return set_err(IDX_EINVAL, "indexer_plan: max_reqs=%d outside 0..%d", max_reqs, kMaxDecodeReqs);
   if (max_pages_per_req < 1 || max_pages_per_req > (1 << 20))
     return set_err(IDX_EINVAL, "indexer_plan: max_pages_per_req=%d outside 1..2^20", max_pages_per_req);
-  if (max_prefill_tokens < 0 || max_prefill_reqs < 0 || max_prefill_reqs > (1 << 16))
+  if (max_prefill_tokens < 0 || max_prefill_reqs < 0 || max_prefill_reqs > kMaxPrefillReqs)
     return set_err(IDX_EINVAL, "indexer_plan: bad prefill limits (%d tokens, %d requests)",
                    max_prefill_tokens, max_prefill_reqs);
 
@@ -96,7 +96,7 @@ int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_quer
   pl->max_pages = max_pages_per_req;
   pl->max_prefill_tokens = max_prefill_tokens;
   pl->max_prefill_reqs = max_prefill_reqs;
-  pl->decode_grid = 2 * pl->num_sms;
+  pl->decode_grid = pl->num_sms;   // one decode CTA per SM
   const size_t slots = (size_t)pl->decode_grid + (size_t)max_reqs;
   e = cudaMalloc(&pl->cand, slots * kMaxRows * kHistK * sizeof(float2));
   if (e == cudaSuccess) e = cudaMalloc(&pl->slot_bad, slots * sizeof(int32_t));
@@ -214,7 +214,7 @@ int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seq
   p.dbg_stride = dbg_stride;
   const int tq = 128 / plan->num_heads;
   const int64_t tiles_bound = (int64_t)total_q / tq + num_reqs;
-  int grid = 2 * plan->num_sms;
+  int grid = plan->num_sms;   // one prefill CTA per SM
   if (tiles_bound < grid) grid = (int)tiles_bound;
   if (grid < 1) grid = 1;
   cudaError_t e = launch_prefill(p, grid, stream);

@@ -8,20 +8,21 @@
 // Work split.  The history pages of all requests (page j < (seq_len-1)/128 of
 // request r) form one list of T pages; CTA c of G = min(grid, T) takes the
 // contiguous range [c*T/G, (c+1)*T/G), never empty.  A CTA walks its range
-// as segments (one per request it touches).  Per page:
-//   * the TMA unit copies the 9216-byte page into a shared-memory stage
-//     (cp.async.bulk, 7-stage ring, mbarrier completion);
-//   * thread t (of 128) reads token t's 72-byte row and dequantises it exactly
-//     to fp16 in registers (E2M1 x E4M3 fits fp16), then stores it into its
-//     own tensor-memory lane (tcgen05.st): the page becomes the MMA's A
-//     operand in tensor memory, M = 128 tokens, K = 128;
-//   * one thread issues 8 tcgen05.mma (K = 16 each) against the request's
-//     queries, B = [NQ rows x 128] fp16 in shared memory (E4M3 widened
-//     exactly), accumulating D[token][row] in fp32 in tensor memory;
-//   * the epilogue of the previous page (overlapping this page's MMA) loads
-//     D, reduces max over the 128 token lanes (butterfly across the warp,
-//     then across the 4 warps through shared memory) and inserts the page's
-//     score into the row's running top-15 (thread = row).
+// as segments (one per request it touches).  One CTA per SM, warp roles
+// linked by mbarrier rings:
+//   * producer warp: the TMA unit copies each 9216-byte page into an 8-stage
+//     shared ring (cp.async.bulk, transaction-count completion);
+//   * dequant warpgroup: thread t reads token t's 72-byte row, dequantises it
+//     exactly to fp16 (E2M1 x E4M3 fits fp16) and stores it into tensor-memory
+//     lane t (tcgen05.st): the page becomes the MMA's A operand (M = 128
+//     tokens, K = 128), 4 buffers deep; at each segment start it also widens
+//     the request's E4M3 queries to fp16 into a 128B-swizzled B tile
+//     (double buffered);
+//   * MMA warp: one thread issues 8 tcgen05.mma (K = 16 each) per page,
+//     D[token][row] in fp32 in tensor memory (4 buffers), and commits;
+//   * epilogue warpgroup: loads D, reduces max over the 128 token lanes
+//     (butterfly inside a warp, shared memory across the four warps) and
+//     inserts the page score into the row's running top-15 (thread = row).
 // A request covered by one CTA is finalised in place; otherwise each segment
 // leaves its 15 candidates per row in scratch and decode_merge_kernel merges
 // them (and writes the rows of requests with no history page).
@@ -35,21 +36,23 @@
 
 namespace nvfp4idx {
 
-constexpr int kDecStages = 7;
-constexpr int kDecThreads = 128;
-constexpr uint32_t kDecTmemCols = 256;   // A0 [0,64) A1 [64,128) D0 [128,192) D1 [192,256)
+constexpr int kDecStages = 8;            // raw page ring (shared memory)
+constexpr int kDecA = 4;                 // A buffers: tensor memory columns [64a, 64a+64)
+constexpr int kDecD = 4;                 // D buffers: columns [256 + 64d, 256 + 64d + NQ)
+constexpr int kDecThreads = 320;         // warp 0 TMA, warp 1 MMA, 2-5 dequant, 6-9 epilogue
+constexpr uint32_t kDecTmemCols = 512;
 
 template <int NQ>
 struct DecLayout {
   static constexpr uint32_t kQBytes = NQ * 256;                   // fp16 [2][NQ][64], SW128
-  static constexpr uint32_t kStageOff = kQBytes;                   // multiple of 1024
+  static constexpr uint32_t kQOff = 0;                             // two query tiles
+  static constexpr uint32_t kStageOff = 2 * kQBytes;               // multiple of 1024
   static constexpr uint32_t kRedOff = kStageOff + kDecStages * kPageBytes;
-  static constexpr uint32_t kPreOff = kRedOff + 4 * NQ * 4;
-  // at least 80 KB so that no more than two CTAs share an SM: each holds 256
-  // of the SM's 512 tensor-memory columns
+  static constexpr uint32_t kPreOff = kRedOff + 2 * 4 * NQ * 4;
+  // one CTA per SM: it holds all 512 tensor-memory columns
   static size_t bytes(int num_reqs) {
     const size_t b = 1024 + kPreOff + (size_t)(num_reqs + 1) * 4;
-    return b < 80 * 1024 ? 80 * 1024 : b;
+    return b < 120 * 1024 ? 120 * 1024 : b;
   }
 };
 
@@ -86,16 +89,38 @@ __device__ __forceinline__ void warp_colmax(float (&v)[NQ], int lane) {
   }
 }
 
+// The CTA's walk over its page range, identical in every role.
+struct SegWalk {
+  const int32_t* pre;
+  int NR;
+  int64_t n;        // pages in the range
+  int64_t g;        // pages walked
+  int r, j;         // current request, page
+  __device__ __forceinline__ bool more() const { return g < n; }
+  // pages [j, j_end) of request r form the current segment
+  __device__ __forceinline__ int seg_end() const {
+    const int hist = pre[r + 1] - pre[r];
+    const int64_t left = n - g;
+    return (int)((int64_t)hist < (int64_t)j + left ? (int64_t)hist : (int64_t)j + left);
+  }
+  __device__ __forceinline__ void next_request() {
+    ++r;
+    while (r < NR && pre[r + 1] - pre[r] == 0) ++r;
+    j = 0;
+  }
+};
+
 template <int NQ>
-__global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const DecodeParams p) {
   using Lay = DecLayout<NQ>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kDecStages];
-  __shared__ __align__(8) uint64_t mma_bar[2];
-  __shared__ int stage_bad[kDecStages];
+  __shared__ __align__(8) uint64_t raw_full[kDecStages], raw_empty[kDecStages];
+  __shared__ __align__(8) uint64_t a_full[kDecA], a_empty[kDecA];
+  __shared__ __align__(8) uint64_t d_full[kDecD], d_empty[kDecD];
+  __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s;
-  __shared__ int warp_sum[4];
+  __shared__ volatile int abort_s;
+  __shared__ int warp_sum[kDecThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -105,6 +130,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
   int32_t* const pre = reinterpret_cast<int32_t*>(base + Lay::kPreOff);
 
   const int NR = p.num_reqs, R = p.R, c = blockIdx.x;
+  constexpr int NW = kDecThreads / 32;
 
   // ---- 1. history pages per request -> exclusive prefix sums in smem
   {
@@ -127,13 +153,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
       pre[r] = run;
       run += hist_pages(__ldg(p.seq_lens + r), p.pt_stride);
     }
-    if (tid == kDecThreads - 1) pre[NR] = off + incl;
+    if (tid == kDecThreads - 1) {
+      int tot = 0;
+      for (int w = 0; w < NW; ++w) tot += warp_sum[w];
+      pre[NR] = tot;
+    }
     __syncthreads();
   }
   const int64_t T = pre[NR];
-  // Split the T pages over G_eff = min(G, T) CTAs: every one of them then
-  // owns at least one page, so every CTA between a request's first and last
-  // owner holds a segment of it (and writes the slot the merge reads).
+  // Split the T pages over G = min(grid, T) CTAs: every one of them then owns
+  // at least one page, so every CTA between a request's first and last owner
+  // holds a segment of it (and writes the slot the merge reads).
   const int G = (int)min((int64_t)gridDim.x, T);
   if (c == 0) {
     for (int r = tid; r < NR; r += kDecThreads) {
@@ -151,14 +181,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
   const int64_t n = x1 - x0;
 
   // ---- 2. tensor memory, barriers
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_s), kDecTmemCols);
     tmem_relinquish();
   }
-  if (tid == 32) {
-    for (int s = 0; s < kDecStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
-    mbar_init(smem_u32(&mma_bar[0]), 1);
-    mbar_init(smem_u32(&mma_bar[1]), 1);
+  if (tid == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(smem_u32(&raw_full[s]), 1);
+      mbar_init(smem_u32(&raw_empty[s]), 128);
+    }
+    for (int b = 0; b < kDecA; ++b) {
+      mbar_init(smem_u32(&a_full[b]), 128);
+      mbar_init(smem_u32(&a_empty[b]), 1);
+    }
+    for (int d = 0; d < kDecD; ++d) {
+      mbar_init(smem_u32(&d_full[d]), 1);
+      mbar_init(smem_u32(&d_empty[d]), 128);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&q_full[k]), 128);
+      mbar_init(smem_u32(&q_empty[k]), 1);
+    }
     abort_s = 0;
     fence_mbar_init();
   }
@@ -166,10 +209,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
-  // first request of the range: largest r with pre[r] <= x0 and a history page
-  int r_start = 0;
+  // first request of the range
+  int r_start;
   {
     int lo = 0, hi = NR - 1;
     while (lo < hi) {
@@ -177,192 +219,232 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_score_kernel(const Deco
       if (pre[mid] <= x0) lo = mid; else hi = mid - 1;
     }
     r_start = lo;
-    while (pre[r_start + 1] - pre[r_start] == 0) ++r_start;   // x0 < T, so this stops
+    while (pre[r_start + 1] - pre[r_start] == 0) ++r_start;
   }
-
-  // ---- producer state (thread 0)
-  int pr = r_start, pj = (int)(x0 - pre[r_start]);
-  int64_t issued = 0;
-  auto produce = [&]() {
-    const int stage = (int)(issued % kDecStages);
-    const uint32_t fb = smem_u32(&full_bar[stage]);
-    const int phys = __ldg(p.page_table + (int64_t)pr * p.pt_stride + pj);
-    if (phys < 0 || phys >= p.num_blocks) {
-      stage_bad[stage] = 1;
-      atomicOr(p.status, kStatusBadPage);
-      mbar_arrive(fb);
-    } else {
-      stage_bad[stage] = 0;
-      mbar_arrive_expect_tx(fb, kPageBytes);
-      bulk_g2s(sbase + Lay::kStageOff + stage * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-               kPageBytes, fb);
-    }
-    ++issued;
-    ++pj;
-    while (pr < NR && pj >= pre[pr + 1] - pre[pr]) { ++pr; pj = 0; }
-  };
-  if (tid == 0) {
-    const int64_t first = n < kDecStages ? n : kDecStages;
-    for (int64_t g = 0; g < first; ++g) produce();
-  }
-
-  constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
-  bool ok = true;
+  SegWalk walk{pre, NR, n, 0, r_start, (int)(x0 - pre[r_start])};
   auto fail = [&]() {
-    if (ok) {
-      ok = false;
+    if (!abort_s) {
       abort_s = 1;
       atomicOr(p.status, kStatusTimeout);
     }
   };
 
-  TopK15 top;
-  int64_t g = 0;            // pages consumed by this CTA
-  int64_t mma_issued = 0;   // tcgen05.commit count (thread 0)
-  int r = r_start;
-  int j = (int)(x0 - pre[r_start]);
-
-  // epilogue of page `jp` consumed at step `gp`
-  int seq_r = 0;
-  auto epilogue = [&](int64_t gp, int jp) {
-    const int b = (int)(gp & 1);
-    if (ok && !abort_s) {
-      if (!mbar_wait(smem_u32(&mma_bar[b]), (uint32_t)((gp >> 1) & 1))) fail();
-    }
-    tc_fence_after();
-    float v[NQ];
-    tmem_ld_row<NQ>(tbase + lane_base + 128 + b * 64, v);
-    tmem_wait_ld();
-    tc_fence_before();
-    warp_colmax<NQ>(v, lane);
-    if constexpr (NQ >= 32) {
-#pragma unroll
-      for (int i = 0; i < NQ / 32; ++i) red[warp * NQ + lane * (NQ / 32) + i] = v[i];
-    } else {
-      if ((lane & 1) == 0) red[warp * NQ + (lane >> 1)] = v[0];
-    }
-    named_bar_sync(1, kDecThreads);
-    if (tid < R) {
-      const float s = canon_zero(fmaxf(fmaxf(red[tid], red[NQ + tid]),
-                                       fmaxf(red[2 * NQ + tid], red[3 * NQ + tid])));
-      const int pos = seq_r - p.qlen + tid / p.H;
-      const int L = pos >= 0 ? (pos >> 7) : -1;
-      if (jp < L) {
-        top.insert(s, jp);
-        if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + tid) * p.dbg_stride + jp] = s;
-      }
-    }
-  };
-
-  while (g < n) {
-    const int hist = pre[r + 1] - pre[r];
-    const int j_end = (int)min((int64_t)hist, (int64_t)j + (n - g));
-    const int j_begin = j;
-    seq_r = __ldg(p.seq_lens + r);
-
-    // ---- segment start: the request's queries -> fp16 B operand (SW128)
-    for (int it = tid; it < NQ * 16; it += kDecThreads) {
-      const int row = it >> 4, c8 = it & 15;
-      uint4 o = make_uint4(0, 0, 0, 0);
-      if (row < R) {
-        const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.q + ((int64_t)r * R + row) * 128 + c8 * 8));
-        o.x = e4m3x2_to_f16x2(e.x & 0xFFFFu);
-        o.y = e4m3x2_to_f16x2(e.x >> 16);
-        o.z = e4m3x2_to_f16x2(e.y & 0xFFFFu);
-        o.w = e4m3x2_to_f16x2(e.y >> 16);
-      }
-      *reinterpret_cast<uint4*>(base + (c8 >> 3) * (NQ * 128) + sw128_offset(row, c8 & 7)) = o;
-    }
-    fence_proxy_async_smem();
-    top.reset();
-    int seg_bad = 0;
-
-    for (int jj = j_begin; jj < j_end; ++jj, ++g) {
-      const int stage = (int)(g % kDecStages);
-      if (ok && !abort_s) {
-        if (!mbar_wait(smem_u32(&full_bar[stage]), (uint32_t)((g / kDecStages) & 1))) fail();
-      }
-      seg_bad |= stage_bad[stage];
-      uint32_t w[18];
-      {
-        const uint2* src = reinterpret_cast<const uint2*>(base + Lay::kStageOff + stage * kPageBytes + tid * kRowBytes);
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          const uint2 t2 = src[i];
-          w[2 * i] = t2.x;
-          w[2 * i + 1] = t2.y;
+  if (warp == 0) {
+    // ================================================= producer (TMA)
+    if (lane == 0) {
+      int64_t g = 0;
+      while (walk.more() && !abort_s) {
+        const int je = walk.seg_end();
+        for (; walk.j < je && !abort_s; ++walk.j, ++walk.g, ++g) {
+          const int s = (int)(g % kDecStages);
+          const uint32_t k = (uint32_t)(g / kDecStages);
+          if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (k & 1) ^ 1, &abort_s)) { fail(); break; }
+          const uint32_t fb = smem_u32(&raw_full[s]);
+          const int phys = __ldg(p.page_table + (int64_t)walk.r * p.pt_stride + walk.j);
+          if (phys < 0 || phys >= p.num_blocks) {
+            atomicOr(p.status, kStatusBadPage);
+            mbar_arrive(fb);
+          } else {
+            mbar_arrive_expect_tx(fb, kPageBytes);
+            bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+                     kPageBytes, fb);
+          }
         }
+        if (walk.more()) walk.next_request();
       }
-      named_bar_sync(1, kDecThreads);                    // stage consumed by all
-      if (tid == 0 && issued < n && !abort_s) produce();
-
-      // dequantise token `tid` of the page into its tensor-memory lane
-      uint32_t a[64];
-      {
-        const uint32_t sc01 = e4m3x2_to_f16x2(w[16] & 0xFFFFu), sc23 = e4m3x2_to_f16x2(w[16] >> 16);
-        const uint32_t sc45 = e4m3x2_to_f16x2(w[17] & 0xFFFFu), sc67 = e4m3x2_to_f16x2(w[17] >> 16);
-        const uint32_t sc[4] = {sc01, sc23, sc45, sc67};
+      if (abort_s) {   // drain issued copies before the CTA may exit
+        for (int64_t k = (g > kDecStages ? g - kDecStages : 0); k < g; ++k)
+          mbar_wait(smem_u32(&raw_full[k % kDecStages]), (uint32_t)((k / kDecStages) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
+      int64_t g = 0;
+      int sq = 0;
+      while (walk.more() && !abort_s) {
+        const int je = walk.seg_end();
+        const int qs = sq & 1;
+        if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
+        const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
+        for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
+          const int b = (int)(g % kDecA), d = (int)(g % kDecD);
+          if (!mbar_wait_or_abort(smem_u32(&a_full[b]), (uint32_t)((g / kDecA) & 1), &abort_s)) { fail(); break; }
+          if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kDecD) & 1) ^ 1), &abort_s)) { fail(); break; }
+          tc_fence_after();
+          const uint32_t d_t = tbase + 256 + d * 64;
+          const uint32_t a_t = tbase + b * 64;
 #pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {
-          const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
-          dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
+            mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&a_empty[b]));
+          mma_commit(smem_u32(&d_full[d]));
         }
+        if (abort_s) break;
+        mma_commit(smem_u32(&q_empty[qs]));
+        ++sq;
+        if (walk.more()) walk.next_request();
       }
-      const int b = (int)(g & 1);
-      tmem_st_32x32b_x64(tbase + lane_base + b * 64, a);
-      tmem_wait_st();
-      tc_fence_before();
-      named_bar_sync(1, kDecThreads);                    // A operand and B operand ready
-      if (tid == 0 && !abort_s) {
+      if (abort_s && g > 0) {   // drain issued MMAs before tensor memory is freed
+        const int64_t k = g - 1;
+        mbar_wait(smem_u32(&d_full[k % kDecD]), (uint32_t)((k / kDecD) & 1));
+      }
+    }
+  } else if (warp < 6) {
+    // ================================================= dequant warpgroup
+    const int tok = ((warp & 3) << 5) | lane;        // tensor-memory lane of this thread
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int dq = tid - 64;                          // 0..127
+    int64_t g = 0;
+    int sq = 0;
+    bool ok = true;
+    while (walk.more() && ok) {
+      const int je = walk.seg_end();
+      const int qs = sq & 1;
+      // the request's queries -> fp16 B tile (128B swizzle, K-major)
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty[qs]),
+                                                       (uint32_t)(((sq >> 1) & 1) ^ 1), &abort_s))) {
+        fail();
+        break;
+      }
+      uint8_t* qt = base + Lay::kQOff + qs * Lay::kQBytes;
+      for (int it = dq; it < NQ * 16; it += 128) {
+        const int row = it >> 4, c8 = it & 15;
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (row < R) {
+          const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.q + ((int64_t)walk.r * R + row) * 128 + c8 * 8));
+          o.x = e4m3x2_to_f16x2(e.x & 0xFFFFu);
+          o.y = e4m3x2_to_f16x2(e.x >> 16);
+          o.z = e4m3x2_to_f16x2(e.y & 0xFFFFu);
+          o.w = e4m3x2_to_f16x2(e.y >> 16);
+        }
+        *reinterpret_cast<uint4*>(qt + (c8 >> 3) * (NQ * 128) + sw128_offset(row, c8 & 7)) = o;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&q_full[qs]));
+      for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
+        const int s = (int)(g % kDecStages);
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
+                                                         (uint32_t)((g / kDecStages) & 1), &abort_s))) {
+          fail();
+          ok = false;
+          break;
+        }
+        uint32_t w[18];
+        {
+          const uint2* src = reinterpret_cast<const uint2*>(base + Lay::kStageOff + s * kPageBytes + tok * kRowBytes);
+#pragma unroll
+          for (int i = 0; i < 9; ++i) {
+            const uint2 t2 = src[i];
+            w[2 * i] = t2.x;
+            w[2 * i + 1] = t2.y;
+          }
+        }
+        mbar_arrive(smem_u32(&raw_empty[s]));
+        uint32_t a[64];
+        {
+          const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
+                                  e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
+#pragma unroll
+          for (int g8 = 0; g8 < 8; ++g8) {
+            const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
+            dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
+          }
+        }
+        const int b = (int)(g % kDecA);
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&a_empty[b]),
+                                                         (uint32_t)(((g / kDecA) & 1) ^ 1), &abort_s))) {
+          fail();
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t d_t = tbase + 128 + b * 64;
-        const uint32_t a_t = tbase + b * 64;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(sbase + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
-          mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+        tmem_st_32x32b_x64(tbase + lane_base + b * 64, a);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&a_full[b]));
+      }
+      ++sq;
+      if (ok && walk.more()) walk.next_request();
+    }
+  } else {
+    // ================================================= epilogue warpgroup
+    const int ep = tid - 192;                         // 0..127: row owner for the top-k
+    const int wq = warp & 3;                          // tensor-memory lane quarter
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    TopK15 top;
+    int64_t g = 0;
+    bool stop = false;
+    while (walk.more() && !stop) {
+      const int je = walk.seg_end();
+      const int r = walk.r;
+      const int seq_r = __ldg(p.seq_lens + r);
+      const int pos = seq_r - p.qlen + ep / p.H;
+      const int L = pos >= 0 ? (pos >> 7) : -1;
+      top.reset();
+      int seg_bad = 0;
+      for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
+        const int d = (int)(g % kDecD);
+        int bad_wait = 0;
+        if (!mbar_wait_or_abort(smem_u32(&d_full[d]), (uint32_t)((g / kDecD) & 1), &abort_s)) {
+          fail();
+          bad_wait = 1;
         }
-        mma_commit(smem_u32(&mma_bar[b]));
-        ++mma_issued;
-      }
-      if (jj > j_begin) epilogue(g - 1, jj - 1);
-    }
-    epilogue(g - 1, j_end - 1);
-
-    // ---- finalise the segment
-    const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
-    if (tid < R) {
-      if (cf == cl) {
-        const int pos = seq_r - p.qlen + tid / p.H;
-        const int L = pos >= 0 ? (pos >> 7) : -1;
-        write_out_row(p.out + ((int64_t)r * R + tid) * kTopK, top.id, L, seg_bad != 0);
-      } else {
-        float2* dst = p.cand + ((int64_t)(c + r) * R + tid) * kHistK;
+        tc_fence_after();
+        float v[NQ];
+        tmem_ld_row<NQ>(tbase + lane_base + 256 + d * 64, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&d_empty[d]));
+        warp_colmax<NQ>(v, lane);
+        float* rd = red + (g & 1) * (4 * NQ);
+        if constexpr (NQ >= 32) {
 #pragma unroll
-        for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+          for (int i = 0; i < NQ / 32; ++i) rd[wq * NQ + lane * (NQ / 32) + i] = v[i];
+        } else {
+          if ((lane & 1) == 0) rd[wq * NQ + (lane >> 1)] = v[0];
+        }
+        if (named_bar_red_or(2, 128, bad_wait | (abort_s ? 1 : 0))) {
+          stop = true;
+          break;
+        }
+        if (ep < R) {
+          const int jp = walk.j;
+          const float sc = canon_zero(fmaxf(fmaxf(rd[ep], rd[NQ + ep]), fmaxf(rd[2 * NQ + ep], rd[3 * NQ + ep])));
+          const int phys = __ldg(p.page_table + (int64_t)r * p.pt_stride + jp);
+          seg_bad |= (phys < 0 || phys >= p.num_blocks);
+          if (jp < L) {
+            top.insert(sc, jp);
+            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + ep) * p.dbg_stride + jp] = sc;
+          }
+        }
       }
+      if (stop) break;
+      // ---- finalise the segment
+      const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+      if (ep < R) {
+        if (cf == cl) {
+          write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, top.id, L, seg_bad != 0);
+        } else {
+          float2* dst = p.cand + ((int64_t)(c + r) * R + ep) * kHistK;
+#pragma unroll
+          for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+        }
+      }
+      if (ep == 0 && cf != cl) p.slot_bad[c + r] = seg_bad;
+      if (walk.more()) walk.next_request();
     }
-    if (tid == 0 && cf != cl) p.slot_bad[c + r] = seg_bad;
-
-    // next request with history pages
-    ++r;
-    while (r < NR && pre[r + 1] - pre[r] == 0) ++r;
-    j = 0;
-    named_bar_sync(1, kDecThreads);    // Q smem free for the next segment
   }
 
-  // ---- drain after a timeout, then free tensor memory
-  __syncthreads();
-  if (tid == 0 && abort_s) {
-    for (int64_t k = (issued > kDecStages ? issued - kDecStages : 0); k < issued; ++k)
-      mbar_wait(smem_u32(&full_bar[k % kDecStages]), (uint32_t)((k / kDecStages) & 1));
-    for (int64_t k = (mma_issued > 2 ? mma_issued - 2 : 0); k < mma_issued; ++k)
-      mbar_wait(smem_u32(&mma_bar[k & 1]), (uint32_t)((k >> 1) & 1));
-  }
+  // ---- free tensor memory once every role is done with it
+  __syncwarp();   // lanes that had no role wait here for their warp's lane 0
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tbase, kDecTmemCols);
+  if (warp == 1) tmem_dealloc(tbase, kDecTmemCols);
 }
 
 // One warp per (request, row): merge the per-segment top-15 lists of split

@@ -108,7 +108,7 @@ extern "C" int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages,
 
   // carve the scratch: status | request info | per-slot bad flags | candidates
   const int R = query_len * num_heads;
-  const int grid = 2 * slot.num_sms;
+  const int grid = slot.num_sms;        // one decode CTA per SM, as indexer_decode
   const size_t slots = (size_t)grid + (size_t)num_reqs;
   const size_t off_status = 0;
   const size_t off_info = align256(off_status + sizeof(int32_t));

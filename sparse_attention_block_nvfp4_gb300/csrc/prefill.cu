@@ -9,18 +9,21 @@
 // straight into shared memory.
 //
 // Tiling.  A tile is 128 query rows = (128/H tokens) x H heads of one
-// request (the last tile of a request may be ragged).  Its rows go into
-// tensor memory once (E4M3 widened exactly to fp16) and serve as the A
-// operand, M = 128, K = 128.  For every history page of the tile:
-//   * the TMA unit copies the raw 9216-byte page into a shared stage;
-//   * thread t dequantises token t to fp16 and writes it into a 128B-swizzled
-//     K-major B tile [128 tokens x 128] (double buffered);
-//   * one thread issues 8 tcgen05.mma: D[row][token] = Q . K^T in fp32;
-//   * while that runs, each thread (= one query row) loads the previous
-//     page's D row from tensor memory, takes the max over the 128 tokens and
-//     updates its running top-15 if the page is a history page of its token.
-// Tiles of a request are visited last-first (they hold the most pages) and
-// dealt round-robin to the CTAs.
+// request (the last tile of a request may be ragged); its rows sit in tensor
+// memory as the MMA's A operand (M = 128, K = 128).  Tiles of a request are
+// visited last-first (they hold the most pages) and dealt round-robin to the
+// CTAs, one CTA per SM.  Warp roles, linked by mbarrier rings:
+//   * producer warp: the TMA unit copies each raw 9216-byte page into a
+//     6-stage shared ring;
+//   * two dequant warpgroups, alternating pages: thread t dequantises token t
+//     to fp16 into a 128B-swizzled K-major B tile [128 tokens x 128] (4 tiles
+//     deep);
+//   * MMA warp: one thread issues 8 tcgen05.mma per page,
+//     D[row][token] = Q . K^T in fp32, 3 accumulators deep;
+//   * epilogue warpgroup, thread = query row: widens the next tile's queries
+//     into tensor memory (2 buffers), loads its D row per page, takes the max
+//     over the 128 tokens and updates its running top-15 if the page is a
+//     history page of its token; writes the row at the end of the tile.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -31,33 +34,62 @@
 
 namespace nvfp4idx {
 
-constexpr int kPreStages = 4;
-constexpr int kPreThreads = 128;
-constexpr uint32_t kPreTmemCols = 256;     // Q [0,64), D [128,256)
+constexpr int kPreStages = 6;              // raw page ring
+constexpr int kPreB = 4;                   // dequantised B tiles
+constexpr int kPreD = 3;                   // accumulators: columns [128 + 128d, 256 + 128d)
+constexpr int kPreThreads = 448;           // warp 0 TMA, 1 MMA, 2-5 / 6-9 dequant, 10-13 epilogue
+constexpr uint32_t kPreTmemCols = 512;     // queries [0,64) and [64,128), accumulators [128,512)
 constexpr uint32_t kBTileBytes = 128 * 256;  // fp16 [2 K-blocks][128 tokens][64]
 
 struct PreLayout {
-  static constexpr uint32_t kBOff = 0;                                  // 2 x 32 KB
-  static constexpr uint32_t kStageOff = 2 * kBTileBytes;
+  static constexpr uint32_t kBOff = 0;
+  static constexpr uint32_t kStageOff = kPreB * kBTileBytes;
   static constexpr uint32_t kTpreOff = kStageOff + kPreStages * kPageBytes;
   static size_t bytes(int num_reqs) { return 1024 + kTpreOff + (size_t)(num_reqs + 1) * 4; }
 };
 
 struct TileInfo {
-  int r, t0, nt, L_max, ctx, row0;   // row0 = first q row of the tile (token index)
+  int r, t0, nt, L_max, ctx, row0;   // row0 = first token (q row) of the tile
   bool table_bad;
 };
 
 template <int H>
-__global__ void __launch_bounds__(kPreThreads, 2) prefill_kernel(const PrefillParams p) {
+__device__ __forceinline__ TileInfo prefill_tile(const PrefillParams& p, const int32_t* tpre, int t) {
+  constexpr int TQ = 128 / H;
+  int lo = 0, hi = p.num_reqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tpre[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.r = lo;
+  const int cu0 = __ldg(p.cu_seqlens_q + lo);
+  const int ql = __ldg(p.cu_seqlens_q + lo + 1) - cu0;
+  const int ntile = (ql + TQ - 1) / TQ;
+  const int lt = ntile - 1 - (t - tpre[lo]);        // last tile first
+  ti.t0 = lt * TQ;
+  ti.nt = min(TQ, ql - ti.t0);
+  const int seq = __ldg(p.seq_lens + lo);
+  ti.ctx = seq - ql;
+  ti.row0 = cu0 + ti.t0;
+  const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
+  ti.table_bad = hist > p.pt_stride;
+  const int pos_last = ti.ctx + ti.t0 + ti.nt - 1;
+  ti.L_max = (pos_last >= 0 && !ti.table_bad) ? (pos_last >> 7) : 0;
+  return ti;
+}
+
+template <int H>
+__global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillParams p) {
   constexpr int TQ = 128 / H;     // tokens per tile
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kPreStages];
-  __shared__ __align__(8) uint64_t mma_bar;
-  __shared__ int stage_bad[kPreStages];
+  __shared__ __align__(8) uint64_t raw_full[kPreStages], raw_empty[kPreStages];
+  __shared__ __align__(8) uint64_t b_full[kPreB], b_empty[kPreB];
+  __shared__ __align__(8) uint64_t d_full[kPreD], d_empty[kPreD];
+  __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s;
-  __shared__ int warp_sum[4];
+  __shared__ volatile int abort_s;
+  __shared__ int warp_sum[kPreThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -65,6 +97,7 @@ __global__ void __launch_bounds__(kPreThreads, 2) prefill_kernel(const PrefillPa
   uint8_t* const base = smem_raw + (sbase - raw_u32);
   int32_t* const tpre = reinterpret_cast<int32_t*>(base + PreLayout::kTpreOff);
   const int NR = p.num_reqs, G = gridDim.x, c = blockIdx.x;
+  constexpr int NW = kPreThreads / 32;
 
   // ---- tiles per request -> exclusive prefix sums
   {
@@ -91,44 +124,38 @@ __global__ void __launch_bounds__(kPreThreads, 2) prefill_kernel(const PrefillPa
       const int ql = __ldg(p.cu_seqlens_q + r + 1) - __ldg(p.cu_seqlens_q + r);
       run += ql > 0 ? (ql + TQ - 1) / TQ : 0;
     }
-    if (tid == kPreThreads - 1) tpre[NR] = off + incl;
+    if (tid == kPreThreads - 1) {
+      int tot = 0;
+      for (int w = 0; w < NW; ++w) tot += warp_sum[w];
+      tpre[NR] = tot;
+    }
     __syncthreads();
   }
   const int NT = tpre[NR];
   if (c >= NT) return;
 
-  auto tile_info = [&](int t) {
-    int lo = 0, hi = NR - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (tpre[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    TileInfo ti;
-    ti.r = lo;
-    const int cu0 = __ldg(p.cu_seqlens_q + lo);
-    const int ql = __ldg(p.cu_seqlens_q + lo + 1) - cu0;
-    const int ntile = (ql + TQ - 1) / TQ;
-    const int lt = ntile - 1 - (t - tpre[lo]);        // last tile first
-    ti.t0 = lt * TQ;
-    ti.nt = min(TQ, ql - ti.t0);
-    const int seq = __ldg(p.seq_lens + lo);
-    ti.ctx = seq - ql;
-    ti.row0 = cu0 + ti.t0;
-    const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
-    ti.table_bad = hist > p.pt_stride;
-    const int pos_last = ti.ctx + ti.t0 + ti.nt - 1;
-    ti.L_max = (pos_last >= 0 && !ti.table_bad) ? (pos_last >> 7) : 0;
-    return ti;
-  };
-
   // ---- tensor memory, barriers
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_s), kPreTmemCols);
     tmem_relinquish();
   }
-  if (tid == 32) {
-    for (int s = 0; s < kPreStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
-    mbar_init(smem_u32(&mma_bar), 1);
+  if (tid == 0) {
+    for (int s = 0; s < kPreStages; ++s) {
+      mbar_init(smem_u32(&raw_full[s]), 1);
+      mbar_init(smem_u32(&raw_empty[s]), 128);
+    }
+    for (int b = 0; b < kPreB; ++b) {
+      mbar_init(smem_u32(&b_full[b]), 128);
+      mbar_init(smem_u32(&b_empty[b]), 1);
+    }
+    for (int d = 0; d < kPreD; ++d) {
+      mbar_init(smem_u32(&d_full[d]), 1);
+      mbar_init(smem_u32(&d_empty[d]), 128);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&q_full[k]), 128);
+      mbar_init(smem_u32(&q_empty[k]), 1);
+    }
     abort_s = 0;
     fence_mbar_init();
   }
@@ -136,72 +163,140 @@ __global__ void __launch_bounds__(kPreThreads, 2) prefill_kernel(const PrefillPa
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-
-  // ---- producer (thread 0): walks (tile, page) in the consumers' order
-  int p_tile = c;               // tile index
-  int p_j = 0;                  // page within tile
-  TileInfo p_ti;
-  int64_t issued = 0;
-  if (tid == 0) {
-    p_ti = tile_info(p_tile);
-    while (p_tile < NT && p_ti.L_max == 0) {
-      p_tile += G;
-      if (p_tile < NT) p_ti = tile_info(p_tile);
-    }
-  }
-  auto produce = [&]() {
-    const int stage = (int)(issued % kPreStages);
-    const uint32_t fb = smem_u32(&full_bar[stage]);
-    const int phys = __ldg(p.page_table + (int64_t)p_ti.r * p.pt_stride + p_j);
-    if (phys < 0 || phys >= p.num_blocks) {
-      stage_bad[stage] = 1;
-      mbar_arrive(fb);
-    } else {
-      stage_bad[stage] = 0;
-      mbar_arrive_expect_tx(fb, kPageBytes);
-      bulk_g2s(sbase + PreLayout::kStageOff + stage * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-               kPageBytes, fb);
-    }
-    ++issued;
-    if (++p_j >= p_ti.L_max) {
-      p_j = 0;
-      do {
-        p_tile += G;
-        if (p_tile < NT) p_ti = tile_info(p_tile);
-      } while (p_tile < NT && p_ti.L_max == 0);
-    }
-  };
-  if (tid == 0) {
-    for (int s = 0; s < kPreStages && p_tile < NT; ++s) produce();
-  }
-
-  constexpr uint32_t idesc = idesc_f16_f32(128, 128);
-  bool ok = true;
   auto fail = [&]() {
-    if (ok) {
-      ok = false;
+    if (!abort_s) {
       abort_s = 1;
       atomicOr(p.status, kStatusTimeout);
     }
   };
 
-  TopK15 top;
-  int64_t g = 0;            // pages consumed
-  int64_t mma_issued = 0;
-  float v[128];
-
-  for (int t = c; t < NT; t += G) {
-    const TileInfo ti = tile_info(t);
-    const int rows = ti.nt * H;
-    const int n = tid;                                // this thread's query row
-    const int pos = ti.ctx + ti.t0 + n / H;
-    const int L = (n < rows && pos >= 0) ? (pos >> 7) : -1;
-
-    // query rows -> tensor memory (A operand)
-    {
+  if (warp == 0) {
+    // ================================================= producer (TMA)
+    if (lane == 0) {
+      int64_t g = 0;
+      for (int t = c; t < NT && !abort_s; t += G) {
+        const TileInfo ti = prefill_tile<H>(p, tpre, t);
+        for (int j = 0; j < ti.L_max; ++j, ++g) {
+          const int s = (int)(g % kPreStages);
+          if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1), &abort_s)) {
+            fail();
+            break;
+          }
+          const uint32_t fb = smem_u32(&raw_full[s]);
+          const int phys = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + j);
+          if (phys < 0 || phys >= p.num_blocks) {
+            mbar_arrive(fb);
+          } else {
+            mbar_arrive_expect_tx(fb, kPageBytes);
+            bulk_g2s(sbase + PreLayout::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+                     kPageBytes, fb);
+          }
+        }
+      }
+      if (abort_s) {
+        for (int64_t k = (g > kPreStages ? g - kPreStages : 0); k < g; ++k)
+          mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(128, 128);
+      int64_t g = 0;
+      int kq = 0;
+      for (int t = c; t < NT && !abort_s; t += G) {
+        const TileInfo ti = prefill_tile<H>(p, tpre, t);
+        if (ti.L_max == 0) continue;
+        const int qb = kq & 1;
+        if (!mbar_wait_or_abort(smem_u32(&q_full[qb]), (uint32_t)((kq >> 1) & 1), &abort_s)) { fail(); break; }
+        for (int j = 0; j < ti.L_max; ++j, ++g) {
+          const int nb = (int)(g % kPreB), d = (int)(g % kPreD);
+          if (!mbar_wait_or_abort(smem_u32(&b_full[nb]), (uint32_t)((g / kPreB) & 1), &abort_s)) { fail(); break; }
+          if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kPreD) & 1) ^ 1), &abort_s)) { fail(); break; }
+          tc_fence_after();
+          const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)nb * kBTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(bt + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
+            mma_f16_tmemA(tbase + 128 + d * 128, tbase + qb * 64 + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&b_empty[nb]));
+          mma_commit(smem_u32(&d_full[d]));
+        }
+        if (abort_s) break;
+        mma_commit(smem_u32(&q_empty[qb]));
+        ++kq;
+      }
+      if (abort_s && g > 0) {
+        const int64_t k = g - 1;
+        mbar_wait(smem_u32(&d_full[k % kPreD]), (uint32_t)((k / kPreD) & 1));
+      }
+    }
+  } else if (warp < 10) {
+    // ================================================= dequant warpgroups
+    const int grp = (warp - 2) >> 2;                 // 0 or 1: takes pages with g % 2 == grp
+    const int tok = ((warp & 3) << 5) | lane;        // token row of the page / of the B tile
+    int64_t g = 0;
+    bool ok = true;
+    for (int t = c; t < NT && ok; t += G) {
+      const TileInfo ti = prefill_tile<H>(p, tpre, t);
+      for (int j = 0; j < ti.L_max; ++j, ++g) {
+        if ((int)(g & 1) != grp) continue;
+        const int s = (int)(g % kPreStages);
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
+                                                         (uint32_t)((g / kPreStages) & 1), &abort_s))) {
+          fail();
+          ok = false;
+          break;
+        }
+        uint32_t w[18];
+        {
+          const uint2* src = reinterpret_cast<const uint2*>(base + PreLayout::kStageOff + s * kPageBytes + tok * kRowBytes);
+#pragma unroll
+          for (int i = 0; i < 9; ++i) {
+            const uint2 t2 = src[i];
+            w[2 * i] = t2.x;
+            w[2 * i + 1] = t2.y;
+          }
+        }
+        mbar_arrive(smem_u32(&raw_empty[s]));
+        const int nb = (int)(g % kPreB);
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&b_empty[nb]),
+                                                         (uint32_t)(((g / kPreB) & 1) ^ 1), &abort_s))) {
+          fail();
+          ok = false;
+          break;
+        }
+        uint8_t* bt = base + PreLayout::kBOff + nb * kBTileBytes;
+        const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
+                                e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
+          uint32_t o[8];
+          dequant16(w[2 * g8], w[2 * g8 + 1], s2, o);
+          // elements 16*g8 .. +15 = 16-byte chunks 2*g8, 2*g8+1 of the row
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c16 = 2 * g8 + h;
+            *reinterpret_cast<uint4*>(bt + (c16 >> 3) * (128 * 128) + sw128_offset(tok, c16 & 7)) =
+                make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&b_full[nb]));
+      }
+    }
+  } else {
+    // ================================================= epilogue warpgroup
+    const int n = ((warp & 3) << 5) | lane;          // query row = tensor-memory lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    TopK15 top;
+    bool ok = true;
+    // widen tile t's queries into tensor-memory buffer qb (thread = row)
+    auto load_q = [&](const TileInfo& ti, int qb) {
       uint32_t a[64];
-      if (n < rows) {
+      if (n < ti.nt * H) {
         const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)ti.row0 * H + n) * 128);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -217,131 +312,105 @@ __global__ void __launch_bounds__(kPreThreads, 2) prefill_kernel(const PrefillPa
 #pragma unroll
         for (int i = 0; i < 64; ++i) a[i] = 0u;
       }
-      tmem_st_32x32b_x64(tbase + lane_base + 0, a);
+      tc_fence_after();
+      tmem_st_32x32b_x64(tbase + lane_base + qb * 64, a);
       tmem_wait_st();
       tc_fence_before();
+      mbar_arrive(smem_u32(&q_full[qb]));
+    };
+    // the k-th tile of this CTA that has pages (the MMA's tile sequence)
+    auto next_mma_tile = [&](int from) {
+      for (int t = from; t < NT; t += G)
+        if (prefill_tile<H>(p, tpre, t).L_max > 0) return t;
+      return NT;
+    };
+    int t_next_q = next_mma_tile(c);      // next tile whose queries are not loaded yet
+    int kq_loaded = 0;
+    if (t_next_q < NT) {
+      load_q(prefill_tile<H>(p, tpre, t_next_q), 0);
+      kq_loaded = 1;
+      t_next_q = next_mma_tile(t_next_q + G);
     }
-    // a request with an unreadable history page gets all -1 rows
-    int bad_local = ti.table_bad ? 1 : 0;
-    if (!ti.table_bad) {
-      const int seq = __ldg(p.seq_lens + ti.r);
-      const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
-      for (int jj = tid; jj < hist; jj += kPreThreads) {
-        const int ph = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + jj);
-        bad_local |= (ph < 0 || ph >= p.num_blocks);
+    int64_t g = 0;
+    for (int t = c; t < NT; t += G) {
+      // every epilogue warp takes the same decision to stop (a barrier it
+      // skipped would otherwise hold the others)
+      if (named_bar_red_or(2, 128, (!ok || abort_s) ? 1 : 0)) break;
+      const TileInfo ti = prefill_tile<H>(p, tpre, t);
+      const int rows = ti.nt * H;
+      const int pos = ti.ctx + ti.t0 + n / H;
+      const int L = (n < rows && pos >= 0) ? (pos >> 7) : -1;
+      if (ti.L_max > 0 && t_next_q < NT) {
+        // one tile ahead: queries of the next tile with pages
+        const int qb = kq_loaded & 1;
+        if (__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty[qb]),
+                                                        (uint32_t)(((kq_loaded >> 1) & 1) ^ 1), &abort_s))) {
+          load_q(prefill_tile<H>(p, tpre, t_next_q), qb);
+        } else {
+          fail();
+          ok = false;
+        }
+        ++kq_loaded;
+        t_next_q = next_mma_tile(t_next_q + G);
       }
-    }
-    const int tile_bad = __syncthreads_or(bad_local);
-    if (tid == 0 && tile_bad) atomicOr(p.status, ti.table_bad ? kStatusBadTable : kStatusBadPage);
-    top.reset();
-
-    for (int j = 0; j < ti.L_max; ++j, ++g) {
-      const int stage = (int)(g % kPreStages);
-      if (ok && !abort_s) {
-        if (!mbar_wait(smem_u32(&full_bar[stage]), (uint32_t)((g / kPreStages) & 1))) fail();
-      }
-      uint32_t w[18];
-      {
-        const uint2* src = reinterpret_cast<const uint2*>(base + PreLayout::kStageOff + stage * kPageBytes + tid * kRowBytes);
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          const uint2 t2 = src[i];
-          w[2 * i] = t2.x;
-          w[2 * i + 1] = t2.y;
+      // a request with an unreadable history page gets all -1 rows
+      int tile_bad = ti.table_bad ? 1 : 0;
+      if (!ti.table_bad) {
+        const int seq = __ldg(p.seq_lens + ti.r);
+        const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
+        for (int jj = n; jj < hist; jj += 128) {
+          const int ph = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + jj);
+          tile_bad |= (ph < 0 || ph >= p.num_blocks);
         }
       }
-      named_bar_sync(1, kPreThreads);
-      if (tid == 0 && p_tile < NT && !abort_s) produce();
-
-      // dequantise token `tid` into row `tid` of the B tile (SW128, K-major)
-      {
-        uint8_t* bt = base + PreLayout::kBOff + (g & 1) * kBTileBytes;
-        const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
-                                e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
-#pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {
-          const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
-          uint32_t o[8];
-          dequant16(w[2 * g8], w[2 * g8 + 1], s2, o);
-          // elements 16*g8 .. +15 = 16-byte chunks 2*g8, 2*g8+1 of the row
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c16 = 2 * g8 + h;
-            *reinterpret_cast<uint4*>(bt + (c16 >> 3) * (128 * 128) + sw128_offset(tid, c16 & 7)) =
-                make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      if (j > 0) {       // previous page's scores -> registers
-        if (ok && !abort_s) {
-          if (!mbar_wait(smem_u32(&mma_bar), (uint32_t)((g - 1) & 1))) fail();
+      tile_bad = named_bar_red_or(2, 128, tile_bad);
+      if (n == 0 && tile_bad) atomicOr(p.status, ti.table_bad ? kStatusBadTable : kStatusBadPage);
+      top.reset();
+      for (int j = 0; j < ti.L_max; ++j, ++g) {
+        const int d = (int)(g % kPreD);
+        if (!ok) continue;
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[d]),
+                                                         (uint32_t)((g / kPreD) & 1), &abort_s))) {
+          fail();
+          ok = false;
+          continue;
         }
         tc_fence_after();
-        tmem_ld_row<128>(tbase + lane_base + 128, v);
-        tmem_wait_ld();
+        const uint32_t dt = tbase + lane_base + 128 + d * 128;
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[64];
+          tmem_ld_32x32b_x16(dt + half * 64 + 0, v);
+          tmem_ld_32x32b_x16(dt + half * 64 + 16, v + 16);
+          tmem_ld_32x32b_x16(dt + half * 64 + 32, v + 32);
+          tmem_ld_32x32b_x16(dt + half * 64 + 48, v + 48);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) m = fmaxf(m, fmaxf(v[i], v[i + 1]));
+        }
         tc_fence_before();
-      }
-      named_bar_sync(1, kPreThreads);
-      if (tid == 0 && !abort_s) {
-        tc_fence_after();
-        const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)(g & 1) * kBTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(bt + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-          mma_f16_tmemA(tbase + 128, tbase + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&mma_bar));
-        ++mma_issued;
-      }
-      if (j > 0) {
-        float m = v[0];
-#pragma unroll
-        for (int i = 1; i < 128; ++i) m = fmaxf(m, v[i]);
+        mbar_arrive(smem_u32(&d_empty[d]));
         m = canon_zero(m);
-        if (j - 1 < L) {
-          top.insert(m, j - 1);
-          if (p.scores_dbg) p.scores_dbg[((int64_t)ti.row0 * H + n) * p.dbg_stride + (j - 1)] = m;
+        if (j < L) {
+          top.insert(m, j);
+          if (p.scores_dbg) p.scores_dbg[((int64_t)ti.row0 * H + n) * p.dbg_stride + j] = m;
         }
       }
+      if (ok && n < rows) write_out_row(p.out + ((int64_t)ti.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
     }
-    if (ti.L_max > 0) {   // last page of the tile
-      if (ok && !abort_s) {
-        if (!mbar_wait(smem_u32(&mma_bar), (uint32_t)((g - 1) & 1))) fail();
-      }
-      tc_fence_after();
-      tmem_ld_row<128>(tbase + lane_base + 128, v);
-      tmem_wait_ld();
-      tc_fence_before();
-      float m = v[0];
-#pragma unroll
-      for (int i = 1; i < 128; ++i) m = fmaxf(m, v[i]);
-      m = canon_zero(m);
-      const int jl = ti.L_max - 1;
-      if (jl < L) {
-        top.insert(m, jl);
-        if (p.scores_dbg) p.scores_dbg[((int64_t)ti.row0 * H + n) * p.dbg_stride + jl] = m;
-      }
-    }
-    if (n < rows) write_out_row(p.out + ((int64_t)ti.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
-    named_bar_sync(1, kPreThreads);      // tensor memory Q free for the next tile
   }
 
-  __syncthreads();
-  if (tid == 0 && abort_s) {
-    for (int64_t k = (issued > kPreStages ? issued - kPreStages : 0); k < issued; ++k)
-      mbar_wait(smem_u32(&full_bar[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
-    if (mma_issued > 0) mbar_wait(smem_u32(&mma_bar), (uint32_t)((mma_issued - 1) & 1));
-  }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tbase, kPreTmemCols);
+  if (warp == 1) tmem_dealloc(tbase, kPreTmemCols);
 }
 
 template <int H>
 static cudaError_t launch_prefill_h(const PrefillParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = PreLayout::bytes(p.num_reqs);
+  const size_t smem = PreLayout::bytes(p.num_reqs);   // > 114 KB: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
