@@ -18,8 +18,8 @@
 //   * two dequant warpgroups, alternating pages: thread t dequantises token t
 //     to fp16 into a 128B-swizzled K-major B tile [128 tokens x 128] (4 tiles
 //     deep);
-//   * MMA warp: one thread issues 8 tcgen05.mma per page,
-//     D[row][token] = Q . K^T in fp32, 3 accumulators deep;
+//   * two MMA warps, alternate pages: one thread each issues 8 tcgen05.mma
+//     per page, D[row][token] = Q . K^T in fp32, 3 accumulators deep;
 //   * epilogue warpgroup, thread = query row: widens the next tile's queries
 //     into tensor memory (2 buffers), loads its D row per page, takes the max
 //     over the 128 tokens and updates its running top-15 if the page is a
@@ -37,7 +37,7 @@ namespace nvfp4idx {
 constexpr int kPreStages = 6;              // raw page ring
 constexpr int kPreB = 4;                   // dequantised B tiles
 constexpr int kPreD = 3;                   // accumulators: columns [128 + 128d, 256 + 128d)
-constexpr int kPreThreads = 448;           // warp 0 TMA, 1 MMA, 2-5 / 6-9 dequant, 10-13 epilogue
+constexpr int kPreThreads = 480;           // warp 0 TMA, 1 / 14 MMA issue, 2-5 / 6-9 dequant, 10-13 epilogue
 constexpr uint32_t kPreTmemCols = 512;     // queries [0,64) and [64,128), accumulators [128,512)
 constexpr uint32_t kBTileBytes = 128 * 256;  // fp16 [2 K-blocks][128 tokens][64]
 
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&q_full[k]), 128);
-      mbar_init(smem_u32(&q_empty[k]), 1);
+      mbar_init(smem_u32(&q_empty[k]), 2);   // both MMA issuers commit
     }
     abort_s = 0;
     fence_mbar_init();
@@ -198,11 +198,14 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
       }
     }
-  } else if (warp == 1) {
-    // ================================================= MMA issuer
+  } else if (warp == 1 || warp == 14) {
+    // ================================================= MMA issuers
+    // Two issuing threads take alternate pages, so that one thread's commits
+    // and waits overlap the other's MMAs and the tensor core stays busy.
     if (lane == 0) {
+      const int mgrp = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = idesc_f16_f32(128, 128);
-      int64_t g = 0;
+      int64_t g = 0, g_last = -1;
       int kq = 0;
       for (int t = c; t < NT && !abort_s; t += G) {
         const TileInfo ti = prefill_tile<H>(p, tpre, t);
@@ -210,6 +213,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         const int qb = kq & 1;
         if (!mbar_wait_or_abort(smem_u32(&q_full[qb]), (uint32_t)((kq >> 1) & 1), &abort_s)) { fail(); break; }
         for (int j = 0; j < ti.L_max; ++j, ++g) {
+          if ((int)(g & 1) != mgrp) continue;
           const int nb = (int)(g % kPreB), d = (int)(g % kPreD);
           if (!mbar_wait_or_abort(smem_u32(&b_full[nb]), (uint32_t)((g / kPreB) & 1), &abort_s)) { fail(); break; }
           if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kPreD) & 1) ^ 1), &abort_s)) { fail(); break; }
@@ -222,13 +226,14 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           }
           mma_commit(smem_u32(&b_empty[nb]));
           mma_commit(smem_u32(&d_full[d]));
+          g_last = g;
         }
         if (abort_s) break;
         mma_commit(smem_u32(&q_empty[qb]));
         ++kq;
       }
-      if (abort_s && g > 0) {
-        const int64_t k = g - 1;
+      if (abort_s && g_last >= 0) {
+        const int64_t k = g_last;
         mbar_wait(smem_u32(&d_full[k % kPreD]), (uint32_t)((k / kPreD) & 1));
       }
     }
