@@ -9,20 +9,26 @@
 // request r) form one list of T pages; CTA c of G = min(grid, T) takes the
 // contiguous range [c*T/G, (c+1)*T/G), never empty.  A CTA walks its range
 // as segments (one per request it touches).  One CTA per SM, warp roles
-// linked by mbarrier rings:
-//   * producer warp: the TMA unit copies each 9216-byte page into an 8-stage
-//     shared ring (cp.async.bulk, transaction-count completion);
-//   * dequant warpgroup: thread t reads token t's 72-byte row, dequantises it
-//     exactly to fp16 (E2M1 x E4M3 fits fp16) and stores it into tensor-memory
-//     lane t (tcgen05.st): the page becomes the MMA's A operand (M = 128
-//     tokens, K = 128), 4 buffers deep; at each segment start it also widens
-//     the request's E4M3 queries to fp16 into a 128B-swizzled B tile
-//     (double buffered);
-//   * MMA warp: one thread issues 8 tcgen05.mma (K = 16 each) per page,
-//     D[token][row] in fp32 in tensor memory (4 buffers), and commits;
-//   * epilogue warpgroup: loads D, reduces max over the 128 token lanes
-//     (butterfly inside a warp, shared memory across the four warps) and
-//     inserts the page score into the row's running top-15 (thread = row).
+// linked by mbarrier rings; page g of the walk uses ring slot g % 4 and is
+// handled by the role instance of parity g % 2:
+//   * producer warp: reads page ids 32 at a time and has the TMA unit copy
+//     each 9216-byte page into an 8-stage shared ring (cp.async.bulk,
+//     transaction-count completion);
+//   * two dequant warpgroups: thread t reads token t's 72-byte row,
+//     dequantises it exactly to fp16 (E2M1 x E4M3 fits fp16) and stores it
+//     into tensor-memory lane t (tcgen05.st): the page becomes the MMA's A
+//     operand (M = 128 tokens, K = 128); at each segment start both widen the
+//     request's E4M3 queries to fp16 into a 128B-swizzled B tile (double
+//     buffered);
+//   * two MMA warps: one thread each issues 8 tcgen05.mma (K = 16) per page,
+//     D[token][row] in fp32 in tensor memory, and commits once per page (a
+//     single thread cannot issue small-N MMAs as fast as the tensor core
+//     retires them);
+//   * two epilogue warpgroups: load D and take the max over each warp's 32
+//     token lanes per column with one redux.sync per column, combine the four
+//     warps through shared memory, and insert the page score into the row's
+//     running top-15 (thread = row); at a segment end group 1 hands its lists
+//     to group 0, which merges them.
 // A request covered by one CTA is finalised in place; otherwise each segment
 // leaves its 15 candidates per row in scratch and decode_merge_kernel merges
 // them (and writes the rows of requests with no history page).
@@ -37,9 +43,12 @@
 namespace nvfp4idx {
 
 constexpr int kDecStages = 8;            // raw page ring (shared memory)
-constexpr int kDecA = 4;                 // A buffers: tensor memory columns [64a, 64a+64)
-constexpr int kDecD = 4;                 // D buffers: columns [256 + 64d, 256 + 64d + NQ)
-constexpr int kDecThreads = 320;         // warp 0 TMA, warp 1 MMA, 2-5 dequant, 6-9 epilogue
+constexpr int kDecA = 4;                 // page g: A buffer g % 4 (columns [64a, 64a+64)) and
+constexpr int kDecD = kDecA;             // D buffer g % 4 (columns [256 + 64d, 256 + 64d + NQ))
+// warp 0 TMA; 1 / 2 MMA issue; 3-6 / 7-10 dequant; 11-14 / 15-18 epilogue
+// (first of each pair: pages of even index, second: odd)
+constexpr int kDecThreads = 608;
+constexpr int kDqTid0 = 96, kEpTid0 = 352;
 constexpr uint32_t kDecTmemCols = 512;
 
 template <int NQ>
@@ -47,8 +56,9 @@ struct DecLayout {
   static constexpr uint32_t kQBytes = NQ * 256;                   // fp16 [2][NQ][64], SW128
   static constexpr uint32_t kQOff = 0;                             // two query tiles
   static constexpr uint32_t kStageOff = 2 * kQBytes;               // multiple of 1024
-  static constexpr uint32_t kRedOff = kStageOff + kDecStages * kPageBytes;
-  static constexpr uint32_t kPreOff = kRedOff + 2 * 4 * NQ * 4;
+  static constexpr uint32_t kRedOff = kStageOff + kDecStages * kPageBytes;   // [2 groups][2][4 warps][NQ]
+  static constexpr uint32_t kMrgOff = kRedOff + 2 * 2 * 4 * NQ * 4;            // [2][64 rows][15] (score, id)
+  static constexpr uint32_t kPreOff = kMrgOff + 2 * kMaxRows * kHistK * 8;
   // one CTA per SM: it holds all 512 tensor-memory columns
   static size_t bytes(int num_reqs) {
     const size_t b = 1024 + kPreOff + (size_t)(num_reqs + 1) * 4;
@@ -66,26 +76,50 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
   return (int)(((x + 1) * G - 1) / T);
 }
 
-// Butterfly reduce-scatter of per-lane row vectors: after it, lane l holds
-// in v[0 .. NQ/32-1] the max over the warp's 32 lanes of columns
-// l*NQ/32 + i (NQ >= 32), or of column l/2 (NQ == 16).
-template <int NQ>
-__device__ __forceinline__ void warp_colmax(float (&v)[NQ], int lane) {
+// Max over the warp's 32 lanes (tokens) of CW <= 32 columns, one redux.sync
+// per column; afterwards lane l holds column l (l < CW).
+template <int CW>
+__device__ __forceinline__ float warp_colmax(const float (&v)[CW], int lane) {
+  float m = 0.0f;
 #pragma unroll
-  for (int lvl = 0; lvl < 5; ++lvl) {
-    const int off = 16 >> lvl;
-    const int cnt = NQ >> (lvl + 1);
-    if (cnt >= 1) {
-      const bool upper = (lane & off) != 0;
+  for (int k = 0; k < CW; ++k) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v[k]));
+    m = (lane == k) ? r : m;
+  }
+  return m;
+}
+
+// Merge a sorted top-15 list `b` (score desc, id asc; id -1 = empty) into `a`.
+__device__ __forceinline__ void merge_top15(TopK15& a, const float2* b) {
+  float s[15];
+  int id[15];
+  int i = 0, j = 0;
 #pragma unroll
-      for (int i = 0; i < cnt; ++i) {
-        const float send = upper ? v[i] : v[i + cnt];
-        const float keep = upper ? v[i + cnt] : v[i];
-        v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+  for (int k = 0; k < 15; ++k) {
+    const float2 bj = b[j < 15 ? j : 14];
+    const float bs = bj.x;
+    const int bi = __float_as_int(bj.y);
+    float as = -CUDART_INF_F;
+    int ai = -1;
+#pragma unroll
+    for (int t = 0; t < 15; ++t)
+      if (t == i) {
+        as = a.s[t];
+        ai = a.id[t];
       }
-    } else {
-      v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
-    }
+    const bool a_ok = i < 15 && ai >= 0;
+    const bool b_ok = j < 15 && bi >= 0;
+    const bool take_a = a_ok && (!b_ok || as > bs || (as == bs && ai < bi));
+    s[k] = take_a ? as : (b_ok ? bs : -CUDART_INF_F);
+    id[k] = take_a ? ai : (b_ok ? bi : -1);
+    i += take_a ? 1 : 0;
+    j += (!take_a && b_ok) ? 1 : 0;
+  }
+#pragma unroll
+  for (int k = 0; k < 15; ++k) {
+    a.s[k] = s[k];
+    a.id[k] = id[k];
   }
 }
 
@@ -115,7 +149,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   using Lay = DecLayout<NQ>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kDecStages], raw_empty[kDecStages];
-  __shared__ __align__(8) uint64_t a_full[kDecA], a_empty[kDecA];
+  __shared__ __align__(8) uint64_t a_full[kDecA];
   __shared__ __align__(8) uint64_t d_full[kDecD], d_empty[kDecD];
   __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
   __shared__ uint32_t tmem_base_s;
@@ -190,17 +224,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       mbar_init(smem_u32(&raw_full[s]), 1);
       mbar_init(smem_u32(&raw_empty[s]), 128);
     }
-    for (int b = 0; b < kDecA; ++b) {
-      mbar_init(smem_u32(&a_full[b]), 128);
-      mbar_init(smem_u32(&a_empty[b]), 1);
-    }
+    for (int b = 0; b < kDecA; ++b) mbar_init(smem_u32(&a_full[b]), 128);
     for (int d = 0; d < kDecD; ++d) {
       mbar_init(smem_u32(&d_full[d]), 1);
       mbar_init(smem_u32(&d_empty[d]), 128);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&q_full[k]), 128);
-      mbar_init(smem_u32(&q_empty[k]), 1);
+      mbar_init(smem_u32(&q_full[k]), 256);   // both dequant groups write the tile
+      mbar_init(smem_u32(&q_empty[k]), 2);    // both MMA issuers commit
     }
     abort_s = 0;
     fence_mbar_init();
@@ -231,37 +262,56 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
 
   if (warp == 0) {
     // ================================================= producer (TMA)
-    if (lane == 0) {
-      int64_t g = 0;
-      while (walk.more() && !abort_s) {
-        const int je = walk.seg_end();
-        for (; walk.j < je && !abort_s; ++walk.j, ++walk.g, ++g) {
-          const int s = (int)(g % kDecStages);
-          const uint32_t k = (uint32_t)(g / kDecStages);
-          if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (k & 1) ^ 1, &abort_s)) { fail(); break; }
-          const uint32_t fb = smem_u32(&raw_full[s]);
-          const int phys = __ldg(p.page_table + (int64_t)walk.r * p.pt_stride + walk.j);
-          if (phys < 0 || phys >= p.num_blocks) {
-            atomicOr(p.status, kStatusBadPage);
-            mbar_arrive(fb);
-          } else {
-            mbar_arrive_expect_tx(fb, kPageBytes);
-            bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-                     kPageBytes, fb);
+    // The whole warp walks the range; page ids are read 32 at a time (one
+    // coalesced load), so no copy waits on a page-table read; lane 0 issues.
+    int64_t g = 0;
+    bool ok = true;
+    while (walk.more() && ok) {
+      const int je = walk.seg_end();
+      const int32_t* row = p.page_table + (int64_t)walk.r * p.pt_stride;
+      for (int jb = walk.j; jb < je && ok; jb += 32) {
+        const int cnt = min(32, je - jb);
+        const int my_phys = lane < cnt ? __ldg(row + jb + lane) : 0;
+        for (int k = 0; k < cnt; ++k, ++g) {
+          const int phys = __shfl_sync(0xffffffffu, my_phys, k);
+          int issued = 1;
+          if (lane == 0) {
+            const int s = (int)(g % kDecStages);
+            if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kDecStages) & 1) ^ 1), &abort_s)) {
+              fail();
+              issued = 0;
+            } else {
+              const uint32_t fb = smem_u32(&raw_full[s]);
+              if (phys < 0 || phys >= p.num_blocks) {
+                atomicOr(p.status, kStatusBadPage);
+                mbar_arrive(fb);
+              } else {
+                mbar_arrive_expect_tx(fb, kPageBytes);
+                bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+                         kPageBytes, fb);
+              }
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, issued, 0)) {
+            ok = false;
+            break;
           }
         }
-        if (walk.more()) walk.next_request();
       }
-      if (abort_s) {   // drain issued copies before the CTA may exit
-        for (int64_t k = (g > kDecStages ? g - kDecStages : 0); k < g; ++k)
-          mbar_wait(smem_u32(&raw_full[k % kDecStages]), (uint32_t)((k / kDecStages) & 1));
-      }
+      walk.g += je - walk.j;
+      walk.j = je;
+      if (ok && walk.more()) walk.next_request();
     }
-  } else if (warp == 1) {
-    // ================================================= MMA issuer
+    if (!ok && lane == 0) {   // drain issued copies before the CTA may exit
+      for (int64_t k = (g > kDecStages ? g - kDecStages : 0); k < g; ++k)
+        mbar_wait(smem_u32(&raw_full[k % kDecStages]), (uint32_t)((k / kDecStages) & 1));
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ================================================= MMA issuers
     if (lane == 0) {
+      const int mgrp = warp - 1;                      // pages with g % 2 == mgrp
       constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
-      int64_t g = 0;
+      int64_t g = 0, g_last = -1;
       int sq = 0;
       while (walk.more() && !abort_s) {
         const int je = walk.seg_end();
@@ -269,35 +319,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
         const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
         for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
-          const int b = (int)(g % kDecA), d = (int)(g % kDecD);
+          if ((int)(g & 1) != mgrp) continue;
+          const int b = (int)(g % kDecA);
           if (!mbar_wait_or_abort(smem_u32(&a_full[b]), (uint32_t)((g / kDecA) & 1), &abort_s)) { fail(); break; }
-          if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kDecD) & 1) ^ 1), &abort_s)) { fail(); break; }
+          if (!mbar_wait_or_abort(smem_u32(&d_empty[b]), (uint32_t)(((g / kDecD) & 1) ^ 1), &abort_s)) { fail(); break; }
           tc_fence_after();
-          const uint32_t d_t = tbase + 256 + d * 64;
+          const uint32_t d_t = tbase + 256 + b * 64;
           const uint32_t a_t = tbase + b * 64;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
             mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&a_empty[b]));
-          mma_commit(smem_u32(&d_full[d]));
+          // one commit per page: d_full[b] also tells the dequant warps that
+          // A buffer b is free again
+          mma_commit(smem_u32(&d_full[b]));
+          g_last = g;
         }
         if (abort_s) break;
         mma_commit(smem_u32(&q_empty[qs]));
         ++sq;
         if (walk.more()) walk.next_request();
       }
-      if (abort_s && g > 0) {   // drain issued MMAs before tensor memory is freed
-        const int64_t k = g - 1;
-        mbar_wait(smem_u32(&d_full[k % kDecD]), (uint32_t)((k / kDecD) & 1));
+      if (abort_s && g_last >= 0) {   // drain issued MMAs before tensor memory is freed
+        mbar_wait(smem_u32(&d_full[g_last % kDecD]), (uint32_t)((g_last / kDecD) & 1));
       }
     }
-  } else if (warp < 6) {
-    // ================================================= dequant warpgroup
+  } else if (warp < 11) {
+    // ================================================= dequant warpgroups
+    const int grp = (warp - 3) >> 2;                 // takes pages with g % 2 == grp
     const int tok = ((warp & 3) << 5) | lane;        // tensor-memory lane of this thread
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int dq = tid - 64;                          // 0..127
+    const int dq = tid - kDqTid0;                     // 0..255 (both groups share the query tile)
     int64_t g = 0;
     int sq = 0;
     bool ok = true;
@@ -311,7 +364,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         break;
       }
       uint8_t* qt = base + Lay::kQOff + qs * Lay::kQBytes;
-      for (int it = dq; it < NQ * 16; it += 128) {
+      for (int it = dq; it < NQ * 16; it += 256) {
         const int row = it >> 4, c8 = it & 15;
         uint4 o = make_uint4(0, 0, 0, 0);
         if (row < R) {
@@ -326,6 +379,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&q_full[qs]));
       for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
+        if ((int)(g & 1) != grp) continue;
         const int s = (int)(g % kDecStages);
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
                                                          (uint32_t)((g / kDecStages) & 1), &abort_s))) {
@@ -354,9 +408,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
             dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
           }
         }
+        // A buffer b was last read by the MMAs of page g - kDecA, whose
+        // completion is phase g / kDecA - 1 of d_full[b]; the next phase of
+        // that barrier needs this page's A, so the parity cannot alias.
         const int b = (int)(g % kDecA);
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&a_empty[b]),
-                                                         (uint32_t)(((g / kDecA) & 1) ^ 1), &abort_s))) {
+        if (g >= kDecA &&
+            !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[b]),
+                                                         (uint32_t)(((g / kDecA) - 1) & 1), &abort_s))) {
           fail();
           ok = false;
           break;
@@ -371,76 +429,101 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       if (ok && walk.more()) walk.next_request();
     }
   } else {
-    // ================================================= epilogue warpgroup
-    const int ep = tid - 192;                         // 0..127: row owner for the top-k
+    // ================================================= epilogue warpgroups
+    // Group `grp` scores pages with g % 2 == grp and keeps its own running
+    // top-15 per row; at a segment end group 1 hands its lists to group 0
+    // through shared memory and group 0 merges and writes the result.  The
+    // walk is never left early, so every barrier is always reached.
+    const int grp = (warp - 11) >> 2;
+    const int ep = (tid - kEpTid0) & 127;             // row owner within the group
     const int wq = warp & 3;                          // tensor-memory lane quarter
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t bar_grp = 2 + grp, bar_both = 4;
+    float2* const mrg = reinterpret_cast<float2*>(base + Lay::kMrgOff);   // [2][64][15] by segment parity
+    constexpr int CW = NQ < 32 ? NQ : 32;             // columns per load + reduction pass
     TopK15 top;
     int64_t g = 0;
-    bool stop = false;
-    while (walk.more() && !stop) {
+    int sq = 0;
+    bool ok = true;                                   // uniform within the group
+    while (walk.more()) {
       const int je = walk.seg_end();
       const int r = walk.r;
       const int seq_r = __ldg(p.seq_lens + r);
       const int pos = seq_r - p.qlen + ep / p.H;
       const int L = pos >= 0 ? (pos >> 7) : -1;
-      top.reset();
+      // an unreadable page id anywhere in the segment: checked once, up front
       int seg_bad = 0;
+      if (grp == 0) {
+        for (int jj = walk.j + ep; jj < je; jj += 128) {
+          const int ph = __ldg(p.page_table + (int64_t)r * p.pt_stride + jj);
+          seg_bad |= (ph < 0 || ph >= p.num_blocks);
+        }
+      }
+      top.reset();
       for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
+        if ((int)(g & 1) != grp) continue;
         const int d = (int)(g % kDecD);
-        int bad_wait = 0;
-        if (!mbar_wait_or_abort(smem_u32(&d_full[d]), (uint32_t)((g / kDecD) & 1), &abort_s)) {
-          fail();
-          bad_wait = 1;
+        int wok = 0;
+        if (ok) {
+          wok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[d]),
+                                                            (uint32_t)((g / kDecD) & 1), &abort_s));
+          if (!wok) fail();
         }
-        tc_fence_after();
-        float v[NQ];
-        tmem_ld_row<NQ>(tbase + lane_base + 256 + d * 64, v);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&d_empty[d]));
-        warp_colmax<NQ>(v, lane);
-        float* rd = red + (g & 1) * (4 * NQ);
-        if constexpr (NQ >= 32) {
+        float* rd = red + (grp * 2 + ((g >> 1) & 1)) * (4 * NQ);
+        if (wok) {
+          tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < NQ / 32; ++i) rd[wq * NQ + lane * (NQ / 32) + i] = v[i];
-        } else {
-          if ((lane & 1) == 0) rd[wq * NQ + (lane >> 1)] = v[0];
+          for (int ch = 0; ch < NQ / CW; ++ch) {
+            float v[CW];
+            tmem_ld_row<CW>(tbase + lane_base + 256 + d * 64 + ch * CW, v);
+            tmem_wait_ld();
+            const float m = warp_colmax<CW>(v, lane);
+            if (lane < CW) rd[wq * NQ + ch * CW + lane] = m;
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&d_empty[d]));
         }
-        if (named_bar_red_or(2, 128, bad_wait | (abort_s ? 1 : 0))) {
-          stop = true;
-          break;
-        }
-        if (ep < R) {
+        ok = !named_bar_red_or(bar_grp, 128, (!wok || abort_s) ? 1 : 0);
+        if (ok && ep < R) {
           const int jp = walk.j;
           const float sc = canon_zero(fmaxf(fmaxf(rd[ep], rd[NQ + ep]), fmaxf(rd[2 * NQ + ep], rd[3 * NQ + ep])));
-          const int phys = __ldg(p.page_table + (int64_t)r * p.pt_stride + jp);
-          seg_bad |= (phys < 0 || phys >= p.num_blocks);
           if (jp < L) {
             top.insert(sc, jp);
             if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + ep) * p.dbg_stride + jp] = sc;
           }
         }
       }
-      if (stop) break;
-      // ---- finalise the segment
-      const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
-      if (ep < R) {
-        if (cf == cl) {
-          write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, top.id, L, seg_bad != 0);
-        } else {
-          float2* dst = p.cand + ((int64_t)(c + r) * R + ep) * kHistK;
+      // ---- hand group 1's lists to group 0, merge, finalise the segment
+      float2* mb = mrg + (sq & 1) * (kMaxRows * kHistK);
+      if (grp == 1 && ep < R) {
 #pragma unroll
-          for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+        for (int k = 0; k < kHistK; ++k) mb[ep * kHistK + k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+      }
+      named_bar_sync(bar_both, 256);
+      if (grp == 0) {
+        const int bad = named_bar_red_or(bar_grp, 128, seg_bad);
+        if (ok) {
+          const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+          if (ep < R) {
+            merge_top15(top, mb + ep * kHistK);
+            if (cf == cl) {
+              write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, top.id, L, bad != 0);
+            } else {
+              float2* dst = p.cand + ((int64_t)(c + r) * R + ep) * kHistK;
+#pragma unroll
+              for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+            }
+          }
+          if (ep == 0 && cf != cl) p.slot_bad[c + r] = bad;
         }
       }
-      if (ep == 0 && cf != cl) p.slot_bad[c + r] = seg_bad;
+      ++sq;
       if (walk.more()) walk.next_request();
     }
   }
 
   // ---- free tensor memory once every role is done with it
-  __syncwarp();   // lanes that had no role wait here for their warp's lane 0
+  __syncwarp();   // lanes without a role wait here for their warp's lane 0
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
