@@ -8,27 +8,35 @@
 // Work split.  The history pages of all requests (page j < (seq_len-1)/128 of
 // request r) form one list of T pages; CTA c of G = min(grid, T) takes the
 // contiguous range [c*T/G, (c+1)*T/G), never empty.  A CTA walks its range
-// as segments (one per request it touches).  One CTA per SM, warp roles
-// linked by mbarrier rings; page g of the walk uses ring slot g % 4 and is
-// handled by the role instance of parity g % 2:
+// as segments (one per request it touches) and each segment as quads of up
+// to 4 consecutive pages.  A quad passes through the tensor core as 4 slices:
+// slice s holds tokens [32s, 32s+32) of the quad's 4 pages, page q of the
+// quad in tensor-memory lanes [32q, 32q+32).  So the MMA of slice s,
+// D[lane][row] = K_slice . Q^T, gives the warp that owns lane quarter q the
+// scores of 32 tokens of ITS page; after the 4 slices that warp has seen all
+// 128 tokens of the page and takes the max over them alone: an in-register
+// max over the slices, then a reduction over its 32 lanes, with no exchange
+// between warps.  One CTA per SM, warp roles linked by mbarrier
+// rings (slice s of every quad uses A buffer s and D buffer s):
 //   * producer warp: reads page ids 32 at a time and has the TMA unit copy
 //     each 9216-byte page into an 8-stage shared ring (cp.async.bulk,
 //     transaction-count completion);
-//   * two dequant warpgroups: thread t reads token t's 72-byte row,
-//     dequantises it exactly to fp16 (E2M1 x E4M3 fits fp16) and stores it
-//     into tensor-memory lane t (tcgen05.st): the page becomes the MMA's A
-//     operand (M = 128 tokens, K = 128); at each segment start both widen the
-//     request's E4M3 queries to fp16 into a 128B-swizzled B tile (double
-//     buffered);
-//   * two MMA warps: one thread each issues 8 tcgen05.mma (K = 16) per page,
-//     D[token][row] in fp32 in tensor memory, and commits once per page (a
+//   * two dequant warpgroups (quads of even / odd index): warp q reads the
+//     72-byte rows of tokens 32s + lane of page q, dequantises them exactly to
+//     fp16 (E2M1 x E4M3 fits fp16) and stores them into its lane quarter of A
+//     buffer s (tcgen05.st), the MMA's A operand (M = 128 lanes, K = 128); at
+//     each segment start both widen the request's E4M3 queries to fp16 into a
+//     128B-swizzled B tile (double buffered);
+//   * two MMA warps (slices of even / odd index): one thread each issues 8
+//     tcgen05.mma (K = 16) per slice into D buffer s, and commits once (a
 //     single thread cannot issue small-N MMAs as fast as the tensor core
 //     retires them);
-//   * two epilogue warpgroups: load D and take the max over each warp's 32
-//     token lanes per column with one redux.sync per column, combine the four
-//     warps through shared memory, and insert the page score into the row's
-//     running top-15 (thread = row); at a segment end group 1 hands its lists
-//     to group 0, which merges them.
+//   * epilogue warpgroup: warp q keeps the running max of its page's tokens
+//     over the 4 slices, reduces it over its lanes (butterfly shuffles that
+//     leave column k in lane k), and lane k inserts the
+//     page score of rows k and k + 32 into their running top-15 (threshold in
+//     a register, list in shared memory); at a segment end the four warps'
+//     lists of each row are merged.
 // A request covered by one CTA is finalised in place; otherwise each segment
 // leaves its 15 candidates per row in scratch and decode_merge_kernel merges
 // them (and writes the rows of requests with no history page).
@@ -42,29 +50,46 @@
 
 namespace nvfp4idx {
 
-constexpr int kDecStages = 8;            // raw page ring (shared memory)
-constexpr int kDecA = 4;                 // page g: A buffer g % 4 (columns [64a, 64a+64)) and
-constexpr int kDecD = kDecA;             // D buffer g % 4 (columns [256 + 64d, 256 + 64d + NQ))
-// warp 0 TMA; 1 / 2 MMA issue; 3-6 / 7-10 dequant; 11-14 / 15-18 epilogue
-// (first of each pair: pages of even index, second: odd)
-constexpr int kDecThreads = 608;
+constexpr int kQuadSlots = 4;            // raw page ring: quad kq fills stages 4 * (kq % 4) + q
+constexpr int kDecStages = 4 * kQuadSlots;
+constexpr int kDecSlices = 4;            // slice s: A buffer s (columns [64s, 64s+64))
+// warp 0 TMA; 1 / 2 MMA issue; 3-6 / 7-10 dequant; 11-14 epilogue
+constexpr int kDecThreads = 480;
 constexpr int kDqTid0 = 96, kEpTid0 = 352;
 constexpr uint32_t kDecTmemCols = 512;
+
+// D buffers in tensor memory from column 256: for NQ <= 32 two sets of four
+// 32-column buffers (quad kq uses set kq % 2, so the epilogue may lag the MMAs
+// by a quad), for NQ = 64 one set of four 64-column buffers.
+template <int NQ>
+struct DecD {
+  static constexpr int kSets = NQ <= 32 ? 2 : 1;
+  static constexpr int kCols = NQ <= 32 ? 32 : 64;
+  __device__ static __forceinline__ int set(int64_t kq) { return kSets == 2 ? (int)(kq & 1) : 0; }
+  // parity of the epilogue's release of quad kq's D buffer
+  __device__ static __forceinline__ uint32_t phase(int64_t kq) {
+    return (uint32_t)((kSets == 2 ? (kq >> 1) : kq) & 1);
+  }
+  __device__ static __forceinline__ uint32_t col(int64_t kq, int sl) {
+    return 256u + (uint32_t)((set(kq) * kDecSlices + sl) * kCols);
+  }
+};
 
 template <int NQ>
 struct DecLayout {
   static constexpr uint32_t kQBytes = NQ * 256;                   // fp16 [2][NQ][64], SW128
   static constexpr uint32_t kQOff = 0;                             // two query tiles
   static constexpr uint32_t kStageOff = 2 * kQBytes;               // multiple of 1024
-  static constexpr uint32_t kRedOff = kStageOff + kDecStages * kPageBytes;   // [2 groups][2][4 warps][NQ]
-  static constexpr uint32_t kMrgOff = kRedOff + 2 * 2 * 4 * NQ * 4;            // [2][64 rows][15] (score, id)
-  static constexpr uint32_t kPreOff = kMrgOff + 2 * kMaxRows * kHistK * 8;
+  static constexpr uint32_t kListOff = kStageOff + kDecStages * kPageBytes;  // [4 warps][64 rows][15] (score, id)
+  static constexpr uint32_t kPreOff = kListOff + 4 * kMaxRows * kHistK * 8;
   // one CTA per SM: it holds all 512 tensor-memory columns
   static size_t bytes(int num_reqs) {
     const size_t b = 1024 + kPreOff + (size_t)(num_reqs + 1) * 4;
     return b < 120 * 1024 ? 120 * 1024 : b;
   }
 };
+static_assert(1024 + DecLayout<64>::kPreOff + (kMaxDecodeReqs + 1) * 4 + 1024 <= 227 * 1024,
+              "decode shared memory above the 227 KB a CTA may hold");
 
 __device__ __forceinline__ int hist_pages(int seq_len, int pt_stride) {
   const int h = seq_len >= 1 ? (seq_len - 1) >> 7 : 0;
@@ -76,50 +101,75 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
   return (int)(((x + 1) * G - 1) / T);
 }
 
-// Max over the warp's 32 lanes (tokens) of CW <= 32 columns, one redux.sync
-// per column; afterwards lane l holds column l (l < CW).
-template <int CW>
-__device__ __forceinline__ float warp_colmax(const float (&v)[CW], int lane) {
-  float m = 0.0f;
-#pragma unroll
-  for (int k = 0; k < CW; ++k) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v[k]));
-    m = (lane == k) ? r : m;
+// Insert (v, j) into a sorted top-15 list in shared memory (score desc; id -1
+// = empty) when v beats its last entry; j exceeds every id already in it, so
+// it goes after equal scores.  Returns the list's new last score.
+__device__ __forceinline__ float list_insert15(float2* l, float v, int j) {
+  int k = kHistK - 1;
+  while (k > 0) {
+    const float2 prev = l[k - 1];
+    if (prev.x >= v) break;
+    l[k] = prev;
+    --k;
   }
+  l[k] = make_float2(v, __int_as_float(j));
+  return l[kHistK - 1].x;
+}
+
+// Column maxima over the warp's 32 lanes by butterfly transpose-reduction:
+// at step H each lane keeps half of its columns, sends the other half to
+// lane ^ H and takes the max with what it receives (H shuffles).  For N = 32
+// columns, lane l ends with column l (31 shuffles in all, against 32
+// warp-wide reductions column by column); for N = 16, lanes l and l ^ 16 end
+// with column l & 15.  v is overwritten.
+template <int H>
+__device__ __forceinline__ void colmax_step(float* v, int lane) {
+  const bool up = (lane & H) != 0;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const float keep = up ? v[i + H] : v[i];
+    const float send = up ? v[i] : v[i + H];
+    v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, H));
+  }
+}
+template <int N>
+__device__ __forceinline__ float warp_colmax(float* v, int lane) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32) colmax_step<16>(v, lane);
+  colmax_step<8>(v, lane);
+  colmax_step<4>(v, lane);
+  colmax_step<2>(v, lane);
+  colmax_step<1>(v, lane);
+  float m = v[0];
+  if constexpr (N == 16) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
   return m;
 }
 
-// Merge a sorted top-15 list `b` (score desc, id asc; id -1 = empty) into `a`.
-__device__ __forceinline__ void merge_top15(TopK15& a, const float2* b) {
-  float s[15];
-  int id[15];
-  int i = 0, j = 0;
+// Merge the four sorted lists of `row` ([4][64][15] in shared memory) into
+// the top 15 by score, equal scores by lower id.
+__device__ __forceinline__ void merge4_top15(const float2* lists, int row, float (&s)[kHistK],
+                                             int (&id)[kHistK]) {
+  int h[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int k = 0; k < 15; ++k) {
-    const float2 bj = b[j < 15 ? j : 14];
-    const float bs = bj.x;
-    const int bi = __float_as_int(bj.y);
-    float as = -CUDART_INF_F;
-    int ai = -1;
+  for (int k = 0; k < kHistK; ++k) {
+    float bs = -CUDART_INF_F;
+    int bi = -1, bw = -1;
 #pragma unroll
-    for (int t = 0; t < 15; ++t)
-      if (t == i) {
-        as = a.s[t];
-        ai = a.id[t];
+    for (int w = 0; w < 4; ++w) {
+      if (h[w] < kHistK) {
+        const float2 e = lists[(w * kMaxRows + row) * kHistK + h[w]];
+        const int ei = __float_as_int(e.y);
+        if (ei >= 0 && (bw < 0 || e.x > bs || (e.x == bs && ei < bi))) {
+          bs = e.x;
+          bi = ei;
+          bw = w;
+        }
       }
-    const bool a_ok = i < 15 && ai >= 0;
-    const bool b_ok = j < 15 && bi >= 0;
-    const bool take_a = a_ok && (!b_ok || as > bs || (as == bs && ai < bi));
-    s[k] = take_a ? as : (b_ok ? bs : -CUDART_INF_F);
-    id[k] = take_a ? ai : (b_ok ? bi : -1);
-    i += take_a ? 1 : 0;
-    j += (!take_a && b_ok) ? 1 : 0;
-  }
+    }
+    s[k] = bs;
+    id[k] = bi;
 #pragma unroll
-  for (int k = 0; k < 15; ++k) {
-    a.s[k] = s[k];
-    a.id[k] = id[k];
+    for (int w = 0; w < 4; ++w) h[w] += (bw == w) ? 1 : 0;
   }
 }
 
@@ -149,8 +199,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   using Lay = DecLayout<NQ>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kDecStages], raw_empty[kDecStages];
-  __shared__ __align__(8) uint64_t a_full[kDecA];
-  __shared__ __align__(8) uint64_t d_full[kDecD], d_empty[kDecD];
+  __shared__ __align__(8) uint64_t a_full[kDecSlices];
+  // d_full[h][s]: MMAs of slice s of the quads kq with kq % 2 == h are done.
+  // Split by quad parity so that every waiter takes each barrier's phases in
+  // order (a parity wait on phase k passes wrongly at phase k - 1 and blocks
+  // at phase k + 2): the epilogue waits d_full[kq % 2] at quad kq, and the
+  // dequant group of quad kq (A buffer free) waits d_full[(kq - 1) % 2].
+  __shared__ __align__(8) uint64_t d_full[2][kDecSlices], d_empty[2][kDecSlices];
   __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
@@ -160,7 +215,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   uint8_t* const base = smem_raw + (sbase - raw_u32);
-  float* const red = reinterpret_cast<float*>(base + Lay::kRedOff);
   int32_t* const pre = reinterpret_cast<int32_t*>(base + Lay::kPreOff);
 
   const int NR = p.num_reqs, R = p.R, c = blockIdx.x;
@@ -222,12 +276,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   if (tid == 0) {
     for (int s = 0; s < kDecStages; ++s) {
       mbar_init(smem_u32(&raw_full[s]), 1);
-      mbar_init(smem_u32(&raw_empty[s]), 128);
+      mbar_init(smem_u32(&raw_empty[s]), 32);   // one dequant warp reads a page
     }
-    for (int b = 0; b < kDecA; ++b) mbar_init(smem_u32(&a_full[b]), 128);
-    for (int d = 0; d < kDecD; ++d) {
-      mbar_init(smem_u32(&d_full[d]), 1);
-      mbar_init(smem_u32(&d_empty[d]), 128);
+    for (int b = 0; b < kDecSlices; ++b) {
+      mbar_init(smem_u32(&a_full[b]), 128);     // the quad's dequant warpgroup
+      mbar_init(smem_u32(&d_full[0][b]), 1);    // MMA commit
+      mbar_init(smem_u32(&d_full[1][b]), 1);
+      mbar_init(smem_u32(&d_empty[0][b]), 128); // epilogue warpgroup
+      mbar_init(smem_u32(&d_empty[1][b]), 128);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&q_full[k]), 256);   // both dequant groups write the tile
@@ -262,9 +318,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
 
   if (warp == 0) {
     // ================================================= producer (TMA)
-    // The whole warp walks the range; page ids are read 32 at a time (one
-    // coalesced load), so no copy waits on a page-table read; lane 0 issues.
-    int64_t g = 0;
+    // Quad kq fills stages 4 * (kq % 4) + q, q < 4; a page missing from a
+    // partial quad gets an arrival without data.  So stage s is filled once
+    // every four quads and read by one warp only (warp q of the dequant group
+    // of parity kq % 2), which waits its phases in order (an mbarrier parity
+    // wait cannot tell phase k from phase k + 2).  Up to four quads are in
+    // the ring: two being dequantised, two in flight from memory.
+    // The whole warp walks the range and reads page ids 32 at a time (one
+    // coalesced load; 32 is a multiple of the quad); lane 0 issues.
+    int64_t kq = 0;
+    int64_t last = -1;                                // lane s < 16: last quad that filled stage s
     bool ok = true;
     while (walk.more() && ok) {
       const int je = walk.seg_end();
@@ -272,29 +335,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       for (int jb = walk.j; jb < je && ok; jb += 32) {
         const int cnt = min(32, je - jb);
         const int my_phys = lane < cnt ? __ldg(row + jb + lane) : 0;
-        for (int k = 0; k < cnt; ++k, ++g) {
-          const int phys = __shfl_sync(0xffffffffu, my_phys, k);
-          int issued = 1;
-          if (lane == 0) {
-            const int s = (int)(g % kDecStages);
-            if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kDecStages) & 1) ^ 1), &abort_s)) {
-              fail();
-              issued = 0;
-            } else {
-              const uint32_t fb = smem_u32(&raw_full[s]);
-              if (phys < 0 || phys >= p.num_blocks) {
-                atomicOr(p.status, kStatusBadPage);
-                mbar_arrive(fb);
+        for (int k = 0; k < cnt && ok; k += 4, ++kq) {
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            const int phys = __shfl_sync(0xffffffffu, my_phys, (k + q) & 31);
+            const int s = 4 * (int)(kq % kQuadSlots) + q;
+            int issued = 1;
+            if (lane == 0) {
+              if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((kq / kQuadSlots) & 1) ^ 1),
+                                      &abort_s)) {
+                fail();
+                issued = 0;
               } else {
-                mbar_arrive_expect_tx(fb, kPageBytes);
-                bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-                         kPageBytes, fb);
+                const uint32_t fb = smem_u32(&raw_full[s]);
+                if (k + q >= cnt) {
+                  mbar_arrive(fb);
+                } else if (phys < 0 || phys >= p.num_blocks) {
+                  atomicOr(p.status, kStatusBadPage);
+                  mbar_arrive(fb);
+                } else {
+                  mbar_arrive_expect_tx(fb, kPageBytes);
+                  bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+                           kPageBytes, fb);
+                }
               }
             }
-          }
-          if (!__shfl_sync(0xffffffffu, issued, 0)) {
-            ok = false;
-            break;
+            if (!__shfl_sync(0xffffffffu, issued, 0)) {
+              ok = false;
+              break;
+            }
+            if (lane == s) last = kq;
           }
         }
       }
@@ -302,56 +372,73 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       walk.j = je;
       if (ok && walk.more()) walk.next_request();
     }
-    if (!ok && lane == 0) {   // drain issued copies before the CTA may exit
-      for (int64_t k = (g > kDecStages ? g - kDecStages : 0); k < g; ++k)
-        mbar_wait(smem_u32(&raw_full[k % kDecStages]), (uint32_t)((k / kDecStages) & 1));
-    }
+    // drain issued copies before the CTA may exit
+    if (!ok && lane < kDecStages && last >= 0)
+      mbar_wait(smem_u32(&raw_full[lane]), (uint32_t)((last / kQuadSlots) & 1));
   } else if (warp == 1 || warp == 2) {
     // ================================================= MMA issuers
+    // Issuer m takes slices m and m + 2 of every quad.
     if (lane == 0) {
-      const int mgrp = warp - 1;                      // pages with g % 2 == mgrp
+      const int m = warp - 1;
       constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
-      int64_t g = 0, g_last = -1;
+      int64_t kq = 0;
+      uint32_t last_bar = 0, last_par = 0;
       int sq = 0;
       while (walk.more() && !abort_s) {
         const int je = walk.seg_end();
         const int qs = sq & 1;
         if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
         const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
-        for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
-          if ((int)(g & 1) != mgrp) continue;
-          const int b = (int)(g % kDecA);
-          if (!mbar_wait_or_abort(smem_u32(&a_full[b]), (uint32_t)((g / kDecA) & 1), &abort_s)) { fail(); break; }
-          if (!mbar_wait_or_abort(smem_u32(&d_empty[b]), (uint32_t)(((g / kDecD) & 1) ^ 1), &abort_s)) { fail(); break; }
-          tc_fence_after();
-          const uint32_t d_t = tbase + 256 + b * 64;
-          const uint32_t a_t = tbase + b * 64;
+        bool ok = true;
+        for (; walk.j < je && ok; ++kq) {
+          const int npq = min(4, je - walk.j);
+          walk.j += npq;
+          walk.g += npq;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
-            mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+            const int sl = m + 2 * h;
+            if (!mbar_wait_or_abort(smem_u32(&a_full[sl]), (uint32_t)(kq & 1), &abort_s) ||
+                !mbar_wait_or_abort(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]), DecD<NQ>::phase(kq) ^ 1u,
+                                    &abort_s)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d_t = tbase + DecD<NQ>::col(kq, sl);
+            const uint32_t a_t = tbase + sl * 64;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
+              mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+            }
+            // d_full also tells the dequant warps that A buffer sl is free
+            mma_commit(smem_u32(&d_full[kq & 1][sl]));
+            last_bar = smem_u32(&d_full[kq & 1][sl]);
+            last_par = (uint32_t)((kq >> 1) & 1);
           }
-          // one commit per page: d_full[b] also tells the dequant warps that
-          // A buffer b is free again
-          mma_commit(smem_u32(&d_full[b]));
-          g_last = g;
         }
-        if (abort_s) break;
+        if (!ok || abort_s) break;
         mma_commit(smem_u32(&q_empty[qs]));
         ++sq;
         if (walk.more()) walk.next_request();
       }
-      if (abort_s && g_last >= 0) {   // drain issued MMAs before tensor memory is freed
-        mbar_wait(smem_u32(&d_full[g_last % kDecD]), (uint32_t)((g_last / kDecD) & 1));
-      }
+      // a commit covers every MMA issued before it: drain the last one
+      // before tensor memory is freed
+      if (abort_s && last_bar != 0) mbar_wait(last_bar, last_par);
     }
   } else if (warp < 11) {
     // ================================================= dequant warpgroups
-    const int grp = (warp - 3) >> 2;                 // takes pages with g % 2 == grp
-    const int tok = ((warp & 3) << 5) | lane;        // tensor-memory lane of this thread
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Group grp takes the quads of parity grp; warp q (tensor-memory lanes
+    // [32q, 32q+32)) dequantises page q of the quad, one 32-token slice at a
+    // time, into its lane quarter of A buffer s.  A warp of a partial quad
+    // with no page still takes part in every barrier (its lanes of the A
+    // buffer then hold stale finite values whose scores nobody reads).
+    const int grp = (warp - 3) >> 2;
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int dq = tid - kDqTid0;                     // 0..255 (both groups share the query tile)
-    int64_t g = 0;
+    int64_t kq = 0;
     int sq = 0;
     bool ok = true;
     while (walk.more() && ok) {
@@ -378,146 +465,182 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&q_full[qs]));
-      for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
-        if ((int)(g & 1) != grp) continue;
-        const int s = (int)(g % kDecStages);
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
-                                                         (uint32_t)((g / kDecStages) & 1), &abort_s))) {
+      for (; walk.j < je && ok; ++kq) {
+        const int npq = min(4, je - walk.j);
+        walk.j += npq;
+        walk.g += npq;
+        if ((int)(kq & 1) != grp) continue;
+        const bool has = q < npq;
+        const int st = 4 * (int)(kq % kQuadSlots) + q;  // this warp's stage (see the producer)
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[st]),
+                                                         (uint32_t)((kq / kQuadSlots) & 1), &abort_s))) {
           fail();
           ok = false;
           break;
         }
-        uint32_t w[18];
-        {
-          const uint2* src = reinterpret_cast<const uint2*>(base + Lay::kStageOff + s * kPageBytes + tok * kRowBytes);
+        if (!has) mbar_arrive(smem_u32(&raw_empty[st]));
+        const uint2* const page = reinterpret_cast<const uint2*>(base + Lay::kStageOff + st * kPageBytes);
+#pragma unroll 1
+        for (int sl = 0; sl < kDecSlices; ++sl) {
+          uint32_t a[64];
+          if (has) {
+            uint32_t w[18];
+            const uint2* src = page + (sl * 32 + lane) * (kRowBytes / 8);
 #pragma unroll
-          for (int i = 0; i < 9; ++i) {
-            const uint2 t2 = src[i];
-            w[2 * i] = t2.x;
-            w[2 * i + 1] = t2.y;
-          }
-        }
-        mbar_arrive(smem_u32(&raw_empty[s]));
-        uint32_t a[64];
-        {
-          const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
-                                  e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
+            for (int i = 0; i < 9; ++i) {
+              const uint2 t2 = src[i];
+              w[2 * i] = t2.x;
+              w[2 * i + 1] = t2.y;
+            }
+            if (sl == kDecSlices - 1) mbar_arrive(smem_u32(&raw_empty[st]));
+            const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
+                                    e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
 #pragma unroll
-          for (int g8 = 0; g8 < 8; ++g8) {
-            const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
-            dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
+            for (int g8 = 0; g8 < 8; ++g8) {
+              const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
+              dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
+            }
           }
+          // A buffer sl is free once the MMAs of quad kq - 1 are done
+          if (kq >= 1 &&
+              !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[(kq - 1) & 1][sl]),
+                                                           (uint32_t)(((kq - 1) >> 1) & 1), &abort_s))) {
+            fail();
+            ok = false;
+            break;
+          }
+          if (has) {
+            tc_fence_after();
+            tmem_st_32x32b_x64(tbase + lane_base + sl * 64, a);
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&a_full[sl]));
         }
-        // A buffer b was last read by the MMAs of page g - kDecA, whose
-        // completion is phase g / kDecA - 1 of d_full[b]; the next phase of
-        // that barrier needs this page's A, so the parity cannot alias.
-        const int b = (int)(g % kDecA);
-        if (g >= kDecA &&
-            !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[b]),
-                                                         (uint32_t)(((g / kDecA) - 1) & 1), &abort_s))) {
-          fail();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        tmem_st_32x32b_x64(tbase + lane_base + b * 64, a);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&a_full[b]));
       }
       ++sq;
       if (ok && walk.more()) walk.next_request();
     }
   } else {
-    // ================================================= epilogue warpgroups
-    // Group `grp` scores pages with g % 2 == grp and keeps its own running
-    // top-15 per row; at a segment end group 1 hands its lists to group 0
-    // through shared memory and group 0 merges and writes the result.  The
-    // walk is never left early, so every barrier is always reached.
-    const int grp = (warp - 11) >> 2;
-    const int ep = (tid - kEpTid0) & 127;             // row owner within the group
-    const int wq = warp & 3;                          // tensor-memory lane quarter
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t bar_grp = 2 + grp, bar_both = 4;
-    float2* const mrg = reinterpret_cast<float2*>(base + Lay::kMrgOff);   // [2][64][15] by segment parity
-    constexpr int CW = NQ < 32 ? NQ : 32;             // columns per load + reduction pass
-    TopK15 top;
-    int64_t g = 0;
-    int sq = 0;
-    bool ok = true;                                   // uniform within the group
+    // ================================================= epilogue warpgroup
+    // Warp q owns page q of every quad: per slice it loads its lanes' NQ
+    // columns of D buffer s and keeps the running max over slices; after the
+    // 4th slice a butterfly transpose-reduction over the lanes gives the page
+    // score of every row (lane l gets rows l and l + 32).  Each warp keeps its own top-15 per
+    // row in shared memory (threshold in a register); at a segment end the
+    // four lists of each row are merged.  The walk is never left early, so
+    // every barrier is always reached.
+    const int q = warp & 3;
+    const int ep = tid - kEpTid0;                     // 0..127: row owner at the merge
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float2* const lists = reinterpret_cast<float2*>(base + Lay::kListOff);   // [4][64][15]
+    float2* const my0 = lists + (q * kMaxRows + lane) * kHistK;              // row lane
+    float2* const my1 = my0 + 32 * kHistK;                                   // row lane + 32
+    constexpr int CW = NQ < 32 ? NQ : 32;             // columns per load + max pass
+    int64_t kq = 0;
+    bool ok = true;                                   // uniform within the warp
     while (walk.more()) {
       const int je = walk.seg_end();
       const int r = walk.r;
       const int seq_r = __ldg(p.seq_lens + r);
-      const int pos = seq_r - p.qlen + ep / p.H;
-      const int L = pos >= 0 ? (pos >> 7) : -1;
+      const int pos0 = seq_r - p.qlen + lane / p.H, pos1 = seq_r - p.qlen + (lane + 32) / p.H;
+      const int L0 = pos0 >= 0 ? (pos0 >> 7) : -1, L1 = pos1 >= 0 ? (pos1 >> 7) : -1;
       // an unreadable page id anywhere in the segment: checked once, up front
       int seg_bad = 0;
-      if (grp == 0) {
-        for (int jj = walk.j + ep; jj < je; jj += 128) {
-          const int ph = __ldg(p.page_table + (int64_t)r * p.pt_stride + jj);
-          seg_bad |= (ph < 0 || ph >= p.num_blocks);
-        }
+      for (int jj = walk.j + ep; jj < je; jj += 128) {
+        const int ph = __ldg(p.page_table + (int64_t)r * p.pt_stride + jj);
+        seg_bad |= (ph < 0 || ph >= p.num_blocks);
       }
+      // NQ <= 32: one row per lane, its top-15 in registers; NQ = 64: two
+      // rows per lane, sorted lists in shared memory behind a threshold
+      TopK15 top;
       top.reset();
-      for (; walk.j < je; ++walk.j, ++walk.g, ++g) {
-        if ((int)(g & 1) != grp) continue;
-        const int d = (int)(g % kDecD);
-        int wok = 0;
-        if (ok) {
-          wok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[d]),
-                                                            (uint32_t)((g / kDecD) & 1), &abort_s));
-          if (!wok) fail();
-        }
-        float* rd = red + (grp * 2 + ((g >> 1) & 1)) * (4 * NQ);
-        if (wok) {
-          tc_fence_after();
+      float thr0 = -CUDART_INF_F, thr1 = -CUDART_INF_F;
+      if constexpr (NQ > 32) {
 #pragma unroll
-          for (int ch = 0; ch < NQ / CW; ++ch) {
-            float v[CW];
-            tmem_ld_row<CW>(tbase + lane_base + 256 + d * 64 + ch * CW, v);
-            tmem_wait_ld();
-            const float m = warp_colmax<CW>(v, lane);
-            if (lane < CW) rd[wq * NQ + ch * CW + lane] = m;
-          }
-          tc_fence_before();
-          mbar_arrive(smem_u32(&d_empty[d]));
-        }
-        ok = !named_bar_red_or(bar_grp, 128, (!wok || abort_s) ? 1 : 0);
-        if (ok && ep < R) {
-          const int jp = walk.j;
-          const float sc = canon_zero(fmaxf(fmaxf(rd[ep], rd[NQ + ep]), fmaxf(rd[2 * NQ + ep], rd[3 * NQ + ep])));
-          if (jp < L) {
-            top.insert(sc, jp);
-            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + ep) * p.dbg_stride + jp] = sc;
-          }
+        for (int k = 0; k < kHistK; ++k) {
+          my0[k] = make_float2(-CUDART_INF_F, __int_as_float(-1));
+          my1[k] = make_float2(-CUDART_INF_F, __int_as_float(-1));
         }
       }
-      // ---- hand group 1's lists to group 0, merge, finalise the segment
-      float2* mb = mrg + (sq & 1) * (kMaxRows * kHistK);
-      if (grp == 1 && ep < R) {
+      for (; walk.j < je; ++kq) {
+        const int npq = min(4, je - walk.j);
+        const int jp = walk.j + q;                    // this warp's page
+        const bool has = q < npq;
+        walk.j += npq;
+        walk.g += npq;
+        float run[NQ];
 #pragma unroll
-        for (int k = 0; k < kHistK; ++k) mb[ep * kHistK + k] = make_float2(top.s[k], __int_as_float(top.id[k]));
-      }
-      named_bar_sync(bar_both, 256);
-      if (grp == 0) {
-        const int bad = named_bar_red_or(bar_grp, 128, seg_bad);
-        if (ok) {
-          const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
-          if (ep < R) {
-            merge_top15(top, mb + ep * kHistK);
-            if (cf == cl) {
-              write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, top.id, L, bad != 0);
-            } else {
-              float2* dst = p.cand + ((int64_t)(c + r) * R + ep) * kHistK;
+        for (int sl = 0; sl < kDecSlices; ++sl) {
+          if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[kq & 1][sl]),
+                                                             (uint32_t)((kq >> 1) & 1), &abort_s));
+            if (!ok) fail();
+          }
+          if (ok) {
+            tc_fence_after();
+            if (has) {
+              const uint32_t ta = tbase + lane_base + DecD<NQ>::col(kq, sl);
+              if (sl == 0) {
+                tmem_ld_row<NQ>(ta, run);
+                tmem_wait_ld();
+              } else {
 #pragma unroll
-              for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+                for (int ch = 0; ch < NQ / CW; ++ch) {
+                  float t[CW];
+                  tmem_ld_row<CW>(ta + ch * CW, t);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < CW; ++i) run[ch * CW + i] = fmaxf(run[ch * CW + i], t[i]);
+                }
+              }
             }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]));
           }
-          if (ep == 0 && cf != cl) p.slot_bad[c + r] = bad;
+        }
+        if (ok && has) {
+          // rows lane and lane + 32: max over the warp's 32 token lanes
+          float m0 = warp_colmax<NQ < 32 ? NQ : 32>(run, lane), m1 = 0.0f;
+          if constexpr (NQ > 32) m1 = warp_colmax<32>(run + 32, lane);
+          m0 = canon_zero(m0);
+          m1 = canon_zero(m1);
+          if (lane < R && jp < L0) {
+            if constexpr (NQ <= 32) top.insert(m0, jp);
+            else if (m0 > thr0) thr0 = list_insert15(my0, m0, jp);
+            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane) * p.dbg_stride + jp] = m0;
+          }
+          if (NQ > 32 && lane + 32 < R && jp < L1) {
+            if (m1 > thr1) thr1 = list_insert15(my1, m1, jp);
+            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane + 32) * p.dbg_stride + jp] = m1;
+          }
         }
       }
-      ++sq;
+      // ---- merge the four warps' lists of each row, finalise the segment
+      if constexpr (NQ <= 32) {
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) my0[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+      }
+      const int bad = named_bar_red_or(2, 128, seg_bad);
+      const int failed = named_bar_red_or(3, 128, (!ok || abort_s) ? 1 : 0);
+      if (!failed) {
+        const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+        if (ep < R) {
+          float ts[kHistK];
+          int ti[kHistK];
+          merge4_top15(lists, ep, ts, ti);
+          const int pe = seq_r - p.qlen + ep / p.H;
+          if (cf == cl) {
+            write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, ti, pe >= 0 ? (pe >> 7) : -1, bad != 0);
+          } else {
+            float2* dst = p.cand + ((int64_t)(c + r) * R + ep) * kHistK;
+#pragma unroll
+            for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(ts[k], __int_as_float(ti[k]));
+          }
+        }
+        if (ep == 0 && cf != cl) p.slot_bad[c + r] = bad;
+      }
+      named_bar_sync(2, 128);                         // lists are read before the next reset
       if (walk.more()) walk.next_request();
     }
   }
