@@ -48,6 +48,13 @@ struct PreLayout {
   static size_t bytes(int num_reqs) { return 1024 + kTpreOff + (size_t)(num_reqs + 1) * 4; }
 };
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 struct TileInfo {
   int r, t0, nt, L_max, ctx, row0;   // row0 = first token (q row) of the tile
   bool table_bad;
@@ -391,8 +398,21 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           tmem_ld_32x32b_x16(dt + half * 64 + 32, v + 32);
           tmem_ld_32x32b_x16(dt + half * 64 + 48, v + 48);
           tmem_wait_ld();
+          // max over the 64 columns as four independent chains of
+          // three-input maxima: one dependent chain of 64 maxima would be
+          // the epilogue's critical path, and the epilogue paces the MMAs
+          float ma = fmax3(v[0], v[1], v[2]), mb = fmax3(v[3], v[4], v[5]), mc = fmax3(v[6], v[7], v[8]),
+                md = fmax3(v[9], v[10], v[11]);
 #pragma unroll
-          for (int i = 0; i < 64; i += 2) m = fmaxf(m, fmaxf(v[i], v[i + 1]));
+          for (int i = 12; i < 60; i += 8) {
+            ma = fmax3(ma, v[i], v[i + 1]);
+            mb = fmax3(mb, v[i + 2], v[i + 3]);
+            mc = fmax3(mc, v[i + 4], v[i + 5]);
+            md = fmax3(md, v[i + 6], v[i + 7]);
+          }
+          ma = fmax3(ma, v[60], v[61]);
+          mb = fmax3(mb, v[62], v[63]);
+          m = fmax3(m, fmaxf(ma, mb), fmaxf(mc, md));
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&d_empty[d]));

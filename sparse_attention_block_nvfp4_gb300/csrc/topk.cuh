@@ -24,19 +24,25 @@ struct TopK15 {
   }
 
   // Insert (v, j); j must exceed every id inserted before with the same score.
+  // Every entry computes its new value independently: entries scoring >= v
+  // stay (equal scores keep the earlier, lower id ahead), the first entry
+  // below v takes (v, j), the rest move down one place.
   __device__ __forceinline__ void insert(float v, int j) {
     if (v > s[14]) {
-      s[14] = v;
-      id[14] = j;
+      bool ge[15];
+#pragma unroll
+      for (int i = 0; i < 15; ++i) ge[i] = s[i] >= v;
 #pragma unroll
       for (int i = 14; i > 0; --i) {
-        const bool up = s[i] > s[i - 1];
-        const float ts = s[i], tu = s[i - 1];
-        const int ti = id[i], tj = id[i - 1];
-        s[i - 1] = up ? ts : tu;
-        s[i] = up ? tu : ts;
-        id[i - 1] = up ? ti : tj;
-        id[i] = up ? tj : ti;
+        const bool here = !ge[i] && ge[i - 1];
+        const float si = ge[i] ? s[i] : (here ? v : s[i - 1]);
+        const int ii = ge[i] ? id[i] : (here ? j : id[i - 1]);
+        s[i] = si;
+        id[i] = ii;
+      }
+      if (!ge[0]) {
+        s[0] = v;
+        id[0] = j;
       }
     }
   }
