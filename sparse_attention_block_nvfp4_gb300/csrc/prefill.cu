@@ -12,18 +12,20 @@
 // request (the last tile of a request may be ragged); its rows sit in tensor
 // memory as the MMA's A operand (M = 128, K = 128).  Tiles of a request are
 // visited last-first (they hold the most pages) and dealt round-robin to the
-// CTAs, one CTA per SM.  Warp roles, linked by mbarrier rings:
-//   * producer warp: the TMA unit copies each raw 9216-byte page into a
-//     6-stage shared ring;
-//   * two dequant warpgroups, alternating pages: thread t dequantises token t
-//     to fp16 into a 128B-swizzled K-major B tile [128 tokens x 128] (4 tiles
-//     deep);
-//   * two MMA warps, alternate pages: one thread each issues 8 tcgen05.mma
-//     per page, D[row][token] = Q . K^T in fp32, 3 accumulators deep;
-//   * epilogue warpgroup, thread = query row: widens the next tile's queries
-//     into tensor memory (2 buffers), loads its D row per page, takes the max
-//     over the 128 tokens and updates its running top-15 if the page is a
-//     history page of its token; writes the row at the end of the tile.
+// CTAs, one CTA per SM.  Warp roles, linked by mbarrier rings, one role per
+// warpgroup so that registers can move between them (setmaxnreg):
+//   * warpgroup 0 (40 registers): warp 0 has the TMA unit copy each raw
+//     9216-byte page into a 6-stage shared ring; warps 1 and 2 take alternate
+//     pages, one thread each issuing 8 tcgen05.mma per page, D[row][token] =
+//     Q . K^T in fp32, 3 accumulators deep; warp 3 idles;
+//   * warpgroups 1 and 2 (dequant, alternating pages): thread t dequantises
+//     token t to fp16 into a 128B-swizzled K-major B tile [128 tokens x 128]
+//     (4 tiles deep);
+//   * warpgroup 3 (epilogue, 208 registers), thread = query row: widens the
+//     next tile's queries into tensor memory (2 buffers), loads its whole
+//     128-column row of D per page in one round trip, takes the max over the
+//     tokens and updates its running top-15 if the page is a history page of
+//     its token; writes the row at the end of the tile.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -37,7 +39,12 @@ namespace nvfp4idx {
 constexpr int kPreStages = 6;              // raw page ring
 constexpr int kPreB = 4;                   // dequantised B tiles
 constexpr int kPreD = 3;                   // accumulators: columns [128 + 128d, 256 + 128d)
-constexpr int kPreThreads = 480;           // warp 0 TMA, 1 / 14 MMA issue, 2-5 / 6-9 dequant, 10-13 epilogue
+// warpgroup 0: warp 0 TMA, warps 1 / 2 MMA issue, warp 3 idle (registers
+// lowered to 40); warpgroups 1 / 2: dequant (128); warpgroup 3: epilogue
+// (raised to 208, so a thread holds its whole 128-column row of D).
+// 4 x 40 + 8 x 128 + 4 x 208 registers x 32 lanes = 64512 <= 512 x 128.
+constexpr int kPreThreads = 512;
+constexpr uint32_t kRegsCtl = 40, kRegsEpi = 208;
 constexpr uint32_t kPreTmemCols = 512;     // queries [0,64) and [64,128), accumulators [128,512)
 constexpr uint32_t kBTileBytes = 128 * 256;  // fp16 [2 K-blocks][128 tokens][64]
 
@@ -177,76 +184,81 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     }
   };
 
-  if (warp == 0) {
-    // ================================================= producer (TMA)
-    if (lane == 0) {
-      int64_t g = 0;
-      for (int t = c; t < NT && !abort_s; t += G) {
-        const TileInfo ti = prefill_tile<H>(p, tpre, t);
-        for (int j = 0; j < ti.L_max; ++j, ++g) {
-          const int s = (int)(g % kPreStages);
-          if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1), &abort_s)) {
-            fail();
-            break;
-          }
-          const uint32_t fb = smem_u32(&raw_full[s]);
-          const int phys = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + j);
-          if (phys < 0 || phys >= p.num_blocks) {
-            mbar_arrive(fb);
-          } else {
-            mbar_arrive_expect_tx(fb, kPageBytes);
-            bulk_g2s(sbase + PreLayout::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-                     kPageBytes, fb);
+  if (warp < 4) {
+    // warpgroup 0 gives registers back to the epilogue (executed by all
+    // four warps of the warpgroup, warp 3 has no other role)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == 0) {
+      // ================================================= producer (TMA)
+      if (lane == 0) {
+        int64_t g = 0;
+        for (int t = c; t < NT && !abort_s; t += G) {
+          const TileInfo ti = prefill_tile<H>(p, tpre, t);
+          for (int j = 0; j < ti.L_max; ++j, ++g) {
+            const int s = (int)(g % kPreStages);
+            if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1), &abort_s)) {
+              fail();
+              break;
+            }
+            const uint32_t fb = smem_u32(&raw_full[s]);
+            const int phys = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + j);
+            if (phys < 0 || phys >= p.num_blocks) {
+              mbar_arrive(fb);
+            } else {
+              mbar_arrive_expect_tx(fb, kPageBytes);
+              bulk_g2s(sbase + PreLayout::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+                       kPageBytes, fb);
+            }
           }
         }
-      }
-      if (abort_s) {
-        for (int64_t k = (g > kPreStages ? g - kPreStages : 0); k < g; ++k)
-          mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
-      }
-    }
-  } else if (warp == 1 || warp == 14) {
-    // ================================================= MMA issuers
-    // Two issuing threads take alternate pages, so that one thread's commits
-    // and waits overlap the other's MMAs and the tensor core stays busy.
-    if (lane == 0) {
-      const int mgrp = warp == 1 ? 0 : 1;
-      constexpr uint32_t idesc = idesc_f16_f32(128, 128);
-      int64_t g = 0, g_last = -1;
-      int kq = 0;
-      for (int t = c; t < NT && !abort_s; t += G) {
-        const TileInfo ti = prefill_tile<H>(p, tpre, t);
-        if (ti.L_max == 0) continue;
-        const int qb = kq & 1;
-        if (!mbar_wait_or_abort(smem_u32(&q_full[qb]), (uint32_t)((kq >> 1) & 1), &abort_s)) { fail(); break; }
-        for (int j = 0; j < ti.L_max; ++j, ++g) {
-          if ((int)(g & 1) != mgrp) continue;
-          const int nb = (int)(g % kPreB), d = (int)(g % kPreD);
-          if (!mbar_wait_or_abort(smem_u32(&b_full[nb]), (uint32_t)((g / kPreB) & 1), &abort_s)) { fail(); break; }
-          if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kPreD) & 1) ^ 1), &abort_s)) { fail(); break; }
-          tc_fence_after();
-          const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)nb * kBTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(bt + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-            mma_f16_tmemA(tbase + 128 + d * 128, tbase + qb * 64 + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&b_empty[nb]));
-          mma_commit(smem_u32(&d_full[d]));
-          g_last = g;
+        if (abort_s) {
+          for (int64_t k = (g > kPreStages ? g - kPreStages : 0); k < g; ++k)
+            mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
         }
-        if (abort_s) break;
-        mma_commit(smem_u32(&q_empty[qb]));
-        ++kq;
       }
-      if (abort_s && g_last >= 0) {
-        const int64_t k = g_last;
-        mbar_wait(smem_u32(&d_full[k % kPreD]), (uint32_t)((k / kPreD) & 1));
+    } else if (warp == 1 || warp == 2) {
+      // ================================================= MMA issuers
+      // Two issuing threads take alternate pages, so that one thread's commits
+      // and waits overlap the other's MMAs and the tensor core stays busy.
+      if (lane == 0) {
+        const int mgrp = warp - 1;
+        constexpr uint32_t idesc = idesc_f16_f32(128, 128);
+        int64_t g = 0, g_last = -1;
+        int kq = 0;
+        for (int t = c; t < NT && !abort_s; t += G) {
+          const TileInfo ti = prefill_tile<H>(p, tpre, t);
+          if (ti.L_max == 0) continue;
+          const int qb = kq & 1;
+          if (!mbar_wait_or_abort(smem_u32(&q_full[qb]), (uint32_t)((kq >> 1) & 1), &abort_s)) { fail(); break; }
+          for (int j = 0; j < ti.L_max; ++j, ++g) {
+            if ((int)(g & 1) != mgrp) continue;
+            const int nb = (int)(g % kPreB), d = (int)(g % kPreD);
+            if (!mbar_wait_or_abort(smem_u32(&b_full[nb]), (uint32_t)((g / kPreB) & 1), &abort_s)) { fail(); break; }
+            if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kPreD) & 1) ^ 1), &abort_s)) { fail(); break; }
+            tc_fence_after();
+            const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)nb * kBTileBytes;
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(bt + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
+              mma_f16_tmemA(tbase + 128 + d * 128, tbase + qb * 64 + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&b_empty[nb]));
+            mma_commit(smem_u32(&d_full[d]));
+            g_last = g;
+          }
+          if (abort_s) break;
+          mma_commit(smem_u32(&q_empty[qb]));
+          ++kq;
+        }
+        if (abort_s && g_last >= 0) {
+          const int64_t k = g_last;
+          mbar_wait(smem_u32(&d_full[k % kPreD]), (uint32_t)((k / kPreD) & 1));
+        }
       }
     }
-  } else if (warp < 10) {
+  } else if (warp < 12) {
     // ================================================= dequant warpgroups
-    const int grp = (warp - 2) >> 2;                 // 0 or 1: takes pages with g % 2 == grp
+    const int grp = (warp - 4) >> 2;                 // 0 or 1: takes pages with g % 2 == grp
     const int tok = ((warp & 3) << 5) | lane;        // token row of the page / of the B tile
     int64_t g = 0;
     bool ok = true;
@@ -301,6 +313,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     }
   } else {
     // ================================================= epilogue warpgroup
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     const int n = ((warp & 3) << 5) | lane;          // query row = tensor-memory lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     TopK15 top;
@@ -389,31 +402,22 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         }
         tc_fence_after();
         const uint32_t dt = tbase + lane_base + 128 + d * 128;
-        float m = -CUDART_INF_F;
+        float v[128];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[64];
-          tmem_ld_32x32b_x16(dt + half * 64 + 0, v);
-          tmem_ld_32x32b_x16(dt + half * 64 + 16, v + 16);
-          tmem_ld_32x32b_x16(dt + half * 64 + 32, v + 32);
-          tmem_ld_32x32b_x16(dt + half * 64 + 48, v + 48);
-          tmem_wait_ld();
-          // max over the 64 columns as four independent chains of
-          // three-input maxima: one dependent chain of 64 maxima would be
-          // the epilogue's critical path, and the epilogue paces the MMAs
-          float ma = fmax3(v[0], v[1], v[2]), mb = fmax3(v[3], v[4], v[5]), mc = fmax3(v[6], v[7], v[8]),
-                md = fmax3(v[9], v[10], v[11]);
+        for (int c16 = 0; c16 < 128; c16 += 16) tmem_ld_32x32b_x16(dt + c16, v + c16);
+        tmem_wait_ld();
+        float ma = fmax3(v[0], v[1], v[2]), mb = fmax3(v[3], v[4], v[5]), mc = fmax3(v[6], v[7], v[8]),
+              md = fmax3(v[9], v[10], v[11]);
 #pragma unroll
-          for (int i = 12; i < 60; i += 8) {
-            ma = fmax3(ma, v[i], v[i + 1]);
-            mb = fmax3(mb, v[i + 2], v[i + 3]);
-            mc = fmax3(mc, v[i + 4], v[i + 5]);
-            md = fmax3(md, v[i + 6], v[i + 7]);
-          }
-          ma = fmax3(ma, v[60], v[61]);
-          mb = fmax3(mb, v[62], v[63]);
-          m = fmax3(m, fmaxf(ma, mb), fmaxf(mc, md));
+        for (int i = 12; i < 124; i += 8) {
+          ma = fmax3(ma, v[i], v[i + 1]);
+          mb = fmax3(mb, v[i + 2], v[i + 3]);
+          mc = fmax3(mc, v[i + 4], v[i + 5]);
+          md = fmax3(md, v[i + 6], v[i + 7]);
         }
+        ma = fmax3(ma, v[124], v[125]);
+        mb = fmax3(mb, v[126], v[127]);
+        float m = fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
         tc_fence_before();
         mbar_arrive(smem_u32(&d_empty[d]));
         m = canon_zero(m);
