@@ -16,27 +16,28 @@
 // scores of 32 tokens of ITS page; after the 4 slices that warp has seen all
 // 128 tokens of the page and takes the max over them alone: an in-register
 // max over the slices, then a reduction over its 32 lanes, with no exchange
-// between warps.  One CTA per SM, warp roles linked by mbarrier
-// rings (slice s of every quad uses A buffer s and D buffer s):
-//   * producer warp: reads page ids 32 at a time and has the TMA unit copy
-//     each 9216-byte page into an 8-stage shared ring (cp.async.bulk,
-//     transaction-count completion);
-//   * two dequant warpgroups (quads of even / odd index): warp q reads the
+// between warps.  One CTA per SM, 16 warps, one role per warpgroup (so that
+// setmaxnreg can move registers to the epilogue), linked by mbarrier rings
+// (slice s of every quad uses A buffer s and D buffer s):
+//   * warpgroup 0 (88 registers): warp 0 reads page ids 32 at a time and has
+//     the TMA unit copy each 9216-byte page into a 16-stage shared ring
+//     (cp.async.bulk, transaction-count completion); warps 1 / 2 (slices of
+//     even / odd index) each have one thread issue the 8 tcgen05.mma (K = 16)
+//     of a slice into D buffer s and commit once (a single thread cannot
+//     issue small-N MMAs as fast as the tensor core retires them); warp 3
+//     idles;
+//   * warpgroups 1 / 2 (dequant, 112 registers, quads of even / odd index): warp q reads the
 //     72-byte rows of tokens 32s + lane of page q, dequantises them exactly to
 //     fp16 (E2M1 x E4M3 fits fp16) and stores them into its lane quarter of A
 //     buffer s (tcgen05.st), the MMA's A operand (M = 128 lanes, K = 128); at
 //     each segment start both widen the request's E4M3 queries to fp16 into a
 //     128B-swizzled B tile (double buffered);
-//   * two MMA warps (slices of even / odd index): one thread each issues 8
-//     tcgen05.mma (K = 16) per slice into D buffer s, and commits once (a
-//     single thread cannot issue small-N MMAs as fast as the tensor core
-//     retires them);
-//   * epilogue warpgroup: warp q keeps the running max of its page's tokens
-//     over the 4 slices, reduces it over its lanes (butterfly shuffles that
-//     leave column k in lane k), and lane k inserts the
-//     page score of rows k and k + 32 into their running top-15 (threshold in
-//     a register, list in shared memory); at a segment end the four warps'
-//     lists of each row are merged.
+//   * warpgroup 3 (epilogue, 200 registers): warp q keeps the running max of
+//     its page's tokens over the 4 slices, reduces it over its lanes
+//     (butterfly shuffles that leave column k in lane k), and lane k inserts
+//     the page score of rows k and k + 32 into their running top-15 in
+//     registers; at a segment end the four warps' lists of each row are
+//     merged.
 // A request covered by one CTA is finalised in place; otherwise each segment
 // leaves its 15 candidates per row in scratch and decode_merge_kernel merges
 // them (and writes the rows of requests with no history page).
@@ -53,9 +54,13 @@ namespace nvfp4idx {
 constexpr int kQuadSlots = 4;            // raw page ring: quad kq fills stages 4 * (kq % 4) + q
 constexpr int kDecStages = 4 * kQuadSlots;
 constexpr int kDecSlices = 4;            // slice s: A buffer s (columns [64s, 64s+64))
-// warp 0 TMA; 1 / 2 MMA issue; 3-6 / 7-10 dequant; 11-14 epilogue
-constexpr int kDecThreads = 480;
-constexpr int kDqTid0 = 96, kEpTid0 = 352;
+// One role per warpgroup, so that setmaxnreg can move registers between
+// them: warpgroup 0 (88 registers) = warp 0 TMA, warps 1 / 2 MMA issue,
+// warp 3 idle; warpgroups 1 / 2 dequant (112); warpgroup 3 epilogue (200).
+// 4 x 88 + 8 x 112 + 4 x 200 registers x 32 lanes = 65536 = 512 x 128.
+constexpr int kDecThreads = 512;
+constexpr int kDqTid0 = 128, kEpTid0 = 384;
+constexpr uint32_t kDecRegsCtl = 88, kDecRegsDq = 112, kDecRegsEpi = 200;
 constexpr uint32_t kDecTmemCols = 512;
 
 // D buffers in tensor memory from column 256: for NQ <= 32 two sets of four
@@ -99,21 +104,6 @@ __device__ __forceinline__ int hist_pages(int seq_len, int pt_stride) {
 // CTA owning global page x when T pages are split over G CTAs.
 __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
   return (int)(((x + 1) * G - 1) / T);
-}
-
-// Insert (v, j) into a sorted top-15 list in shared memory (score desc; id -1
-// = empty) when v beats its last entry; j exceeds every id already in it, so
-// it goes after equal scores.  Returns the list's new last score.
-__device__ __forceinline__ float list_insert15(float2* l, float v, int j) {
-  int k = kHistK - 1;
-  while (k > 0) {
-    const float2 prev = l[k - 1];
-    if (prev.x >= v) break;
-    l[k] = prev;
-    --k;
-  }
-  l[k] = make_float2(v, __int_as_float(j));
-  return l[kHistK - 1].x;
 }
 
 // Column maxima over the warp's 32 lanes by butterfly transpose-reduction:
@@ -316,125 +306,131 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     }
   };
 
-  if (warp == 0) {
-    // ================================================= producer (TMA)
-    // Quad kq fills stages 4 * (kq % 4) + q, q < 4; a page missing from a
-    // partial quad gets an arrival without data.  So stage s is filled once
-    // every four quads and read by one warp only (warp q of the dequant group
-    // of parity kq % 2), which waits its phases in order (an mbarrier parity
-    // wait cannot tell phase k from phase k + 2).  Up to four quads are in
-    // the ring: two being dequantised, two in flight from memory.
-    // The whole warp walks the range and reads page ids 32 at a time (one
-    // coalesced load; 32 is a multiple of the quad); lane 0 issues.
-    int64_t kq = 0;
-    int64_t last = -1;                                // lane s < 16: last quad that filled stage s
-    bool ok = true;
-    while (walk.more() && ok) {
-      const int je = walk.seg_end();
-      const int32_t* row = p.page_table + (int64_t)walk.r * p.pt_stride;
-      for (int jb = walk.j; jb < je && ok; jb += 32) {
-        const int cnt = min(32, je - jb);
-        const int my_phys = lane < cnt ? __ldg(row + jb + lane) : 0;
-        for (int k = 0; k < cnt && ok; k += 4, ++kq) {
-#pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
-            const int phys = __shfl_sync(0xffffffffu, my_phys, (k + q) & 31);
-            const int s = 4 * (int)(kq % kQuadSlots) + q;
-            int issued = 1;
-            if (lane == 0) {
-              if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((kq / kQuadSlots) & 1) ^ 1),
-                                      &abort_s)) {
-                fail();
-                issued = 0;
-              } else {
-                const uint32_t fb = smem_u32(&raw_full[s]);
-                if (k + q >= cnt) {
-                  mbar_arrive(fb);
-                } else if (phys < 0 || phys >= p.num_blocks) {
-                  atomicOr(p.status, kStatusBadPage);
-                  mbar_arrive(fb);
+  if (warp < 4) {
+    // warpgroup 0 gives registers back to the epilogue (executed by all
+    // four warps of the warpgroup, warp 3 has no other role)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsCtl));
+    if (warp == 0) {
+      // ================================================= producer (TMA)
+      // Quad kq fills stages 4 * (kq % 4) + q, q < 4; a page missing from a
+      // partial quad gets an arrival without data.  So stage s is filled once
+      // every four quads and read by one warp only (warp q of the dequant group
+      // of parity kq % 2), which waits its phases in order (an mbarrier parity
+      // wait cannot tell phase k from phase k + 2).  Up to four quads are in
+      // the ring: two being dequantised, two in flight from memory.
+      // The whole warp walks the range and reads page ids 32 at a time (one
+      // coalesced load; 32 is a multiple of the quad); lane 0 issues.
+      int64_t kq = 0;
+      int64_t last = -1;                                // lane s < 16: last quad that filled stage s
+      bool ok = true;
+      while (walk.more() && ok) {
+        const int je = walk.seg_end();
+        const int32_t* row = p.page_table + (int64_t)walk.r * p.pt_stride;
+        for (int jb = walk.j; jb < je && ok; jb += 32) {
+          const int cnt = min(32, je - jb);
+          const int my_phys = lane < cnt ? __ldg(row + jb + lane) : 0;
+          for (int k = 0; k < cnt && ok; k += 4, ++kq) {
+  #pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              const int phys = __shfl_sync(0xffffffffu, my_phys, (k + q) & 31);
+              const int s = 4 * (int)(kq % kQuadSlots) + q;
+              int issued = 1;
+              if (lane == 0) {
+                if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((kq / kQuadSlots) & 1) ^ 1),
+                                        &abort_s)) {
+                  fail();
+                  issued = 0;
                 } else {
-                  mbar_arrive_expect_tx(fb, kPageBytes);
-                  bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-                           kPageBytes, fb);
+                  const uint32_t fb = smem_u32(&raw_full[s]);
+                  if (k + q >= cnt) {
+                    mbar_arrive(fb);
+                  } else if (phys < 0 || phys >= p.num_blocks) {
+                    atomicOr(p.status, kStatusBadPage);
+                    mbar_arrive(fb);
+                  } else {
+                    mbar_arrive_expect_tx(fb, kPageBytes);
+                    bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
+                             kPageBytes, fb);
+                  }
                 }
               }
+              if (!__shfl_sync(0xffffffffu, issued, 0)) {
+                ok = false;
+                break;
+              }
+              if (lane == s) last = kq;
             }
-            if (!__shfl_sync(0xffffffffu, issued, 0)) {
-              ok = false;
-              break;
-            }
-            if (lane == s) last = kq;
           }
         }
+        walk.g += je - walk.j;
+        walk.j = je;
+        if (ok && walk.more()) walk.next_request();
       }
-      walk.g += je - walk.j;
-      walk.j = je;
-      if (ok && walk.more()) walk.next_request();
-    }
-    // drain issued copies before the CTA may exit
-    if (!ok && lane < kDecStages && last >= 0)
-      mbar_wait(smem_u32(&raw_full[lane]), (uint32_t)((last / kQuadSlots) & 1));
-  } else if (warp == 1 || warp == 2) {
-    // ================================================= MMA issuers
-    // Issuer m takes slices m and m + 2 of every quad.
-    if (lane == 0) {
-      const int m = warp - 1;
-      constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
-      int64_t kq = 0;
-      uint32_t last_bar = 0, last_par = 0;
-      int sq = 0;
-      while (walk.more() && !abort_s) {
-        const int je = walk.seg_end();
-        const int qs = sq & 1;
-        if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
-        const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
-        bool ok = true;
-        for (; walk.j < je && ok; ++kq) {
-          const int npq = min(4, je - walk.j);
-          walk.j += npq;
-          walk.g += npq;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int sl = m + 2 * h;
-            if (!mbar_wait_or_abort(smem_u32(&a_full[sl]), (uint32_t)(kq & 1), &abort_s) ||
-                !mbar_wait_or_abort(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]), DecD<NQ>::phase(kq) ^ 1u,
-                                    &abort_s)) {
-              fail();
-              ok = false;
-              break;
+      // drain issued copies before the CTA may exit
+      if (!ok && lane < kDecStages && last >= 0)
+        mbar_wait(smem_u32(&raw_full[lane]), (uint32_t)((last / kQuadSlots) & 1));
+    } else if (warp == 1 || warp == 2) {
+      // ================================================= MMA issuers
+      // Issuer m takes slices m and m + 2 of every quad.
+      if (lane == 0) {
+        const int m = warp - 1;
+        constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
+        int64_t kq = 0;
+        uint32_t last_bar = 0, last_par = 0;
+        int sq = 0;
+        while (walk.more() && !abort_s) {
+          const int je = walk.seg_end();
+          const int qs = sq & 1;
+          if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
+          const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
+          bool ok = true;
+          for (; walk.j < je && ok; ++kq) {
+            const int npq = min(4, je - walk.j);
+            walk.j += npq;
+            walk.g += npq;
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int sl = m + 2 * h;
+              if (!mbar_wait_or_abort(smem_u32(&a_full[sl]), (uint32_t)(kq & 1), &abort_s) ||
+                  !mbar_wait_or_abort(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]), DecD<NQ>::phase(kq) ^ 1u,
+                                      &abort_s)) {
+                fail();
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d_t = tbase + DecD<NQ>::col(kq, sl);
+              const uint32_t a_t = tbase + sl * 64;
+  #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
+                mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+              }
+              // d_full also tells the dequant warps that A buffer sl is free
+              mma_commit(smem_u32(&d_full[kq & 1][sl]));
+              last_bar = smem_u32(&d_full[kq & 1][sl]);
+              last_par = (uint32_t)((kq >> 1) & 1);
             }
-            tc_fence_after();
-            const uint32_t d_t = tbase + DecD<NQ>::col(kq, sl);
-            const uint32_t a_t = tbase + sl * 64;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
-              mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-            }
-            // d_full also tells the dequant warps that A buffer sl is free
-            mma_commit(smem_u32(&d_full[kq & 1][sl]));
-            last_bar = smem_u32(&d_full[kq & 1][sl]);
-            last_par = (uint32_t)((kq >> 1) & 1);
           }
+          if (!ok || abort_s) break;
+          mma_commit(smem_u32(&q_empty[qs]));
+          ++sq;
+          if (walk.more()) walk.next_request();
         }
-        if (!ok || abort_s) break;
-        mma_commit(smem_u32(&q_empty[qs]));
-        ++sq;
-        if (walk.more()) walk.next_request();
+        // a commit covers every MMA issued before it: drain the last one
+        // before tensor memory is freed
+        if (abort_s && last_bar != 0) mbar_wait(last_bar, last_par);
       }
-      // a commit covers every MMA issued before it: drain the last one
-      // before tensor memory is freed
-      if (abort_s && last_bar != 0) mbar_wait(last_bar, last_par);
     }
-  } else if (warp < 11) {
+  } else if (warp < 12) {
     // ================================================= dequant warpgroups
+    if constexpr (kDecRegsDq < 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsDq));
     // Group grp takes the quads of parity grp; warp q (tensor-memory lanes
     // [32q, 32q+32)) dequantises page q of the quad, one 32-token slice at a
     // time, into its lane quarter of A buffer s.  A warp of a partial quad
     // with no page still takes part in every barrier (its lanes of the A
     // buffer then hold stale finite values whose scores nobody reads).
-    const int grp = (warp - 3) >> 2;
+    const int grp = (warp - 4) >> 2;
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int dq = tid - kDqTid0;                     // 0..255 (both groups share the query tile)
@@ -523,20 +519,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     }
   } else {
     // ================================================= epilogue warpgroup
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDecRegsEpi));
     // Warp q owns page q of every quad: per slice it loads its lanes' NQ
     // columns of D buffer s and keeps the running max over slices; after the
     // 4th slice a butterfly transpose-reduction over the lanes gives the page
-    // score of every row (lane l gets rows l and l + 32).  Each warp keeps its own top-15 per
-    // row in shared memory (threshold in a register); at a segment end the
-    // four lists of each row are merged.  The walk is never left early, so
-    // every barrier is always reached.
+    // score of every row (lane l gets rows l and l + 32).  Each lane keeps
+    // the running top-15 of its row(s) in registers (this warpgroup runs
+    // with 200); at a segment end the lists go through shared memory and
+    // the four warps' lists of each row are merged.  The walk is never left
+    // early, so every barrier is always reached.
     const int q = warp & 3;
     const int ep = tid - kEpTid0;                     // 0..127: row owner at the merge
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float2* const lists = reinterpret_cast<float2*>(base + Lay::kListOff);   // [4][64][15]
     float2* const my0 = lists + (q * kMaxRows + lane) * kHistK;              // row lane
     float2* const my1 = my0 + 32 * kHistK;                                   // row lane + 32
-    constexpr int CW = NQ < 32 ? NQ : 32;             // columns per load + max pass
+    constexpr int CW = NQ == 32 ? 32 : 16;            // columns per load + max pass
     int64_t kq = 0;
     bool ok = true;                                   // uniform within the warp
     while (walk.more()) {
@@ -551,18 +549,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         const int ph = __ldg(p.page_table + (int64_t)r * p.pt_stride + jj);
         seg_bad |= (ph < 0 || ph >= p.num_blocks);
       }
-      // NQ <= 32: one row per lane, its top-15 in registers; NQ = 64: two
-      // rows per lane, sorted lists in shared memory behind a threshold
-      TopK15 top;
-      top.reset();
-      float thr0 = -CUDART_INF_F, thr1 = -CUDART_INF_F;
-      if constexpr (NQ > 32) {
-#pragma unroll
-        for (int k = 0; k < kHistK; ++k) {
-          my0[k] = make_float2(-CUDART_INF_F, __int_as_float(-1));
-          my1[k] = make_float2(-CUDART_INF_F, __int_as_float(-1));
-        }
-      }
+      // rows lane (and lane + 32 when NQ = 64)
+      TopK15 top0, top1;
+      top0.reset();
+      if constexpr (NQ > 32) top1.reset();
       for (; walk.j < je; ++kq) {
         const int npq = min(4, je - walk.j);
         const int jp = walk.j + q;                    // this warp's page
@@ -606,20 +596,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           m0 = canon_zero(m0);
           m1 = canon_zero(m1);
           if (lane < R && jp < L0) {
-            if constexpr (NQ <= 32) top.insert(m0, jp);
-            else if (m0 > thr0) thr0 = list_insert15(my0, m0, jp);
+            top0.insert(m0, jp);
             if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane) * p.dbg_stride + jp] = m0;
           }
           if (NQ > 32 && lane + 32 < R && jp < L1) {
-            if (m1 > thr1) thr1 = list_insert15(my1, m1, jp);
+            top1.insert(m1, jp);
             if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane + 32) * p.dbg_stride + jp] = m1;
           }
         }
       }
       // ---- merge the four warps' lists of each row, finalise the segment
-      if constexpr (NQ <= 32) {
 #pragma unroll
-        for (int k = 0; k < kHistK; ++k) my0[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+      for (int k = 0; k < kHistK; ++k) {
+        my0[k] = make_float2(top0.s[k], __int_as_float(top0.id[k]));
+        if constexpr (NQ > 32) my1[k] = make_float2(top1.s[k], __int_as_float(top1.id[k]));
       }
       const int bad = named_bar_red_or(2, 128, seg_bad);
       const int failed = named_bar_red_or(3, 128, (!ok || abort_s) ? 1 : 0);
