@@ -211,3 +211,17 @@ def test_decode_small_batch_after_wide_batch_same_plan():
         ref = oidx.decode(w.q_decode, oracle_cache(w), w.dec_page_table, w.dec_seq_lens, w.query_len, 8)
         assert_ids(out, ref, w.name)
     assert plan.status() == 0
+
+
+@pytest.mark.parametrize("H,qlen", [(2, 3), (8, 4), (8, 8)])
+def test_decode_partial_quads_and_split_segments(H, qlen):
+    """Many short requests: every CTA walks several segments, most of them
+    starting inside a request, and ends of segments leave partial groups of
+    1, 2 or 3 pages (the kernel takes pages four at a time)."""
+    rng = np.random.Generator(np.random.PCG64(500 + H * 10 + qlen))
+    hist = np.concatenate([np.arange(1, 14), rng.integers(1, 14, size=67), [41, 42, 43, 45]])
+    rng.shuffle(hist)
+    seq = 128 * hist + rng.integers(1, 129, size=hist.size)     # history = hist pages exactly
+    w = workloads.make_workload(name=f"quads_H{H}_q{qlen}", seed=5, rng=rng, num_heads=H,
+                                dec_seq_lens=seq, query_len=qlen, outlier_channels=4)
+    _check_workload(w)
