@@ -83,7 +83,7 @@ typedef struct indexer_plan_s* indexer_plan_t;
  *                      more than 8 decode queries per request)
  *   max_pages_per_req  largest page-table width a call may pass as pt_stride
  *   max_prefill_tokens largest total_q of any indexer_prefill call
- *   max_prefill_reqs   largest num_reqs of any indexer_prefill call
+ *   max_prefill_reqs   largest num_reqs of any indexer_prefill call, at most 4096
  * Returns IDX_OK and *plan, or an error (nothing allocated).
  */
 int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_query_len,

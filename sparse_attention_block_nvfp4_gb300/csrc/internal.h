@@ -13,7 +13,7 @@ constexpr int kTopK = 16;
 constexpr int kHistK = 15;        // score-ranked history pages per row
 constexpr int kMaxRows = 64;      // query_len (<= 8) x heads (<= 8) per request
 constexpr int kMaxDecodeReqs = 4096;   // per-request prefix sums live in shared memory
-constexpr int kMaxPrefillReqs = 8192;
+constexpr int kMaxPrefillReqs = 4096;
 
 // device status bits (mirror IDX_STATUS_* in include/nvfp4_indexer.h)
 constexpr int32_t kStatusBadPage = 1;

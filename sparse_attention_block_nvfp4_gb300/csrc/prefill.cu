@@ -9,23 +9,34 @@
 // straight into shared memory.
 //
 // Tiling.  A tile is 128 query rows = (128/H tokens) x H heads of one
-// request (the last tile of a request may be ragged); its rows sit in tensor
-// memory as the MMA's A operand (M = 128, K = 128).  Tiles of a request are
-// visited last-first (they hold the most pages) and dealt round-robin to the
-// CTAs, one CTA per SM.  Warp roles, linked by mbarrier rings, one role per
-// warpgroup so that registers can move between them (setmaxnreg):
+// request (the last tile of a request may be ragged).  A CTA takes a PAIR of
+// consecutive tiles of one request (tiles ntile-1-2k and ntile-2-2k) and
+// walks the pages of the later one, which has the most: every page is
+// dequantised once and multiplied against both tiles, so the CUDA-core work
+// per unit of tensor work is halved.  Work units are dealt round-robin to the
+// CTAs (one per SM): first the pairs (requests in order, last tiles first),
+// then the tiles left over as singles (a pair whose second tile is empty).
+// How many pairs to form is chosen so that the slowest CTA finishes first:
+// all possible pairs, or only whole rounds of pairs (one per CTA) with the
+// rest as singles, whichever gives the smaller estimated makespan (a pair
+// costs about 1.7 singles).
+// Warp roles, one per warpgroup (setmaxnreg moves registers between them),
+// linked by mbarrier rings:
 //   * warpgroup 0 (40 registers): warp 0 has the TMA unit copy each raw
-//     9216-byte page into a 6-stage shared ring; warps 1 and 2 take alternate
-//     pages, one thread each issuing 8 tcgen05.mma per page, D[row][token] =
-//     Q . K^T in fp32, 3 accumulators deep; warp 3 idles;
-//   * warpgroups 1 and 2 (dequant, alternating pages): thread t dequantises
-//     token t to fp16 into a 128B-swizzled K-major B tile [128 tokens x 128]
-//     (4 tiles deep);
-//   * warpgroup 3 (epilogue, 208 registers), thread = query row: widens the
-//     next tile's queries into tensor memory (2 buffers), loads its whole
-//     128-column row of D per page in one round trip, takes the max over the
-//     tokens and updates its running top-15 if the page is a history page of
-//     its token; writes the row at the end of the tile.
+//     9216-byte page into a 6-stage shared ring; warps 1 / 2 issue the 8
+//     tcgen05.mma of every page for tile A / tile B (both operands in shared
+//     memory: the tile's queries, M = 128, and the page, N = 128; K = 16),
+//     D[row][token] in fp32 in tensor memory, two accumulators per tile;
+//     warp 3 idles;
+//   * warpgroups 1 / 2 (88 registers, pages of even / odd index): thread t
+//     dequantises token t to fp16 into the group's own 128B-swizzled K-major
+//     B tile [128 tokens x 128];
+//   * warpgroups 3 / 4 (128 registers, tile A / tile B), thread = query row:
+//     at a pair start widen the tile's E4M3 queries into a 128B-swizzled
+//     fp16 A tile in shared memory; per page load the row of D (16 columns
+//     per tcgen05.ld), take the max over the 128 tokens and update the row's
+//     top-15 if the page is a history page of its token; write the row at the
+//     end of the pair.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -36,24 +47,23 @@
 
 namespace nvfp4idx {
 
-constexpr int kPreStages = 6;              // raw page ring
-constexpr int kPreB = 4;                   // dequantised B tiles
-constexpr int kPreD = 3;                   // accumulators: columns [128 + 128d, 256 + 128d)
-// warpgroup 0: warp 0 TMA, warps 1 / 2 MMA issue, warp 3 idle (registers
-// lowered to 40); warpgroups 1 / 2: dequant (128); warpgroup 3: epilogue
-// (raised to 208, so a thread holds its whole 128-column row of D).
-// 4 x 40 + 8 x 128 + 4 x 208 registers x 32 lanes = 64512 <= 512 x 128.
-constexpr int kPreThreads = 512;
-constexpr uint32_t kRegsCtl = 40, kRegsEpi = 208;
-constexpr uint32_t kPreTmemCols = 512;     // queries [0,64) and [64,128), accumulators [128,512)
-constexpr uint32_t kBTileBytes = 128 * 256;  // fp16 [2 K-blocks][128 tokens][64]
+constexpr int kPreStages = 6;              // raw page ring (even: pages of one parity per stage)
+constexpr int kPreThreads = 640;           // 5 warpgroups
+// 4 x 40 + 8 x 88 + 8 x 128 = 1888 registers per lane slot <= 640 x 96 / 32
+constexpr uint32_t kRegsCtl = 40, kRegsDq = 88, kRegsEpi = 128;
+constexpr uint32_t kPreTmemCols = 512;     // tile A: D [0,128), [128,256); tile B: [256,384), [384,512)
+constexpr uint32_t kTileBytes = 128 * 256; // fp16 [2 K-blocks][128 rows][64], 128B swizzle
 
 struct PreLayout {
-  static constexpr uint32_t kBOff = 0;
-  static constexpr uint32_t kStageOff = kPreB * kBTileBytes;
+  static constexpr uint32_t kQOff = 0;                           // A tiles of tile A and tile B
+  static constexpr uint32_t kBOff = 2 * kTileBytes;              // B tiles of dequant groups 0 and 1
+  static constexpr uint32_t kStageOff = kBOff + 2 * kTileBytes;
   static constexpr uint32_t kTpreOff = kStageOff + kPreStages * kPageBytes;
-  static size_t bytes(int num_reqs) { return 1024 + kTpreOff + (size_t)(num_reqs + 1) * 4; }
+  // two prefix arrays per request: tiles and possible pairs
+  static size_t bytes(int num_reqs) { return 1024 + kTpreOff + (size_t)(num_reqs + 1) * 8; }
 };
+static_assert(1024 + PreLayout::kTpreOff + (kMaxPrefillReqs + 1) * 8 + 1024 <= 227 * 1024,
+              "prefill shared memory above the 227 KB a CTA may hold");
 
 // Three-input maximum (one instruction on sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -62,35 +72,81 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-struct TileInfo {
-  int r, t0, nt, L_max, ctx, row0;   // row0 = first token (q row) of the tile
+// max of 64 floats: four independent chains of three-input maxima (one
+// dependent chain of 64 maxima would be the epilogue's critical path)
+__device__ __forceinline__ float max64(const float (&v)[64]) {
+  float ma = fmax3(v[0], v[1], v[2]), mb = fmax3(v[3], v[4], v[5]), mc = fmax3(v[6], v[7], v[8]),
+        md = fmax3(v[9], v[10], v[11]);
+#pragma unroll
+  for (int i = 12; i < 60; i += 8) {
+    ma = fmax3(ma, v[i], v[i + 1]);
+    mb = fmax3(mb, v[i + 2], v[i + 3]);
+    mc = fmax3(mc, v[i + 4], v[i + 5]);
+    md = fmax3(md, v[i + 6], v[i + 7]);
+  }
+  ma = fmax3(ma, v[60], v[61]);
+  mb = fmax3(mb, v[62], v[63]);
+  return fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
+}
+
+struct TileRows {
+  int t0, nt, row0;   // first token of the tile within the request, tokens, first q row
+};
+
+struct PairInfo {
+  int r, ctx, L_max;  // request, context length, pages walked (those of tile A)
   bool table_bad;
+  TileRows tile[2];   // tile A (the later one) and tile B (nt = 0 when absent)
+};
+
+// The work schedule, identical in every thread: tpre[r] / fpre[r] = tiles /
+// possible pairs of the requests before r; P pairs are formed (requests in
+// order, each request's last tiles first), the remaining tiles are singles.
+struct Sched {
+  const int32_t* tpre;
+  const int32_t* fpre;
+  int NR, P;
+  __device__ __forceinline__ int pairs_before(int r) const { return min(fpre[r], P); }
+  __device__ __forceinline__ int singles_before(int r) const { return tpre[r] - 2 * pairs_before(r); }
 };
 
 template <int H>
-__device__ __forceinline__ TileInfo prefill_tile(const PrefillParams& p, const int32_t* tpre, int t) {
+__device__ __forceinline__ PairInfo prefill_pair(const PrefillParams& p, const Sched& sc, int u) {
   constexpr int TQ = 128 / H;
-  int lo = 0, hi = p.num_reqs - 1;
+  const bool is_pair = u < sc.P;
+  const int key = is_pair ? u : u - sc.P;
+  int lo = 0, hi = sc.NR - 1;                        // last request whose prefix <= key
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (tpre[mid] <= t) lo = mid; else hi = mid - 1;
+    if ((is_pair ? sc.fpre[mid] : sc.singles_before(mid)) <= key) lo = mid; else hi = mid - 1;
   }
-  TileInfo ti;
-  ti.r = lo;
+  PairInfo pi;
+  pi.r = lo;
   const int cu0 = __ldg(p.cu_seqlens_q + lo);
   const int ql = __ldg(p.cu_seqlens_q + lo + 1) - cu0;
   const int ntile = (ql + TQ - 1) / TQ;
-  const int lt = ntile - 1 - (t - tpre[lo]);        // last tile first
-  ti.t0 = lt * TQ;
-  ti.nt = min(TQ, ql - ti.t0);
+  int la;                                            // tile A; tile B = la - 1 for a pair
+  if (is_pair) {
+    la = ntile - 1 - 2 * (key - sc.fpre[lo]);
+  } else {
+    const int pairs_r = sc.pairs_before(lo + 1) - sc.pairs_before(lo);
+    la = ntile - 1 - 2 * pairs_r - (key - sc.singles_before(lo));
+  }
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int lt = (x == 0 || is_pair) ? la - x : -1;
+    TileRows& tr = pi.tile[x];
+    tr.t0 = lt >= 0 ? lt * TQ : 0;
+    tr.nt = lt >= 0 ? min(TQ, ql - tr.t0) : 0;
+    tr.row0 = cu0 + tr.t0;
+  }
   const int seq = __ldg(p.seq_lens + lo);
-  ti.ctx = seq - ql;
-  ti.row0 = cu0 + ti.t0;
+  pi.ctx = seq - ql;
   const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
-  ti.table_bad = hist > p.pt_stride;
-  const int pos_last = ti.ctx + ti.t0 + ti.nt - 1;
-  ti.L_max = (pos_last >= 0 && !ti.table_bad) ? (pos_last >> 7) : 0;
-  return ti;
+  pi.table_bad = hist > p.pt_stride;
+  const int pos_last = pi.ctx + pi.tile[0].t0 + pi.tile[0].nt - 1;
+  pi.L_max = (pos_last >= 0 && !pi.table_bad) ? (pos_last >> 7) : 0;
+  return pi;
 }
 
 template <int H>
@@ -98,12 +154,12 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   constexpr int TQ = 128 / H;     // tokens per tile
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kPreStages], raw_empty[kPreStages];
-  __shared__ __align__(8) uint64_t b_full[kPreB], b_empty[kPreB];
-  __shared__ __align__(8) uint64_t d_full[kPreD], d_empty[kPreD];
-  __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
+  __shared__ __align__(8) uint64_t b_full[2], b_empty[2];          // B tile of dequant group h
+  __shared__ __align__(8) uint64_t d_full[2][2], d_empty[2][2];    // [tile][accumulator]
+  __shared__ __align__(8) uint64_t q_full[2], q_empty;             // A tiles (queries)
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
-  __shared__ int warp_sum[kPreThreads / 32];
+  __shared__ int warp_sum[kPreThreads / 32], warp_sum2[kPreThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -113,40 +169,65 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   const int NR = p.num_reqs, G = gridDim.x, c = blockIdx.x;
   constexpr int NW = kPreThreads / 32;
 
-  // ---- tiles per request -> exclusive prefix sums
+  // ---- tiles and possible pairs per request -> exclusive prefix sums
+  int32_t* const fpre = tpre + (NR + 1);
   {
     const int per = (NR + kPreThreads - 1) / kPreThreads;
     const int r0 = tid * per, r1 = min(NR, r0 + per);
-    int sum = 0;
-    for (int r = r0; r < r1; ++r) {
+    auto tiles = [&](int r) {
       const int ql = __ldg(p.cu_seqlens_q + r + 1) - __ldg(p.cu_seqlens_q + r);
-      sum += ql > 0 ? (ql + TQ - 1) / TQ : 0;
+      return ql > 0 ? (ql + TQ - 1) / TQ : 0;
+    };
+    int st = 0, sp = 0;
+    for (int r = r0; r < r1; ++r) {
+      const int nt = tiles(r);
+      st += nt;
+      sp += nt >> 1;
     }
-    int incl = sum;
+    int it = st, ipp = sp;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      const int a1 = __shfl_up_sync(0xffffffffu, it, o), a2 = __shfl_up_sync(0xffffffffu, ipp, o);
+      if (lane >= o) {
+        it += a1;
+        ipp += a2;
+      }
     }
-    if (lane == 31) warp_sum[warp] = incl;
+    if (lane == 31) warp_sum[warp] = it, warp_sum2[warp] = ipp;
     __syncthreads();
-    int off = 0;
-    for (int w = 0; w < warp; ++w) off += warp_sum[w];
-    int run = off + incl - sum;
+    int ot = 0, op = 0;
+    for (int w = 0; w < warp; ++w) ot += warp_sum[w], op += warp_sum2[w];
+    int rt = ot + it - st, rp = op + ipp - sp;
     for (int r = r0; r < r1; ++r) {
-      tpre[r] = run;
-      const int ql = __ldg(p.cu_seqlens_q + r + 1) - __ldg(p.cu_seqlens_q + r);
-      run += ql > 0 ? (ql + TQ - 1) / TQ : 0;
+      tpre[r] = rt;
+      fpre[r] = rp;
+      const int nt = tiles(r);
+      rt += nt;
+      rp += nt >> 1;
     }
     if (tid == kPreThreads - 1) {
-      int tot = 0;
-      for (int w = 0; w < NW; ++w) tot += warp_sum[w];
-      tpre[NR] = tot;
+      int tt = 0, tp = 0;
+      for (int w = 0; w < NW; ++w) tt += warp_sum[w], tp += warp_sum2[w];
+      tpre[NR] = tt;
+      fpre[NR] = tp;
     }
     __syncthreads();
   }
-  const int NT = tpre[NR];
-  if (c >= NT) return;
+  // how many pairs: all possible ones, or whole rounds of G pairs and the
+  // rest as singles, whichever finishes sooner (pair ~ 17, single ~ 10)
+  Sched sched{tpre, fpre, NR, 0};
+  int NU;
+  {
+    const int NT = tpre[NR], Pall = fpre[NR];
+    const int Sall = NT - 2 * Pall;
+    const int Pr = min(Pall, (NT / (2 * G)) * G);
+    const int Sr = NT - 2 * Pr;
+    const long long cost_all = (long long)((Pall + G - 1) / G) * 17 + (long long)((Sall + G - 1) / G) * 10;
+    const long long cost_rounds = (long long)((Pr + G - 1) / G) * 17 + (long long)((Sr + G - 1) / G) * 10;
+    sched.P = cost_rounds < cost_all ? Pr : Pall;
+    NU = NT - sched.P;                               // P pairs + (NT - 2P) singles
+  }
+  if (c >= NU) return;
 
   // ---- tensor memory, barriers
   if (warp == 1) {
@@ -156,20 +237,18 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   if (tid == 0) {
     for (int s = 0; s < kPreStages; ++s) {
       mbar_init(smem_u32(&raw_full[s]), 1);
-      mbar_init(smem_u32(&raw_empty[s]), 128);
+      mbar_init(smem_u32(&raw_empty[s]), 128);  // the page's dequant group
     }
-    for (int b = 0; b < kPreB; ++b) {
-      mbar_init(smem_u32(&b_full[b]), 128);
-      mbar_init(smem_u32(&b_empty[b]), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&b_full[h]), 128);     // dequant group h
+      mbar_init(smem_u32(&b_empty[h]), 2);      // both MMA issuers commit
+      for (int d = 0; d < 2; ++d) {
+        mbar_init(smem_u32(&d_full[h][d]), 1);    // MMA issuer of tile h commits
+        mbar_init(smem_u32(&d_empty[h][d]), 128); // epilogue of tile h
+      }
+      mbar_init(smem_u32(&q_full[h]), 128);     // epilogue of tile h writes its A tile
     }
-    for (int d = 0; d < kPreD; ++d) {
-      mbar_init(smem_u32(&d_full[d]), 1);
-      mbar_init(smem_u32(&d_empty[d]), 128);
-    }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&q_full[k]), 128);
-      mbar_init(smem_u32(&q_empty[k]), 2);   // both MMA issuers commit
-    }
+    mbar_init(smem_u32(&q_empty), 2);           // both MMA issuers commit per pair
     abort_s = 0;
     fence_mbar_init();
   }
@@ -185,23 +264,24 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   };
 
   if (warp < 4) {
-    // warpgroup 0 gives registers back to the epilogue (executed by all
-    // four warps of the warpgroup, warp 3 has no other role)
+    // warpgroup 0 gives registers back to the epilogues (executed by all four
+    // warps of the warpgroup; warp 3 has no other role)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == 0) {
       // ================================================= producer (TMA)
       if (lane == 0) {
         int64_t g = 0;
-        for (int t = c; t < NT && !abort_s; t += G) {
-          const TileInfo ti = prefill_tile<H>(p, tpre, t);
-          for (int j = 0; j < ti.L_max; ++j, ++g) {
+        for (int t = c; t < NU && !abort_s; t += G) {
+          const PairInfo pi = prefill_pair<H>(p, sched, t);
+          for (int j = 0; j < pi.L_max; ++j, ++g) {
             const int s = (int)(g % kPreStages);
-            if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1), &abort_s)) {
+            if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
+                                    &abort_s)) {
               fail();
               break;
             }
             const uint32_t fb = smem_u32(&raw_full[s]);
-            const int phys = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + j);
+            const int phys = __ldg(p.page_table + (int64_t)pi.r * p.pt_stride + j);
             if (phys < 0 || phys >= p.num_blocks) {
               mbar_arrive(fb);
             } else {
@@ -211,60 +291,71 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
             }
           }
         }
-        if (abort_s) {
+        if (abort_s) {   // drain issued copies before the CTA may exit
           for (int64_t k = (g > kPreStages ? g - kPreStages : 0); k < g; ++k)
             mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
         }
       }
     } else if (warp == 1 || warp == 2) {
       // ================================================= MMA issuers
-      // Two issuing threads take alternate pages, so that one thread's commits
-      // and waits overlap the other's MMAs and the tensor core stays busy.
+      // Issuer x multiplies every page against tile x's queries.
       if (lane == 0) {
-        const int mgrp = warp - 1;
+        const int x = warp - 1;
         constexpr uint32_t idesc = idesc_f16_f32(128, 128);
-        int64_t g = 0, g_last = -1;
-        int kq = 0;
-        for (int t = c; t < NT && !abort_s; t += G) {
-          const TileInfo ti = prefill_tile<H>(p, tpre, t);
-          if (ti.L_max == 0) continue;
-          const int qb = kq & 1;
-          if (!mbar_wait_or_abort(smem_u32(&q_full[qb]), (uint32_t)((kq >> 1) & 1), &abort_s)) { fail(); break; }
-          for (int j = 0; j < ti.L_max; ++j, ++g) {
-            if ((int)(g & 1) != mgrp) continue;
-            const int nb = (int)(g % kPreB), d = (int)(g % kPreD);
-            if (!mbar_wait_or_abort(smem_u32(&b_full[nb]), (uint32_t)((g / kPreB) & 1), &abort_s)) { fail(); break; }
-            if (!mbar_wait_or_abort(smem_u32(&d_empty[d]), (uint32_t)(((g / kPreD) & 1) ^ 1), &abort_s)) { fail(); break; }
-            tc_fence_after();
-            const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)nb * kBTileBytes;
-  #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bdesc = smem_desc_sw128(bt + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-              mma_f16_tmemA(tbase + 128 + d * 128, tbase + qb * 64 + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+        const uint32_t qaddr = sbase + PreLayout::kQOff + (uint32_t)x * kTileBytes;
+        int64_t g = 0;
+        int ip = 0;                                   // pairs with pages so far
+        uint32_t last_bar = 0, last_par = 0;
+        for (int t = c; t < NU && !abort_s; t += G) {
+          const PairInfo pi = prefill_pair<H>(p, sched, t);
+          if (pi.L_max == 0) continue;
+          if (!mbar_wait_or_abort(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s)) { fail(); break; }
+          bool ok = true;
+          for (int j = 0; j < pi.L_max; ++j, ++g) {
+            const int b = (int)(g & 1);
+            const uint32_t par = (uint32_t)((g >> 1) & 1);
+            if (!mbar_wait_or_abort(smem_u32(&b_full[b]), par, &abort_s) ||
+                !mbar_wait_or_abort(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s)) {
+              fail();
+              ok = false;
+              break;
             }
-            mma_commit(smem_u32(&b_empty[nb]));
-            mma_commit(smem_u32(&d_full[d]));
-            g_last = g;
+            tc_fence_after();
+            const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)b * kTileBytes;
+            const uint32_t dt = tbase + (uint32_t)(x * 256 + b * 128);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t koff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+              mma_f16_ss(dt, smem_desc_sw128(qaddr + koff), smem_desc_sw128(bt + koff), idesc,
+                         kk > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&d_full[x][b]));
+            mma_commit(smem_u32(&b_empty[b]));
+            last_bar = smem_u32(&d_full[x][b]);
+            last_par = par;
           }
-          if (abort_s) break;
-          mma_commit(smem_u32(&q_empty[qb]));
-          ++kq;
+          if (!ok || abort_s) break;
+          mma_commit(smem_u32(&q_empty));
+          ++ip;
         }
-        if (abort_s && g_last >= 0) {
-          const int64_t k = g_last;
-          mbar_wait(smem_u32(&d_full[k % kPreD]), (uint32_t)((k / kPreD) & 1));
-        }
+        // a commit covers every MMA issued before it: drain the last one
+        // before tensor memory is freed
+        if (abort_s && last_bar != 0) mbar_wait(last_bar, last_par);
       }
     }
   } else if (warp < 12) {
     // ================================================= dequant warpgroups
-    const int grp = (warp - 4) >> 2;                 // 0 or 1: takes pages with g % 2 == grp
+    // Group grp takes the pages of parity grp and owns B tile grp, so each of
+    // its barriers has one waiter that takes the phases in order.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDq));
+    const int grp = (warp - 4) >> 2;
     const int tok = ((warp & 3) << 5) | lane;        // token row of the page / of the B tile
+    uint8_t* const bt = base + PreLayout::kBOff + grp * kTileBytes;
     int64_t g = 0;
     bool ok = true;
-    for (int t = c; t < NT && ok; t += G) {
-      const TileInfo ti = prefill_tile<H>(p, tpre, t);
-      for (int j = 0; j < ti.L_max; ++j, ++g) {
+    for (int t = c; t < NU && ok; t += G) {
+      const PairInfo pi = prefill_pair<H>(p, sched, t);
+      for (int j = 0; j < pi.L_max; ++j, ++g) {
         if ((int)(g & 1) != grp) continue;
         const int s = (int)(g % kPreStages);
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
@@ -284,14 +375,13 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           }
         }
         mbar_arrive(smem_u32(&raw_empty[s]));
-        const int nb = (int)(g % kPreB);
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&b_empty[nb]),
-                                                         (uint32_t)(((g / kPreB) & 1) ^ 1), &abort_s))) {
+        // the B tile is free once both MMA issuers are done with page g - 2
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&b_empty[grp]),
+                                                         (uint32_t)(((g >> 1) & 1) ^ 1), &abort_s))) {
           fail();
           ok = false;
           break;
         }
-        uint8_t* bt = base + PreLayout::kBOff + nb * kBTileBytes;
         const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
                                 e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
 #pragma unroll
@@ -308,125 +398,105 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&b_full[nb]));
+        mbar_arrive(smem_u32(&b_full[grp]));
       }
     }
   } else {
-    // ================================================= epilogue warpgroup
+    // ================================================= epilogue warpgroups
+    // Warpgroup x handles tile x of every pair; thread = query row.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    const int x = (warp - 12) >> 2;
     const int n = ((warp & 3) << 5) | lane;          // query row = tensor-memory lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t bar_id = 2 + x;                   // named barrier of this warpgroup
+    uint8_t* const qt = base + PreLayout::kQOff + x * kTileBytes;
     TopK15 top;
     bool ok = true;
-    // widen tile t's queries into tensor-memory buffer qb (thread = row)
-    auto load_q = [&](const TileInfo& ti, int qb) {
-      uint32_t a[64];
-      if (n < ti.nt * H) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)ti.row0 * H + n) * 128);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 e = __ldg(src + i);
-          const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            a[8 * i + 2 * k] = e4m3x2_to_f16x2(ew[k] & 0xFFFFu);
-            a[8 * i + 2 * k + 1] = e4m3x2_to_f16x2(ew[k] >> 16);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) a[i] = 0u;
-      }
-      tc_fence_after();
-      tmem_st_32x32b_x64(tbase + lane_base + qb * 64, a);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&q_full[qb]));
-    };
-    // the k-th tile of this CTA that has pages (the MMA's tile sequence)
-    auto next_mma_tile = [&](int from) {
-      for (int t = from; t < NT; t += G)
-        if (prefill_tile<H>(p, tpre, t).L_max > 0) return t;
-      return NT;
-    };
-    int t_next_q = next_mma_tile(c);      // next tile whose queries are not loaded yet
-    int kq_loaded = 0;
-    if (t_next_q < NT) {
-      load_q(prefill_tile<H>(p, tpre, t_next_q), 0);
-      kq_loaded = 1;
-      t_next_q = next_mma_tile(t_next_q + G);
-    }
     int64_t g = 0;
-    for (int t = c; t < NT; t += G) {
-      // every epilogue warp takes the same decision to stop (a barrier it
+    int ip = 0;
+    for (int t = c; t < NU; t += G) {
+      // every warp of the group takes the same decision to stop (a barrier it
       // skipped would otherwise hold the others)
-      if (named_bar_red_or(2, 128, (!ok || abort_s) ? 1 : 0)) break;
-      const TileInfo ti = prefill_tile<H>(p, tpre, t);
-      const int rows = ti.nt * H;
-      const int pos = ti.ctx + ti.t0 + n / H;
-      const int L = (n < rows && pos >= 0) ? (pos >> 7) : -1;
-      if (ti.L_max > 0 && t_next_q < NT) {
-        // one tile ahead: queries of the next tile with pages
-        const int qb = kq_loaded & 1;
-        if (__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty[qb]),
-                                                        (uint32_t)(((kq_loaded >> 1) & 1) ^ 1), &abort_s))) {
-          load_q(prefill_tile<H>(p, tpre, t_next_q), qb);
-        } else {
+      if (named_bar_red_or(bar_id, 128, (!ok || abort_s) ? 1 : 0)) break;
+      const PairInfo pi = prefill_pair<H>(p, sched, t);
+      const TileRows tr = x ? pi.tile[1] : pi.tile[0];
+      const int rows = tr.nt * H;
+      const int pos = pi.ctx + tr.t0 + n / H;
+      const int L = (n < rows && pos >= 0 && !pi.table_bad) ? (pos >> 7) : -1;
+      if (pi.L_max > 0) {
+        // this tile's queries -> fp16 A tile, once the MMAs of the previous
+        // pair are done with it
+        if (ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty),
+                                                                    (uint32_t)((ip - 1) & 1), &abort_s))) {
           fail();
           ok = false;
         }
-        ++kq_loaded;
-        t_next_q = next_mma_tile(t_next_q + G);
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint4 e = make_uint4(0, 0, 0, 0);
+            if (n < rows) e = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)tr.row0 * H + n) * 128) + i);
+            const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+            uint32_t a[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              a[2 * k] = e4m3x2_to_f16x2(ew[k] & 0xFFFFu);
+              a[2 * k + 1] = e4m3x2_to_f16x2(ew[k] >> 16);
+            }
+            // 16 query bytes = elements 16i .. 16i+15 = 16-byte chunks 2i, 2i+1
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c16 = 2 * i + h;
+              *reinterpret_cast<uint4*>(qt + (c16 >> 3) * (128 * 128) + sw128_offset(n, c16 & 7)) =
+                  make_uint4(a[4 * h], a[4 * h + 1], a[4 * h + 2], a[4 * h + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&q_full[x]));
+        }
+        ++ip;
       }
       // a request with an unreadable history page gets all -1 rows
-      int tile_bad = ti.table_bad ? 1 : 0;
-      if (!ti.table_bad) {
-        const int seq = __ldg(p.seq_lens + ti.r);
+      int tile_bad = pi.table_bad ? 1 : 0;
+      if (!pi.table_bad) {
+        const int seq = __ldg(p.seq_lens + pi.r);
         const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
         for (int jj = n; jj < hist; jj += 128) {
-          const int ph = __ldg(p.page_table + (int64_t)ti.r * p.pt_stride + jj);
+          const int ph = __ldg(p.page_table + (int64_t)pi.r * p.pt_stride + jj);
           tile_bad |= (ph < 0 || ph >= p.num_blocks);
         }
       }
-      tile_bad = named_bar_red_or(2, 128, tile_bad);
-      if (n == 0 && tile_bad) atomicOr(p.status, ti.table_bad ? kStatusBadTable : kStatusBadPage);
+      tile_bad = named_bar_red_or(bar_id, 128, tile_bad);
+      if (n == 0 && tile_bad && rows > 0) atomicOr(p.status, pi.table_bad ? kStatusBadTable : kStatusBadPage);
       top.reset();
-      for (int j = 0; j < ti.L_max; ++j, ++g) {
-        const int d = (int)(g % kPreD);
+      for (int j = 0; j < pi.L_max; ++j, ++g) {
+        const int b = (int)(g & 1);
         if (!ok) continue;
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[d]),
-                                                         (uint32_t)((g / kPreD) & 1), &abort_s))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
+                                                         &abort_s))) {
           fail();
           ok = false;
           continue;
         }
         tc_fence_after();
-        const uint32_t dt = tbase + lane_base + 128 + d * 128;
-        float v[128];
+        const uint32_t dt = tbase + lane_base + (uint32_t)(x * 256 + b * 128);
+        float v[64];
 #pragma unroll
-        for (int c16 = 0; c16 < 128; c16 += 16) tmem_ld_32x32b_x16(dt + c16, v + c16);
+        for (int c16 = 0; c16 < 64; c16 += 16) tmem_ld_32x32b_x16(dt + c16, v + c16);
         tmem_wait_ld();
-        float ma = fmax3(v[0], v[1], v[2]), mb = fmax3(v[3], v[4], v[5]), mc = fmax3(v[6], v[7], v[8]),
-              md = fmax3(v[9], v[10], v[11]);
+        const float m0 = max64(v);
 #pragma unroll
-        for (int i = 12; i < 124; i += 8) {
-          ma = fmax3(ma, v[i], v[i + 1]);
-          mb = fmax3(mb, v[i + 2], v[i + 3]);
-          mc = fmax3(mc, v[i + 4], v[i + 5]);
-          md = fmax3(md, v[i + 6], v[i + 7]);
-        }
-        ma = fmax3(ma, v[124], v[125]);
-        mb = fmax3(mb, v[126], v[127]);
-        float m = fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
+        for (int c16 = 0; c16 < 64; c16 += 16) tmem_ld_32x32b_x16(dt + 64 + c16, v + c16);
+        tmem_wait_ld();
+        const float m = canon_zero(fmaxf(m0, max64(v)));
         tc_fence_before();
-        mbar_arrive(smem_u32(&d_empty[d]));
-        m = canon_zero(m);
+        mbar_arrive(smem_u32(&d_empty[x][b]));
         if (j < L) {
           top.insert(m, j);
-          if (p.scores_dbg) p.scores_dbg[((int64_t)ti.row0 * H + n) * p.dbg_stride + j] = m;
+          if (p.scores_dbg) p.scores_dbg[((int64_t)tr.row0 * H + n) * p.dbg_stride + j] = m;
         }
       }
-      if (ok && n < rows) write_out_row(p.out + ((int64_t)ti.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
+      if (ok && n < rows) write_out_row(p.out + ((int64_t)tr.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
     }
   }
 
