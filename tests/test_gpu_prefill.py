@@ -104,3 +104,21 @@ def test_prefill_full_size_sampled(idx):
     rows = np.unique(np.array(rows))
     ref = oidx.prefill(w.q_prefill, cu, kv_ref, w.pre_page_table, w.pre_seq_lens, w.num_heads, rows=rows)
     assert_ids(out[rows], ref, w.name)
+
+
+@pytest.mark.parametrize("H", [1, 8])
+def test_prefill_tile_pairs_every_row(H):
+    """At least two tiles per CTA, so the kernel forms pairs of consecutive
+    query tiles (one dequantised page multiplied against both) and deals the
+    odd tiles as singles; every row checked against the oracle."""
+    rng = np.random.Generator(np.random.PCG64(60 + H))
+    tq = 128 // H
+    nreq = 160 if H == 1 else 40
+    tiles = rng.integers(1, 5, size=nreq) if H == 1 else rng.integers(6, 11, size=nreq)
+    ql = [int(t) * tq - int(rng.integers(0, tq // 2 + 1)) for t in tiles]
+    ctx = [int(c) for c in rng.choice([0, 0, 37, 128, 300, 1000], size=nreq)]
+    seq = [c + n for c, n in zip(ctx, ql)]
+    w = workloads.make_workload(name=f"pairs_H{H}", seed=60 + H, rng=rng, num_heads=H,
+                                pre_seq_lens=seq, pre_query_lens=ql, outlier_channels=4)
+    assert sum((n + tq - 1) // tq for n in ql) >= 2 * 152
+    _check(w)
