@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   constexpr int TQ = 128 / H;     // tokens per tile
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kPreStages], raw_empty[kPreStages];
-  __shared__ __align__(8) uint64_t b_full[2], b_empty[2];          // B tile of dequant group h
+  // B tile h is free again once both tiles' MMAs of its last page are done,
+  // which d_full[0][h] and d_full[1][h] tell: no separate release barrier
+  __shared__ __align__(8) uint64_t b_full[2];                      // B tile of dequant group h
   __shared__ __align__(8) uint64_t d_full[2][2], d_empty[2][2];    // [tile][accumulator]
   __shared__ __align__(8) uint64_t q_full[2], q_empty;             // A tiles (queries)
   __shared__ uint32_t tmem_base_s;
@@ -241,7 +243,6 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&b_full[h]), 128);     // dequant group h
-      mbar_init(smem_u32(&b_empty[h]), 2);      // both MMA issuers commit
       for (int d = 0; d < 2; ++d) {
         mbar_init(smem_u32(&d_full[h][d]), 1);    // MMA issuer of tile h commits
         mbar_init(smem_u32(&d_empty[h][d]), 128); // epilogue of tile h
@@ -329,8 +330,9 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
               mma_f16_ss(dt, smem_desc_sw128(qaddr + koff), smem_desc_sw128(bt + koff), idesc,
                          kk > 0 ? 1u : 0u);
             }
+            // one commit per page: d_full[x][b] also tells dequant group b
+            // that tile x is done with its B tile
             mma_commit(smem_u32(&d_full[x][b]));
-            mma_commit(smem_u32(&b_empty[b]));
             last_bar = smem_u32(&d_full[x][b]);
             last_par = par;
           }
@@ -375,9 +377,14 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           }
         }
         mbar_arrive(smem_u32(&raw_empty[s]));
-        // the B tile is free once both MMA issuers are done with page g - 2
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&b_empty[grp]),
-                                                         (uint32_t)(((g >> 1) & 1) ^ 1), &abort_s))) {
+        // the B tile is free once both tiles' MMAs of page g - 2 are done:
+        // phase (g - 2) / 2 of d_full[0][grp] and d_full[1][grp] (this group
+        // waits on each of them at every one of its pages, in order; the next
+        // phase needs this page)
+        const uint32_t fpar = (uint32_t)((((g >> 1) - 1)) & 1);
+        if (g >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[0][grp]), fpar, &abort_s) &&
+                                         mbar_wait_or_abort(smem_u32(&d_full[1][grp]), fpar, &abort_s))) {
           fail();
           ok = false;
           break;
