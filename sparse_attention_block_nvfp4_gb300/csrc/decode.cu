@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           const int cnt = min(32, je - jb);
           const int my_phys = lane < cnt ? __ldg(row + jb + lane) : 0;
           for (int k = 0; k < cnt && ok; k += 4, ++kq) {
-  #pragma unroll 1
+#pragma unroll 1
             for (int q = 0; q < 4; ++q) {
               const int phys = __shfl_sync(0xffffffffu, my_phys, (k + q) & 31);
               const int s = 4 * (int)(kq % kQuadSlots) + q;
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
             const int npq = min(4, je - walk.j);
             walk.j += npq;
             walk.g += npq;
-  #pragma unroll
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int sl = m + 2 * h;
               if (!mbar_wait_or_abort(smem_u32(&a_full[sl]), (uint32_t)(kq & 1), &abort_s) ||
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
               tc_fence_after();
               const uint32_t d_t = tbase + DecD<NQ>::col(kq, sl);
               const uint32_t a_t = tbase + sl * 64;
-  #pragma unroll
+#pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
                 mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
