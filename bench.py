@@ -389,54 +389,72 @@ def roofline_block(res, w, wname, peaks, peak_kind):
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
-def oracle_sample(w, budget_s: float, rng_seed: int = 0):
-    """Time the CPU oracle on a bounded sample of the workload's step: the
-    step's new keys of the sampled requests quantised, then a sample of decode
-    and prefill rows scored and selected.  Returns (pages_scored, seconds, text)."""
-    from oracle import indexer as oidx, nvfp4 as onvfp4
-    rng = np.random.Generator(np.random.PCG64(rng_seed))
-    seq = w.seq_lens.astype(np.int64)
-    start = np.concatenate([[0], np.cumsum(np.maximum(seq, 0))])
-    pages, secs, parts = 0, 0.0, []
-    kv = np.zeros((w.num_blocks, 128, 72), np.uint8)
-    # history of the sampled requests (resident cache: not timed)
-    dr = [int(rng.integers(w.num_decode_reqs))] if w.num_decode_reqs else []
-    pr = [int(rng.integers(w.num_prefill_reqs))] if w.num_prefill_reqs else []
-    for r in dr + [w.num_decode_reqs + k for k in pr]:
-        a, b = int(start[r]), int(start[r + 1])
-        onvfp4.insert(w.k_bf16[a:b], w.slot_mapping[a:b], kv)
-    H = w.num_heads
-    t_end = time.perf_counter() + budget_s
-    while time.perf_counter() < t_end:
-        if dr:
-            r = dr[0]
+class OracleSampler:
+    """Time the CPU oracle on bounded samples of the workload's step.  The
+    history of one sampled decode request and one sampled prefill chunk is
+    inserted once (the resident cache; not timed); each unit then quantises
+    that request's new keys and scores and selects its rows: the decode
+    request's query rows, or 32 rows of the prefill chunk."""
+
+    def __init__(self, w, rng_seed: int = 0):
+        from oracle import nvfp4 as onvfp4
+        self.w = w
+        self.rng = np.random.Generator(np.random.PCG64(rng_seed))
+        seq = w.seq_lens.astype(np.int64)
+        self.seq = seq
+        self.start = np.concatenate([[0], np.cumsum(np.maximum(seq, 0))])
+        self.kv = np.zeros((w.num_blocks, 128, 72), np.uint8)
+        self.dr = int(self.rng.integers(w.num_decode_reqs)) if w.num_decode_reqs else None
+        self.pr = int(self.rng.integers(w.num_prefill_reqs)) if w.num_prefill_reqs else None
+        for r in ([self.dr] if self.dr is not None else []) + \
+                 ([w.num_decode_reqs + self.pr] if self.pr is not None else []):
+            a, b = int(self.start[r]), int(self.start[r + 1])
+            onvfp4.insert(w.k_bf16[a:b], w.slot_mapping[a:b], self.kv)
+        self.turn = 0
+
+    def _unit(self):
+        """One unit of oracle work: returns (pages scored, seconds, description)."""
+        from oracle import indexer as oidx, nvfp4 as onvfp4
+        w, H = self.w, self.w.num_heads
+        kinds = [k for k, v in (("decode", self.dr), ("prefill", self.pr)) if v is not None]
+        kind = kinds[self.turn % len(kinds)]
+        self.turn += 1
+        if kind == "decode":
+            r = self.dr
             rows = np.arange(r * w.query_len, (r + 1) * w.query_len)
             t0 = time.perf_counter()
-            a = int(start[r + 1]) - w.query_len
-            onvfp4.insert(w.k_bf16[a:int(start[r + 1])], w.slot_mapping[a:int(start[r + 1])], kv)
-            res = oidx.decode(w.q_decode, kv, w.dec_page_table, w.dec_seq_lens, w.query_len, H, rows=rows)
-            secs += time.perf_counter() - t0
-            pages += int(np.nansum(~np.isnan(res.S)))
-            parts.append(f"decode request {r}: {len(rows)} rows x {H} heads")
-        if pr and time.perf_counter() < t_end:
-            k = pr[0]
-            cu = w.cu_seqlens_q
-            rows = np.sort(rng.choice(np.arange(cu[k], cu[k + 1]), size=min(32, int(cu[k + 1] - cu[k])),
-                                      replace=False))
-            t0 = time.perf_counter()
-            r = w.num_decode_reqs + k
-            toks = int(start[r]) + (int(seq[r]) - int(w.pre_query_lens[k])) + (rows - cu[k])
-            onvfp4.insert(w.k_bf16[toks], w.slot_mapping[toks], kv)
-            res = oidx.prefill(w.q_prefill, cu, kv, w.pre_page_table, w.pre_seq_lens, H, rows=rows)
-            secs += time.perf_counter() - t0
-            pages += int(np.count_nonzero(~np.isnan(res.S)))
-            parts.append(f"prefill chunk {k}: {len(rows)} rows x {H} heads")
-    uniq = sorted(set(parts))
-    return pages, secs, "; ".join(uniq)
+            a = int(self.start[r + 1]) - w.query_len
+            onvfp4.insert(w.k_bf16[a:int(self.start[r + 1])], w.slot_mapping[a:int(self.start[r + 1])], self.kv)
+            res = oidx.decode(w.q_decode, self.kv, w.dec_page_table, w.dec_seq_lens, w.query_len, H, rows=rows)
+            return int(np.count_nonzero(~np.isnan(res.S))), time.perf_counter() - t0, \
+                f"decode request {r}: {len(rows)} rows x {H} heads"
+        k = self.pr
+        cu = w.cu_seqlens_q
+        rows = np.sort(self.rng.choice(np.arange(cu[k], cu[k + 1]), size=min(32, int(cu[k + 1] - cu[k])),
+                                       replace=False))
+        t0 = time.perf_counter()
+        r = w.num_decode_reqs + k
+        toks = int(self.start[r]) + (int(self.seq[r]) - int(w.pre_query_lens[k])) + (rows - cu[k])
+        onvfp4.insert(w.k_bf16[toks], w.slot_mapping[toks], self.kv)
+        res = oidx.prefill(w.q_prefill, cu, self.kv, w.pre_page_table, w.pre_seq_lens, H, rows=rows)
+        return int(np.count_nonzero(~np.isnan(res.S))), time.perf_counter() - t0, \
+            f"prefill chunk {k}: {len(rows)} rows x {H} heads"
+
+    def run(self, budget_s: float):
+        """Whole units until budget_s of oracle time has passed (at least one)."""
+        pages, secs, parts = 0, 0.0, set()
+        while True:
+            p, s, what = self._unit()
+            pages += p
+            secs += s
+            parts.add(what)
+            if secs >= budget_s:
+                break
+        return pages, secs, "; ".join(sorted(parts))
 
 
 def cpu_block(w, budget_s):
-    pages, secs, what = oracle_sample(w, budget_s)
+    pages, secs, what = OracleSampler(w).run(budget_s)
     return {"value": pages / secs if secs else None, "unit": "pages/s", "cores": os.cpu_count(),
             "kind": "oracle", "sample": f"{what}; {pages} (row, head, page) scores in {secs:.1f} s, "
                                         f"NumPy float64, BLAS on all host cores"}
@@ -468,15 +486,21 @@ def main():
         if rank != 0:
             return
         w = workloads.config(WORKLOAD_INDEX[args.workload])
-        per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+        # each step a bounded sample: whole units (a decode request's rows or
+        # 32 rows of a prefill chunk, in turn) until the step's share of about
+        # two minutes of oracle time, at most a second, has passed
+        per_step = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+        sampler = OracleSampler(w)
         for _ in range(args.warmup):
-            oracle_sample(w, per_step)
+            sampler.run(per_step)
         pages, secs = 0, 0.0
-        what = ""
+        whats = set()
         for _ in range(args.steps):
-            p, s, what = oracle_sample(w, per_step)
+            p, s, what = sampler.run(per_step)
             pages += p
             secs += s
+            whats.add(what)
+        what = "; ".join(sorted(whats))
         v = pages / secs
         line = {"impl": "reference", "metric": "indexer pages scored/s", "value": v, "unit": "pages/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
