@@ -73,8 +73,9 @@ typedef struct indexer_plan_s* indexer_plan_t;
 /*
  * indexer_plan -- create a plan on the current CUDA device.
  * Owns the device scratch of the decode split-merge (per-split top-15
- * candidates, per-request bookkeeping) and the status word; sized here and
- * never resized.  Mirrors MiniMaxM3IndexerNvfp4MetadataBuilder.__init__,
+ * candidates, per-request bookkeeping), that of the prefill split-merge (two
+ * candidate slots per SM for the work units that straddle two CTAs: about
+ * 9 MB on a 152-SM GPU) and the status word; sized here and never resized.  Mirrors MiniMaxM3IndexerNvfp4MetadataBuilder.__init__,
  * which sizes one decode score buffer for the largest batch and context.
  *   num_heads          index heads H; one of 1, 2, 4, 8 (the builder's
  *                      DECODE_NUM_HEADS check; read here as {1,2,4,8})

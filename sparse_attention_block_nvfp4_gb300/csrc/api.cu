@@ -50,6 +50,8 @@ struct indexer_plan_s {
   int32_t* slot_bad = nullptr; // [decode_grid + max_reqs]
   int2* req_info = nullptr;    // [max_reqs]
   int32_t* status = nullptr;   // 1 word
+  float2* pcand = nullptr;     // [2 * num_sms][2][128][15]: prefill units cut by a CTA boundary
+  int32_t* pslot = nullptr;    // [2 * num_sms][kPreSlotInts]
 };
 
 extern "C" {
@@ -104,6 +106,9 @@ int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_quer
   if (e == cudaSuccess) e = cudaMalloc(&pl->status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(pl->status, 0, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(pl->slot_bad, 0, slots * sizeof(int32_t));
+  if (e == cudaSuccess)
+    e = cudaMalloc(&pl->pcand, (size_t)2 * pl->num_sms * 2 * 128 * kHistK * sizeof(float2));
+  if (e == cudaSuccess) e = cudaMalloc(&pl->pslot, (size_t)2 * pl->num_sms * kPreSlotInts * sizeof(int32_t));
   if (e != cudaSuccess) {
     indexer_plan_destroy(pl);
     return cuda_err(e, "indexer_plan: allocation");
@@ -118,6 +123,8 @@ int indexer_plan_destroy(indexer_plan_t plan) {
   cudaFree(plan->slot_bad);
   cudaFree(plan->req_info);
   cudaFree(plan->status);
+  cudaFree(plan->pcand);
+  cudaFree(plan->pslot);
   delete plan;
   return IDX_OK;
 }
@@ -212,11 +219,9 @@ int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seq
   p.total_q = total_q;
   p.H = plan->num_heads;
   p.dbg_stride = dbg_stride;
-  const int tq = 128 / plan->num_heads;
-  const int64_t tiles_bound = (int64_t)total_q / tq + num_reqs;
-  int grid = plan->num_sms;   // one prefill CTA per SM
-  if (tiles_bound < grid) grid = (int)tiles_bound;
-  if (grid < 1) grid = 1;
+  p.pcand = plan->pcand;
+  p.pslot = plan->pslot;
+  const int grid = plan->num_sms;   // one prefill CTA per SM; the work is split evenly by pages
   cudaError_t e = launch_prefill(p, grid, stream);
   if (e != cudaSuccess) return cuda_err(e, "indexer_prefill: launch");
   return IDX_OK;

@@ -44,13 +44,19 @@ struct PrefillParams {
   int32_t* out;                // [total_q][H][16]
   float* scores_dbg;
   int32_t* status;
+  // units cut by a CTA boundary: slot 2c / 2c + 1 = the first / last unit of
+  // CTA c; per slot the candidates [2 tiles][128 rows][15] and the unit's
+  // description (kPreSlotInts ints, slot_meta[0] = unit id or -1)
+  float2* pcand;
+  int32_t* pslot;
   int num_blocks, pt_stride, num_reqs, total_q, H, dbg_stride;
 };
+constexpr int kPreSlotInts = 20;
 
 cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
                           int num_blocks, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream);   // + the merge
 
 // smallest power-of-two >= 16 that holds R rows (the MMA N dimension)
 inline int decode_nq(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }

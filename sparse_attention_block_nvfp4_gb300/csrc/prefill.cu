@@ -9,20 +9,25 @@
 // straight into shared memory.
 //
 // Tiling.  A tile is 128 query rows = (128/H tokens) x H heads of one
-// request (the last tile of a request may be ragged).  A CTA takes a PAIR of
-// consecutive tiles of one request (tiles ntile-1-2k and ntile-2-2k) and
-// walks the pages of the later one, which has the most: every page is
-// dequantised once and multiplied against both tiles, so the CUDA-core work
-// per unit of tensor work is halved.  Work units are dealt round-robin to the
-// CTAs (one per SM): first the pairs (requests in order, last tiles first),
-// then the tiles left over as singles (a pair whose second tile is empty).
-// How many pairs to form is chosen so that the slowest CTA finishes first:
-// all possible pairs, or only whole rounds of pairs (one per CTA) with the
-// rest as singles, whichever gives the smaller estimated makespan (a pair
-// costs about 1.7 singles).
+// request (the last tile of a request may be ragged).  A work unit is a PAIR
+// of consecutive tiles of one request (tiles ntile-1-2k and ntile-2-2k) or,
+// for the tile left over in a request with an odd number of tiles, a single
+// tile; a unit walks the pages of its later tile, which has the most: every
+// page is dequantised once and multiplied against both tiles, so the
+// CUDA-core work per unit of tensor work is halved.  Units are ordered pairs
+// first (requests in order, last tiles first), then singles.
+//
+// Balance.  The pages of all units, weighted by their measured cost (a page
+// of a pair 17, of a single 10, plus 96 per unit for the switch to its
+// queries), are split evenly over the CTAs (one per SM): a CTA walks a
+// contiguous range of (unit, page), so no CTA waits for a long request's
+// last tiles while others idle.  A unit cut by a CTA boundary leaves, per
+// CTA, its rows' top-15 candidates in plan scratch (two slots per CTA: its
+// first and its last unit), and prefill_merge_kernel merges them in page
+// order.
 // Warp roles, one per warpgroup (setmaxnreg moves registers between them),
 // linked by mbarrier rings:
-//   * warpgroup 0 (40 registers): warp 0 has the TMA unit copy each raw
+//   * warpgroup 0 (56 registers): warp 0 has the TMA unit copy each raw
 //     9216-byte page into a 6-stage shared ring; warps 1 / 2 issue the 8
 //     tcgen05.mma of every page for tile A / tile B (both operands in shared
 //     memory: the tile's queries, M = 128, and the page, N = 128; K = 16),
@@ -31,12 +36,13 @@
 //   * warpgroups 1 / 2 (88 registers, pages of even / odd index): thread t
 //     dequantises token t to fp16 into the group's own 128B-swizzled K-major
 //     B tile [128 tokens x 128];
-//   * warpgroups 3 / 4 (128 registers, tile A / tile B), thread = query row:
-//     at a pair start widen the tile's E4M3 queries into a 128B-swizzled
-//     fp16 A tile in shared memory; per page load the row of D (16 columns
-//     per tcgen05.ld), take the max over the 128 tokens and update the row's
-//     top-15 if the page is a history page of its token; write the row at the
-//     end of the pair.
+//   * warpgroups 3 / 4 (120 registers, tile A / tile B), thread = query row:
+//     at a unit start widen the tile's E4M3 queries into a 128B-swizzled
+//     fp16 A tile in shared memory; per page take the row's max over the 128
+//     tokens with four load-and-reduce tensor-memory reads (tcgen05.ld.red,
+//     32 columns each: no CUDA-core instruction per score) and update the
+//     row's top-15 if the page is a history page of its token; write the row
+//     (or its candidates) at the end of the unit.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -49,8 +55,8 @@ namespace nvfp4idx {
 
 constexpr int kPreStages = 6;              // raw page ring (even: pages of one parity per stage)
 constexpr int kPreThreads = 640;           // 5 warpgroups
-// 4 x 40 + 8 x 88 + 8 x 128 = 1888 registers per lane slot <= 640 x 96 / 32
-constexpr uint32_t kRegsCtl = 40, kRegsDq = 88, kRegsEpi = 128;
+// 4 x 56 + 8 x 88 + 8 x 120 = 1888 registers per lane slot <= 640 x 96 / 32
+constexpr uint32_t kRegsCtl = 56, kRegsDq = 88, kRegsEpi = 120;
 constexpr uint32_t kPreTmemCols = 512;     // tile A: D [0,128), [128,256); tile B: [256,384), [384,512)
 constexpr uint32_t kTileBytes = 128 * 256; // fp16 [2 K-blocks][128 rows][64], 128B swizzle
 
@@ -64,30 +70,6 @@ struct PreLayout {
 };
 static_assert(1024 + PreLayout::kTpreOff + (kMaxPrefillReqs + 1) * 8 + 1024 <= 227 * 1024,
               "prefill shared memory above the 227 KB a CTA may hold");
-
-// Three-input maximum (one instruction on sm_100 and later).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// max of 64 floats: four independent chains of three-input maxima (one
-// dependent chain of 64 maxima would be the epilogue's critical path)
-__device__ __forceinline__ float max64(const float (&v)[64]) {
-  float ma = fmax3(v[0], v[1], v[2]), mb = fmax3(v[3], v[4], v[5]), mc = fmax3(v[6], v[7], v[8]),
-        md = fmax3(v[9], v[10], v[11]);
-#pragma unroll
-  for (int i = 12; i < 60; i += 8) {
-    ma = fmax3(ma, v[i], v[i + 1]);
-    mb = fmax3(mb, v[i + 2], v[i + 3]);
-    mc = fmax3(mc, v[i + 4], v[i + 5]);
-    md = fmax3(md, v[i + 6], v[i + 7]);
-  }
-  ma = fmax3(ma, v[60], v[61]);
-  mb = fmax3(mb, v[62], v[63]);
-  return fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
-}
 
 struct TileRows {
   int t0, nt, row0;   // first token of the tile within the request, tokens, first q row
@@ -148,6 +130,62 @@ __device__ __forceinline__ PairInfo prefill_pair(const PrefillParams& p, const S
   pi.L_max = (pos_last >= 0 && !pi.table_bad) ? (pos_last >> 7) : 0;
   return pi;
 }
+
+// weighted cost of one page of unit u (pair 17, single 10); a unit with pages
+// also costs kUnitOverhead before its first page (the switch to its queries
+// drains the MMA pipeline; measured: about five and a half pages of a pair)
+__device__ __forceinline__ int unit_weight(const Sched& sc, int u) { return u < sc.P ? 17 : 10; }
+constexpr int kUnitOverhead = 96;
+__device__ __forceinline__ long long unit_cost(int w, int L) {
+  return L > 0 ? kUnitOverhead + (long long)w * L : 0;
+}
+
+// Pages [ja, jb) of a unit of L pages whose weighted range starts at U that
+// fall in the CTA range [A, B) (last: B is the end of all work): page j sits
+// at U + w j.
+__device__ __forceinline__ void seg_pages(long long U, int w, int L, long long A, long long B, bool last,
+                                          int& ja, int& jb) {
+  ja = 0;
+  jb = L;
+  if (U < A) ja = (int)min((long long)L, (A - U + w - 1) / w);
+  if (!last && U + (long long)w * L > B) jb = (int)min((long long)L, max(0ll, (B - U + w - 1) / w));
+  jb = max(jb, ja);   // none here: ja == jb (also for a unit of no pages)
+}
+
+// CTA owning weighted position x when [0, W) is split over G CTAs at
+// floor(c W / G).
+__device__ __forceinline__ int split_cta(long long x, long long W, int G) {
+  return (int)(((x + 1) * G - 1) / W);
+}
+
+// This CTA's share of the work (in shared memory: every role reads it).
+struct PreRange {
+  long long A, B, W;   // weighted range [A, B) of [0, W)
+  long long Uua;       // weighted start of unit ua
+  int ua, ub;          // units walked
+  int last;            // the last CTA (takes everything up to W)
+};
+
+// The CTA's walk over units ua..ub, identical in every role: for each unit its
+// description and the pages [ja, jb) of it that fall in this CTA's range.
+struct PreWalk {
+  const PreRange* rg;
+  int u;
+  long long U;         // weighted start of unit u
+  __device__ __forceinline__ explicit PreWalk(const PreRange* r) : rg(r), u(r->ua), U(r->Uua) {}
+  __device__ __forceinline__ bool more() const { return u <= rg->ub; }
+  template <int H>
+  __device__ __forceinline__ void get(const PrefillParams& p, const Sched& sc, PairInfo& pi, int& w, int& ja,
+                                      int& jb) const {
+    pi = prefill_pair<H>(p, sc, u);
+    w = unit_weight(sc, u);
+    seg_pages(U + kUnitOverhead, w, pi.L_max, rg->A, rg->B, rg->last != 0, ja, jb);
+  }
+  __device__ __forceinline__ void next(int w, int L) {
+    U += unit_cost(w, L);
+    ++u;
+  }
+};
 
 template <int H>
 __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillParams p) {
@@ -215,21 +253,74 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     }
     __syncthreads();
   }
-  // how many pairs: all possible ones, or whole rounds of G pairs and the
-  // rest as singles, whichever finishes sooner (pair ~ 17, single ~ 10)
-  Sched sched{tpre, fpre, NR, 0};
-  int NU;
+  // every possible pair is formed (the split below balances the CTAs)
+  Sched sched{tpre, fpre, NR, fpre[NR]};
+  const int NU = tpre[NR] - sched.P;                 // P pairs + the singles
+
+  // ---- this CTA's share of the weighted pages: [A, B) of [0, W), walked as
+  // the units ua..ub (64-bit block scan over per-thread chunks of units)
+  __shared__ PreRange rg;
   {
-    const int NT = tpre[NR], Pall = fpre[NR];
-    const int Sall = NT - 2 * Pall;
-    const int Pr = min(Pall, (NT / (2 * G)) * G);
-    const int Sr = NT - 2 * Pr;
-    const long long cost_all = (long long)((Pall + G - 1) / G) * 17 + (long long)((Sall + G - 1) / G) * 10;
-    const long long cost_rounds = (long long)((Pr + G - 1) / G) * 17 + (long long)((Sr + G - 1) / G) * 10;
-    sched.P = cost_rounds < cost_all ? Pr : Pall;
-    NU = NT - sched.P;                               // P pairs + (NT - 2P) singles
+    __shared__ long long cs_warp[kPreThreads / 32];
+    __shared__ int ua_s, ub_s;
+    __shared__ long long uua_s;
+    const int k = (NU + kPreThreads - 1) / kPreThreads;
+    const int u0 = min(NU, tid * k), u1 = min(NU, u0 + k);
+    long long sum = 0;
+    for (int u = u0; u < u1; ++u)
+      sum += unit_cost(unit_weight(sched, u), prefill_pair<H>(p, sched, u).L_max);
+    long long incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) cs_warp[warp] = incl;
+    if (tid == 0) {
+      ua_s = NU;
+      ub_s = -1;
+      uua_s = 0;
+    }
+    __syncthreads();
+    long long off = 0, W = 0;
+    for (int w = 0; w < NW; ++w) {
+      if (w < warp) off += cs_warp[w];
+      W += cs_warp[w];
+    }
+    const long long A = (long long)c * W / G;
+    const long long B = (c == G - 1) ? W : (long long)(c + 1) * W / G;
+    long long U = off + incl - sum;
+    int my_a = NU, my_b = -1;
+    for (int u = u0; u < u1; ++u) {
+      const long long cu = unit_cost(unit_weight(sched, u), prefill_pair<H>(p, sched, u).L_max);
+      // first unit: overlaps [A, ...) (a unit of no pages: sits at or after A)
+      if (my_a == NU && (cu > 0 ? (U + cu > A) : (U >= A))) my_a = u;
+      if (c == G - 1 || U < B) my_b = u;
+      U += cu;
+    }
+    if (my_a < NU) atomicMin(&ua_s, my_a);
+    if (my_b >= 0) atomicMax(&ub_s, my_b);
+    __syncthreads();
+    if (ua_s >= u0 && ua_s < u1) {
+      long long V = off + incl - sum;
+      for (int u = u0; u < ua_s; ++u) V += unit_cost(unit_weight(sched, u), prefill_pair<H>(p, sched, u).L_max);
+      uua_s = V;
+    }
+    // both scratch slots of this CTA start empty
+    if (tid < 2) p.pslot[(2 * c + tid) * kPreSlotInts] = -1;
+    __syncthreads();
+    if (tid == 0) {
+      rg.A = A;
+      rg.B = B;
+      rg.W = W;
+      rg.Uua = uua_s;
+      rg.ua = ua_s;
+      rg.ub = ub_s;
+      rg.last = (c == G - 1) ? 1 : 0;
+    }
+    __syncthreads();
   }
-  if (c >= NU) return;
+  if (rg.ua > rg.ub) return;                        // no work for this CTA
 
   // ---- tensor memory, barriers
   if (warp == 1) {
@@ -272,9 +363,12 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       // ================================================= producer (TMA)
       if (lane == 0) {
         int64_t g = 0;
-        for (int t = c; t < NU && !abort_s; t += G) {
-          const PairInfo pi = prefill_pair<H>(p, sched, t);
-          for (int j = 0; j < pi.L_max; ++j, ++g) {
+        for (PreWalk sw(&rg); sw.more() && !abort_s;) {
+          PairInfo pi;
+          int w, ja, jb;
+          sw.get<H>(p, sched, pi, w, ja, jb);
+          sw.next(w, pi.L_max);
+          for (int j = ja; j < jb; ++j, ++g) {
             const int s = (int)(g % kPreStages);
             if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
                                     &abort_s)) {
@@ -307,12 +401,15 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         int64_t g = 0;
         int ip = 0;                                   // pairs with pages so far
         uint32_t last_bar = 0, last_par = 0;
-        for (int t = c; t < NU && !abort_s; t += G) {
-          const PairInfo pi = prefill_pair<H>(p, sched, t);
-          if (pi.L_max == 0) continue;
+        for (PreWalk sw(&rg); sw.more() && !abort_s;) {
+          PairInfo pi;
+          int w, ja, jb;
+          sw.get<H>(p, sched, pi, w, ja, jb);
+          sw.next(w, pi.L_max);
+          if (jb <= ja) continue;                     // no pages of this unit here
           if (!mbar_wait_or_abort(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s)) { fail(); break; }
           bool ok = true;
-          for (int j = 0; j < pi.L_max; ++j, ++g) {
+          for (int j = ja; j < jb; ++j, ++g) {
             const int b = (int)(g & 1);
             const uint32_t par = (uint32_t)((g >> 1) & 1);
             if (!mbar_wait_or_abort(smem_u32(&b_full[b]), par, &abort_s) ||
@@ -355,9 +452,12 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     uint8_t* const bt = base + PreLayout::kBOff + grp * kTileBytes;
     int64_t g = 0;
     bool ok = true;
-    for (int t = c; t < NU && ok; t += G) {
-      const PairInfo pi = prefill_pair<H>(p, sched, t);
-      for (int j = 0; j < pi.L_max; ++j, ++g) {
+    for (PreWalk sw(&rg); sw.more() && ok;) {
+      PairInfo pi;
+      int w, ja, jb;
+      sw.get<H>(p, sched, pi, w, ja, jb);
+      sw.next(w, pi.L_max);
+      for (int j = ja; j < jb; ++j, ++g) {
         if ((int)(g & 1) != grp) continue;
         const int s = (int)(g % kPreStages);
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
@@ -421,18 +521,23 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     bool ok = true;
     int64_t g = 0;
     int ip = 0;
-    for (int t = c; t < NU; t += G) {
+    for (PreWalk sw(&rg); sw.more();) {
       // every warp of the group takes the same decision to stop (a barrier it
       // skipped would otherwise hold the others)
       if (named_bar_red_or(bar_id, 128, (!ok || abort_s) ? 1 : 0)) break;
-      const PairInfo pi = prefill_pair<H>(p, sched, t);
+      PairInfo pi;
+      int w, ja, jb;
+      sw.get<H>(p, sched, pi, w, ja, jb);
+      const int u = sw.u;
+      sw.next(w, pi.L_max);
+      if (jb <= ja && pi.L_max > 0) continue;        // none of this unit's pages here
       const TileRows tr = x ? pi.tile[1] : pi.tile[0];
       const int rows = tr.nt * H;
       const int pos = pi.ctx + tr.t0 + n / H;
       const int L = (n < rows && pos >= 0 && !pi.table_bad) ? (pos >> 7) : -1;
-      if (pi.L_max > 0) {
+      if (jb > ja) {
         // this tile's queries -> fp16 A tile, once the MMAs of the previous
-        // pair are done with it
+        // unit are done with it
         if (ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty),
                                                                     (uint32_t)((ip - 1) & 1), &abort_s))) {
           fail();
@@ -476,7 +581,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       tile_bad = named_bar_red_or(bar_id, 128, tile_bad);
       if (n == 0 && tile_bad && rows > 0) atomicOr(p.status, pi.table_bad ? kStatusBadTable : kStatusBadPage);
       top.reset();
-      for (int j = 0; j < pi.L_max; ++j, ++g) {
+      for (int j = ja; j < jb; ++j, ++g) {
         const int b = (int)(g & 1);
         if (!ok) continue;
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
@@ -487,15 +592,17 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         }
         tc_fence_after();
         const uint32_t dt = tbase + lane_base + (uint32_t)(x * 256 + b * 128);
-        float v[64];
-#pragma unroll
-        for (int c16 = 0; c16 < 64; c16 += 16) tmem_ld_32x32b_x16(dt + c16, v + c16);
-        tmem_wait_ld();
-        const float m0 = max64(v);
-#pragma unroll
-        for (int c16 = 0; c16 < 64; c16 += 16) tmem_ld_32x32b_x16(dt + 64 + c16, v + c16);
-        tmem_wait_ld();
-        const float m = canon_zero(fmaxf(m0, max64(v)));
+        // the row's maximum over the page's 128 tokens: the tensor-memory
+        // loads reduce 32 columns each
+        float m = -CUDART_INF_F;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          float v[32];
+          const float r = tmem_ld_red_max_32x32b_x32(dt + (uint32_t)c, v);
+          tmem_wait_ld();
+          m = fmaxf(m, r);
+        }
+        m = canon_zero(m);
         tc_fence_before();
         mbar_arrive(smem_u32(&d_empty[x][b]));
         if (j < L) {
@@ -503,7 +610,42 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           if (p.scores_dbg) p.scores_dbg[((int64_t)tr.row0 * H + n) * p.dbg_stride + j] = m;
         }
       }
-      if (ok && n < rows) write_out_row(p.out + ((int64_t)tr.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
+      if (!ok) continue;
+      if (ja == 0 && jb == pi.L_max) {
+        if (n < rows) write_out_row(p.out + ((int64_t)tr.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
+      } else {
+        // cut by a CTA boundary: this CTA's candidates go to its slot of the
+        // unit (2c for its first unit, 2c + 1 for its last) and
+        // prefill_merge_kernel writes the rows
+        const int slot = 2 * c + (u == rg.ua ? 0 : 1);
+        float2* dst = p.pcand + (((int64_t)slot * 2 + x) * 128 + n) * kHistK;
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+        if (x == 0 && n == 0) {
+          int32_t* m = p.pslot + slot * kPreSlotInts;
+          m[1] = ja;
+          m[2] = jb;
+          m[3] = pi.L_max;
+          m[4] = pi.r;
+          m[5] = pi.ctx;
+#pragma unroll
+          for (int y = 0; y < 2; ++y) {
+            m[6 + 3 * y] = pi.tile[y].t0;
+            m[7 + 3 * y] = pi.tile[y].nt;
+            m[8 + 3 * y] = pi.tile[y].row0;
+          }
+          m[12] = tile_bad;
+          m[13] = w;
+          // weighted position of page 0 (the walk has moved past the unit)
+          const long long U0 = sw.U - unit_cost(w, pi.L_max) + kUnitOverhead;
+          m[14] = (int32_t)(uint32_t)(U0 & 0xFFFFFFFFll);
+          m[15] = (int32_t)(U0 >> 32);
+          m[16] = (int32_t)(uint32_t)(rg.W & 0xFFFFFFFFll);
+          m[17] = (int32_t)(rg.W >> 32);
+          m[18] = pi.table_bad ? 1 : 0;
+          m[0] = u;
+        }
+      }
     }
   }
 
@@ -514,6 +656,67 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   if (warp == 1) tmem_dealloc(tbase, kPreTmemCols);
 }
 
+// Merge a sorted top-15 list b (score desc, id asc; id -1 = empty) into (s, id).
+__device__ __forceinline__ void merge_top15_list(float (&s)[kHistK], int (&id)[kHistK], const float2* b) {
+  float rs[kHistK];
+  int ri[kHistK];
+  int i = 0, j = 0;
+  for (int k = 0; k < kHistK; ++k) {
+    const bool a_ok = i < kHistK && id[i] >= 0;
+    const float2 bj = b[j < kHistK ? j : kHistK - 1];
+    const int bi = __float_as_int(bj.y);
+    const bool b_ok = j < kHistK && bi >= 0;
+    const bool take_a = a_ok && (!b_ok || s[i] > bj.x || (s[i] == bj.x && id[i] < bi));
+    rs[k] = take_a ? s[i] : (b_ok ? bj.x : -CUDART_INF_F);
+    ri[k] = take_a ? id[i] : (b_ok ? bi : -1);
+    i += take_a ? 1 : 0;
+    j += (!take_a && b_ok) ? 1 : 0;
+  }
+  for (int k = 0; k < kHistK; ++k) {
+    s[k] = rs[k];
+    id[k] = ri[k];
+  }
+}
+
+// Rows of the units cut by CTA boundaries: block c takes each unit whose first
+// page lies in CTA c's range and that goes on past it, merges the candidate
+// lists that the CTAs holding its pages left (in page order, so equal scores
+// keep the lower page id first) and writes the unit's rows; thread = row of
+// tile (t / 128).
+template <int H>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
+  const int c = blockIdx.x, G = gridDim.x;
+  const int x = threadIdx.x >> 7, n = threadIdx.x & 127;
+  for (int sh = 0; sh < 2; ++sh) {
+    const int slot = 2 * c + sh;
+    const int32_t* m = p.pslot + slot * kPreSlotInts;
+    const int u = m[0];
+    if (u < 0 || m[1] != 0) continue;                // empty, or begun in an earlier CTA
+    const int L = m[3], w = m[13];
+    const long long U = (long long)(uint32_t)m[14] | ((long long)m[15] << 32);
+    const long long W = (long long)(uint32_t)m[16] | ((long long)m[17] << 32);
+    const int cl = split_cta(U + (long long)w * (L - 1), W, G);   // CTA of its last page
+    const int t0 = m[6 + 3 * x], nt = m[7 + 3 * x], row0 = m[8 + 3 * x];
+    if (n >= nt * H) continue;
+    float s[kHistK];
+    int id[kHistK];
+    {
+      const float2* own = p.pcand + (((int64_t)slot * 2 + x) * 128 + n) * kHistK;
+      for (int k = 0; k < kHistK; ++k) {
+        s[k] = own[k].x;
+        id[k] = __float_as_int(own[k].y);
+      }
+    }
+    for (int cc = c + 1; cc <= cl && cc < G; ++cc) {
+      if (p.pslot[(2 * cc) * kPreSlotInts] != u) continue;   // none of the unit's pages there
+      merge_top15_list(s, id, p.pcand + (((int64_t)(2 * cc) * 2 + x) * 128 + n) * kHistK);
+    }
+    const int pos = m[5] + t0 + n / H;
+    const int Lrow = (pos >= 0 && !m[18]) ? (pos >> 7) : -1;
+    write_out_row(p.out + ((int64_t)row0 * H + n) * kTopK, id, Lrow, m[12] != 0);
+  }
+}
+
 template <int H>
 static cudaError_t launch_prefill_h(const PrefillParams& p, int grid, cudaStream_t stream) {
   const size_t smem = PreLayout::bytes(p.num_reqs);   // > 114 KB: one CTA per SM
@@ -521,6 +724,9 @@ static cudaError_t launch_prefill_h(const PrefillParams& p, int grid, cudaStream
                                        (int)smem);
   if (e != cudaSuccess) return e;
   prefill_kernel<H><<<grid, kPreThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prefill_merge_kernel<H><<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -194,6 +194,29 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Each thread loads 32 consecutive fp32 columns of its own lane and returns
+// their maximum (tcgen05.ld.red, sm_103a): the tensor-memory read path does
+// the reduction, no CUDA-core instruction per value.  NaN inputs are ignored
+// like fmaxf does; -0 and +0 may come back in either order.  The loaded
+// values themselves are not used: `v` is only where they land.  ptxas keeps
+// the destination vectors of several such loads in straight-line code apart
+// from each other, so callers walk the columns in a loop that is not unrolled.
+__device__ __forceinline__ float tmem_ld_red_max_32x32b_x32(uint32_t taddr, float (&v)[32]) {
+  float r;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+        "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]),
+        "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]),
+        "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31]), "=f"(r)
+      : "r"(taddr)
+      : "memory");
+  return r;
+}
+
 // Load `N` (multiple of 16) consecutive columns of the thread's lane.
 template <int N>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[N]) {

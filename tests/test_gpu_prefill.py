@@ -108,9 +108,9 @@ def test_prefill_full_size_sampled(idx):
 
 @pytest.mark.parametrize("H", [1, 8])
 def test_prefill_tile_pairs_every_row(H):
-    """At least two tiles per CTA, so the kernel forms pairs of consecutive
-    query tiles (one dequantised page multiplied against both) and deals the
-    odd tiles as singles; every row checked against the oracle."""
+    """Many tiles per request: the kernel forms pairs of consecutive query
+    tiles (one dequantised page multiplied against both) and takes each
+    request's odd tile as a single; every row checked against the oracle."""
     rng = np.random.Generator(np.random.PCG64(60 + H))
     tq = 128 // H
     nreq = 160 if H == 1 else 40
@@ -121,4 +121,19 @@ def test_prefill_tile_pairs_every_row(H):
     w = workloads.make_workload(name=f"pairs_H{H}", seed=60 + H, rng=rng, num_heads=H,
                                 pre_seq_lens=seq, pre_query_lens=ql, outlier_channels=4)
     assert sum((n + tq - 1) // tq for n in ql) >= 2 * 152
+    _check(w)
+
+
+@pytest.mark.parametrize("H", [2, 8])
+def test_prefill_units_cut_across_ctas(H):
+    """Few units with long histories next to empty and one-token prompts: the
+    even split by pages cuts most units over several CTAs (each leaves its
+    top-15 candidates, merged afterwards in page order) and leaves some CTAs a
+    range with no page at all; every row checked against the oracle."""
+    rng = np.random.Generator(np.random.PCG64(70 + H))
+    ctx = [20000, 0, 5000, 0, 130 * 128, 127, 0]
+    new = [700, 0, 3, 1, 260, 1, 129]
+    seq = [c + n for c, n in zip(ctx, new)]
+    w = workloads.make_workload(name=f"cut_H{H}", seed=70 + H, rng=rng, num_heads=H,
+                                pre_seq_lens=seq, pre_query_lens=new, outlier_channels=4)
     _check(w)
