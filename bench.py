@@ -229,8 +229,9 @@ class GpuStep:
         self.out = torch.empty((rows, w.num_heads, 16), dtype=torch.int32, device=device)
         self.nd = w.num_decode_rows
         self.max_q = int(w.pre_query_lens.max()) if w.num_prefill_reqs else 0
+        # insert; decode scoring + merge; prefill scoring + merge
         self.launches_per_step = (1 if len(new) else 0) + (2 if w.num_decode_reqs else 0) + \
-            (1 if w.num_prefill_reqs else 0)
+            (2 if w.num_prefill_reqs else 0)
 
     def run(self, stream, d=None, events=None, k_new=None, slot_new=None):
         """Enqueue one step; events: dict name -> (start, end) recorded around each kernel."""

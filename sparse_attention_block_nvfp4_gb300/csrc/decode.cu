@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   __shared__ int warp_sum[kDecThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();                       // the merge kernel may be scheduled
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   uint8_t* const base = smem_raw + (sbase - raw_u32);
@@ -646,6 +647,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
 // One warp per (request, row): merge the per-segment top-15 lists of split
 // requests; write rows of requests with no history page or an unreadable one.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  griddep_wait();                                    // the scoring grid's candidates are written
   __shared__ float2 lists[8][32][kHistK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * 8 + warp;
@@ -732,8 +734,7 @@ static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;
-  decode_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(decode_merge_kernel, (unsigned)((warps + 7) / 8), 256u, 0, stream, p);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {

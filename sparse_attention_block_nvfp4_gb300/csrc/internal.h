@@ -53,6 +53,25 @@ struct PrefillParams {
 };
 constexpr int kPreSlotInts = 20;
 
+// Launch `kernel` so that it may be scheduled while the kernel before it on
+// the stream is still running (programmatic dependent launch); the kernel
+// must call griddep_wait() before reading what its predecessor wrote.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Args...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
                           int num_blocks, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);

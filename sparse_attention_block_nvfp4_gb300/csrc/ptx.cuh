@@ -113,6 +113,17 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// The running grid lets the next kernel on the stream (launched with the
+// programmatic-serialization attribute) be scheduled before it ends; that
+// kernel calls griddep_wait() before it reads anything this grid wrote.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid has completed and its writes are visible (a
+// no-op when this kernel was launched without the attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------ tensor memory
 // Allocation is warp-wide; the allocated base address is written to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
