@@ -27,6 +27,9 @@ Readings the pages leave open are listed in each function's docstring.
 Modules:
   formats  - E2M1 / E4M3 value tables, decoding and round-to-nearest-even.
   nvfp4    - NVFP4 page-row decoding and the quantise-insert.
+  mxfp4    - MXFP4 page decoding and the OCP MX quantise-insert (page
+             vllm.models.minimax_m3.amd.indexer_mxfp4: the same scores and
+             top-k over [pages, 8704] e2m1 / e8m0 pages).
   indexer  - positions, page scores, selection; decode and prefill oracles.
   brute    - scalar pure-Python brute force for tiny inputs (a pin).
   checker  - parity checker (ids modulo score ties within tolerance).

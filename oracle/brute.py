@@ -35,10 +35,41 @@ def e4m3(byte: int) -> float:
     return s * math.ldexp(8 + m, e - 10)       # (1 + m/8) * 2^(e-7)
 
 
+def e8m0(byte: int) -> float:
+    """E8M0 from its field: 8-bit exponent, bias 127; 0xFF is NaN."""
+    return math.nan if byte == 0xFF else math.ldexp(1.0, byte - 127)
+
+
 def key_element(row: bytes, e: int) -> float:
     b = row[e // 2]
     code = (b >> 4) if (e & 1) else (b & 0xF)
     return e2m1(code) * e4m3(row[64 + e // 16])
+
+
+def key_element_mx(page: bytes, t: int, e: int) -> float:
+    """Element e of token t of an MXFP4 page: codes of token t at bytes
+    64 t .. 64 t + 63, its four E8M0 scales at 8192 + 4 t .. 8192 + 4 t + 3."""
+    b = page[64 * t + e // 2]
+    code = (b >> 4) if (e & 1) else (b & 0xF)
+    return e2m1(code) * e8m0(page[8192 + 4 * t + e // 32])
+
+
+def score_mx(q_bytes, page) -> tuple:
+    """score() for one MXFP4 page (8704 bytes)."""
+    q = [e4m3(int(b)) for b in q_bytes]
+    page = bytes(int(x) for x in page)
+    best = -math.inf
+    best_abs = -math.inf
+    for t in range(128):
+        acc = 0.0
+        acc_abs = 0.0
+        for d in range(128):
+            p = q[d] * key_element_mx(page, t, d)
+            acc += p
+            acc_abs += abs(p)
+        best = max(best, acc)
+        best_abs = max(best_abs, acc_abs)
+    return best, best_abs
 
 
 def score(q_bytes, page_rows) -> tuple:
@@ -59,8 +90,10 @@ def score(q_bytes, page_rows) -> tuple:
     return best, best_abs
 
 
-def indexer_rows(q, kv_pages, page_table, seq_lens, qlens, num_heads):
-    """Ids [rows][H][16] and scores {(row, h, page): S} by brute force."""
+def indexer_rows(q, kv_pages, page_table, seq_lens, qlens, num_heads, page_format="nvfp4"):
+    """Ids [rows][H][16] and scores {(row, h, page): S} by brute force
+    (``page_format`` "nvfp4": pages [n, 128, 72]; "mxfp4": pages [n, 8704])."""
+    page_score = score_mx if page_format == "mxfp4" else score
     out = []
     scores = {}
     row = 0
@@ -76,7 +109,7 @@ def indexer_rows(q, kv_pages, page_table, seq_lens, qlens, num_heads):
                 cand = []
                 for j in range(L):
                     phys = int(page_table[r][j])
-                    s, a = score(q[row][h], kv_pages[phys])
+                    s, a = page_score(q[row][h], kv_pages[phys])
                     scores[(row, h, j)] = (s, a)
                     cand.append((-s, j))
                 cand.sort()

@@ -9,8 +9,13 @@ E4M3 "fn" (OCP FP8): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; the
 exponent-0 encodings are subnormals m/8 * 2^-6; 0x7F / 0xFF are NaN; no inf;
 largest finite 448.
 
+E8M0 (OCP microscaling shared scale): 8 exponent bits, bias 127, no sign or
+mantissa; 0xFF is NaN.
+
 Page vllm.models.minimax_m3.nvidia.indexer_nvfp4 (module description) names
-the formats: "E2M1 codes, then E4M3 block scales" for K and E4M3 for Q.
+the formats: "E2M1 codes, then E4M3 block scales" for K and E4M3 for Q; page
+vllm.models.minimax_m3.amd.indexer_mxfp4 (module description) names "e2m1 /
+e8m0 pages" for its MXFP4 K.
 """
 from __future__ import annotations
 
@@ -80,6 +85,14 @@ def e2m1_round(x: np.ndarray) -> np.ndarray:
     mag = np.where(a >= 6.0, 7, mag)
     sign = np.signbit(x).astype(np.int64) << 3
     return (mag | sign).astype(np.uint8)
+
+
+def e8m0_value(byte: np.ndarray) -> np.ndarray:
+    """Value of E8M0 bytes (OCP microscaling shared scale): 2^(byte - 127), no
+    sign, no mantissa; 0xFF is NaN."""
+    b = np.asarray(byte).astype(np.int64) & 0xFF
+    v = np.exp2(b.astype(np.float64) - 127.0)
+    return np.where(b == 0xFF, np.nan, v)
 
 
 def bf16_value(bits: np.ndarray) -> np.ndarray:

@@ -38,6 +38,7 @@ from typing import Optional, Sequence
 
 import numpy as np
 
+from . import mxfp4
 from .formats import e4m3_value
 from .nvfp4 import decode_pages
 
@@ -107,8 +108,15 @@ def _request_pages(kv_pages, page_table_row, n_hist, width_tokens, seq_len):
     return phys
 
 
-def _dequant_request(kv_pages, phys):
-    """Decode a request's history pages once: float64 [P, 128, 128]."""
+def _dequant_request(kv_pages, phys, page_format="nvfp4"):
+    """Decode a request's history pages once: float64 [P, 128, 128].
+    ``page_format``: "nvfp4" pages [num_blocks, 128, 72] or "mxfp4" pages
+    [num_blocks, 8704] (page vllm.models.minimax_m3.amd.indexer_mxfp4: the
+    same scores and top-k over a different codec)."""
+    if page_format == "mxfp4":
+        if phys.size and np.any(mxfp4.scale_bytes(kv_pages, phys) == 0xFF):
+            raise ValueError("oracle: NaN E8M0 scale byte in a scored page")
+        return mxfp4.decode_pages(kv_pages, phys)
     if phys.size:
         scales = kv_pages[phys][:, :, 64:72]
         if np.any((scales & 0x7F) == 0x7F):
@@ -126,7 +134,7 @@ def _score_rows(q_rows_bytes, K, H):
     return S.reshape(n, H, -1), A.reshape(n, H, -1)
 
 
-def _run(q, kv_pages, page_table, seq_lens, qlens, H, rows_wanted):
+def _run(q, kv_pages, page_table, seq_lens, qlens, H, rows_wanted, page_format="nvfp4"):
     """Shared driver: requests r with qlens[r] rows each, right-aligned."""
     kv_pages = np.asarray(kv_pages, dtype=np.uint8)
     page_table = np.asarray(page_table)
@@ -158,7 +166,7 @@ def _run(q, kv_pages, page_table, seq_lens, qlens, H, rows_wanted):
             continue                       # rows stay all -1
         # only the pages up to the largest wanted local page are needed
         need = int(max(0, L_all[sel].max()))
-        K = _dequant_request(kv_pages, phys[:need])
+        K = _dequant_request(kv_pages, phys[:need], page_format)
         # query rows in chunks that keep the [rows*H, need*128] products small
         step = max(1, (1 << 23) // max(1, H * need * PAGE))
         for c0 in range(0, sel.size, step):
@@ -180,16 +188,17 @@ def _run(q, kv_pages, page_table, seq_lens, qlens, H, rows_wanted):
 
 
 def decode(q, kv_pages, page_table, seq_lens, query_len: int, num_heads: int,
-           rows: Optional[Sequence[int]] = None) -> Result:
+           rows: Optional[Sequence[int]] = None, page_format: str = "nvfp4") -> Result:
     """Decode indexer: every request has ``query_len`` query rows at its last
     ``query_len`` positions.  q uint8 [num_reqs * query_len, H, 128]."""
     R = len(seq_lens)
-    return _run(q, kv_pages, page_table, seq_lens, np.full(R, query_len), num_heads, rows)
+    return _run(q, kv_pages, page_table, seq_lens, np.full(R, query_len), num_heads, rows,
+                page_format)
 
 
 def prefill(q, cu_seqlens_q, kv_pages, page_table, seq_lens, num_heads: int,
-            rows: Optional[Sequence[int]] = None) -> Result:
+            rows: Optional[Sequence[int]] = None, page_format: str = "nvfp4") -> Result:
     """Prefill indexer: request r owns rows cu[r] .. cu[r+1]-1, right-aligned
     to seq_lens[r] (context = seq_len - query_len tokens before them)."""
     cu = np.asarray(cu_seqlens_q, dtype=np.int64)
-    return _run(q, kv_pages, page_table, seq_lens, np.diff(cu), num_heads, rows)
+    return _run(q, kv_pages, page_table, seq_lens, np.diff(cu), num_heads, rows, page_format)

@@ -152,3 +152,78 @@ def test_planted_mistake_is_caught(monkeypatch, name, mod, attr, bad, pin_names)
         monkeypatch.setattr(nvfp4, "decode_pages", lambda kv, phys: bad(np.asarray(kv)[np.asarray(phys, dtype=np.int64)]))
         monkeypatch.setattr(indexer, "decode_pages", lambda kv, phys: bad(np.asarray(kv)[np.asarray(phys, dtype=np.int64)]))
     assert _any_pin_fails(pin_names), f"planted mistake not caught: {name}"
+
+
+# ---------------------------------------------------------------- MXFP4 pages
+import test_oracle_mxfp4 as mxpins   # noqa: E402
+from oracle import mxfp4             # noqa: E402
+
+_ORIG_MX_DECODE = mxfp4.decode_pages
+_ORIG_MX_QUANT = mxfp4.quantize_rows
+
+
+def _mx_decode(pages, phys, swap=False, per=32, bias=127, interleaved=False):
+    pg = np.asarray(pages, dtype=np.uint8)[np.asarray(phys, dtype=np.int64)]
+    if interleaved:                         # 68-byte token rows instead of the split page
+        rows = pg.reshape(-1, 128, 68)
+        cb, sb = rows[..., :64].astype(np.int64), rows[..., 64:]
+    else:
+        cb = pg[:, :8192].reshape(-1, 128, 64).astype(np.int64)
+        sb = pg[:, 8192:].reshape(-1, 128, 4)
+    lo, hi = (cb >> 4, cb & 0xF) if swap else (cb & 0xF, cb >> 4)
+    codes = np.stack([lo, hi], axis=-1).reshape(-1, 128, 128)
+    sc = np.exp2(sb.astype(np.float64) - bias)
+    if per == 32:
+        scale = np.repeat(sc, 32, axis=-1)
+    else:                                   # one scale per 16 elements, repeated
+        scale = np.concatenate([np.repeat(sc, 16, axis=-1)] * 2, axis=-1)
+    return formats.e2m1_value(codes) * scale
+
+
+def _mx_quant_exponent(bits, shift):
+    x = formats.bf16_value(bits).reshape(-1, 4, 32)
+    amax = np.abs(x).max(axis=-1)
+    _, e2 = np.frexp(amax)
+    E = np.clip(np.where(amax > 0, e2.astype(np.int64) - 1 - shift, -127), -127, 127)
+    codes = formats.e2m1_round(x / np.exp2(E.astype(np.float64))[..., None]).astype(np.int64).reshape(-1, 128)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), (E + 127).astype(np.uint8)
+
+
+def _mx_quant_no_clamp(bits):
+    x = formats.bf16_value(bits).reshape(-1, 4, 32)
+    amax = np.abs(x).max(axis=-1)
+    _, e2 = np.frexp(amax)
+    E = np.where(amax > 0, e2.astype(np.int64) - 3, -127)
+    codes = formats.e2m1_round(x / np.exp2(E.astype(np.float64))[..., None]).astype(np.int64).reshape(-1, 128)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), ((E + 127) & 0xFF).astype(np.uint8)
+
+
+MX_MUTATIONS = [
+    ("MXFP4 nibble order swapped", "decode_pages", lambda p, f: _mx_decode(p, f, swap=True),
+     ["pin_mx_page_decode_golden", "pin_mx_round_trip"]),
+    ("MXFP4 one scale per 16 elements", "decode_pages", lambda p, f: _mx_decode(p, f, per=16),
+     ["pin_mx_page_decode_golden", "pin_mx_round_trip"]),
+    ("MXFP4 E8M0 bias 128", "decode_pages", lambda p, f: _mx_decode(p, f, bias=128),
+     ["pin_mx_page_decode_golden", "pin_mx_round_trip"]),
+    ("MXFP4 interleaved 68-byte rows", "decode_pages", lambda p, f: _mx_decode(p, f, interleaved=True),
+     ["pin_mx_page_decode_golden", "pin_mx_round_trip"]),
+    ("MXFP4 shared exponent floor(log2 amax) - 1", "quantize_rows", lambda b: _mx_quant_exponent(b, 1),
+     ["pin_mx_quantize_golden", "pin_mx_quantize_search", "pin_mx_round_trip"]),
+    ("MXFP4 shared exponent not clamped", "quantize_rows", _mx_quant_no_clamp,
+     ["pin_mx_quantize_golden", "pin_mx_quantize_search"]),
+]
+
+
+@pytest.mark.parametrize("name,attr,bad,pin_names", MX_MUTATIONS, ids=[m[0] for m in MX_MUTATIONS])
+def test_planted_mxfp4_mistake_is_caught(monkeypatch, name, attr, bad, pin_names):
+    for n in pin_names:
+        assert getattr(mxpins, n)() is None, n
+    monkeypatch.setattr(mxfp4, attr, bad)
+    assert any(_fails(getattr(mxpins, n)) for n in pin_names), f"planted mistake not caught: {name}"
+
+
+def _fails(pin):
+    try:
+        return pin() is not None
+    except Exception:
+        return True
