@@ -160,6 +160,54 @@ int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uin
                  int num_blocks, int32_t* status, cudaStream_t stream);
 
 /*
+ * MXFP4 index-K pages (page vllm.models.minimax_m3.amd.indexer_mxfp4: its
+ * scorers read "e2m1 / e8m0 pages" [pages, 8704] uint8 and feed the same
+ * top-k as indexer_nvfp4).  Layout, as this library reads the page's
+ * mxfp4_page_views split: bytes 0..8191 hold the E2M1 codes of tokens
+ * 0..127 in order (64 bytes per token, element e in byte e/2, low nibble for
+ * even e); bytes 8192..8703 hold 4 E8M0 scales per token in token order,
+ * scale j covering elements 32j..32j+31; value = code * 2^(scale - 127),
+ * scale 0xFF = NaN.  The scorers compute the same scores, selection and
+ * output as their NVFP4 counterparts; the pages are dequantised exactly to
+ * bf16 (an E8M0 scale can leave fp16's range), queries are widened to bf16.
+ */
+
+/*
+ * mxfp4_insert -- quantise bf16 index keys into MXFP4 pages.  Per token and
+ * 32-element block (the OCP Microscaling Formats v1.0 conversion): shared
+ * exponent E = floor(log2(amax)) - 2, clamped to [-127, 127] (amax = 0 gives
+ * -127), scale byte = E + 127; code = E2M1 round-to-nearest-even of
+ * x / 2^E, saturating at 6, sign kept.
+ *   k_bf16       [n][128] bf16 bit patterns, 16-byte aligned
+ *   slot_mapping int64 [n]: page * 128 + row; negative = skip
+ *   n            tokens (0 is a no-op)
+ *   pages        [num_blocks][8704], 16-byte aligned
+ *   status       NULL, or a device int32 that gets IDX_STATUS_BAD_SLOT OR-ed
+ *                in when a slot >= num_blocks*128 was skipped
+ */
+int mxfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* pages,
+                 int num_blocks, int32_t* status, cudaStream_t stream);
+
+/*
+ * indexer_decode_mxfp4 -- indexer_decode over MXFP4 pages [num_blocks][8704];
+ * every other argument, the output and the errors as indexer_decode.
+ */
+int indexer_decode_mxfp4(indexer_plan_t plan, const uint8_t* q, const uint8_t* pages, int num_blocks,
+                         const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
+                         int num_reqs, int query_len, int32_t* out, float* scores_dbg, int dbg_stride,
+                         cudaStream_t stream);
+
+/*
+ * indexer_prefill_mxfp4 -- indexer_prefill over MXFP4 pages [num_blocks][8704];
+ * every other argument, the output and the errors as indexer_prefill.
+ */
+int indexer_prefill_mxfp4(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seqlens_q,
+                          int num_reqs, int total_q, int max_seqlen_q, const uint8_t* pages,
+                          int num_blocks, const int32_t* page_table, int pt_stride,
+                          const int32_t* seq_lens, int32_t* out, float* scores_dbg, int dbg_stride,
+                          cudaStream_t stream);
+
+/*
  * indexer_decode_noalloc -- indexer_decode for callers that cannot allocate
  * device memory.  (No counterpart in the source pages: an addition of this
  * library.)

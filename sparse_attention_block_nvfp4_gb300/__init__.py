@@ -64,11 +64,15 @@ def load_library():
     lib.indexer_decode.argtypes = [P, P, P, I, P, I, P, I, I, P, P, I, P]
     lib.indexer_prefill.argtypes = [P, P, P, I, I, I, P, I, P, I, P, P, P, I, P]
     lib.nvfp4_insert.argtypes = [P, P, I, P, I, P, P]
+    lib.indexer_decode_mxfp4.argtypes = lib.indexer_decode.argtypes
+    lib.indexer_prefill_mxfp4.argtypes = lib.indexer_prefill.argtypes
+    lib.mxfp4_insert.argtypes = lib.nvfp4_insert.argtypes
     lib.indexer_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.indexer_last_error.restype = ctypes.c_char_p
     lib.indexer_version.restype = ctypes.c_char_p
     for name in ("indexer_plan", "indexer_plan_destroy", "indexer_decode", "indexer_prefill",
-                 "nvfp4_insert", "indexer_get_status"):
+                 "nvfp4_insert", "indexer_get_status", "indexer_decode_mxfp4", "indexer_prefill_mxfp4",
+                 "mxfp4_insert"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -130,7 +134,32 @@ class Plan:
 
     def decode(self, q, kv_pages, page_table, seq_lens, query_len: int, out=None, scores_dbg=None,
                stream=None):
-        """Top-k pages of a uniform decode batch; returns ``out`` int32 [rows, H, 16]."""
+        """Top-k pages of a uniform decode batch over NVFP4 pages [num_blocks, 128, 72];
+        returns ``out`` int32 [rows, H, 16]."""
+        return self._decode("indexer_decode", 3, q, kv_pages, page_table, seq_lens, query_len, out,
+                            scores_dbg, stream)
+
+    def decode_mxfp4(self, q, pages, page_table, seq_lens, query_len: int, out=None, scores_dbg=None,
+                     stream=None):
+        """``decode`` over MXFP4 pages [num_blocks, 8704] (``indexer_decode_mxfp4``)."""
+        return self._decode("indexer_decode_mxfp4", 2, q, pages, page_table, seq_lens, query_len, out,
+                            scores_dbg, stream)
+
+    def prefill(self, q, cu_seqlens_q, kv_pages, page_table, seq_lens, max_seqlen_q: int, out=None,
+                scores_dbg=None, stream=None):
+        """Top-k pages of ragged prefill rows over NVFP4 pages [num_blocks, 128, 72];
+        returns ``out`` int32 [total_q, H, 16]."""
+        return self._prefill("indexer_prefill", 3, q, cu_seqlens_q, kv_pages, page_table, seq_lens,
+                             max_seqlen_q, out, scores_dbg, stream)
+
+    def prefill_mxfp4(self, q, cu_seqlens_q, pages, page_table, seq_lens, max_seqlen_q: int, out=None,
+                      scores_dbg=None, stream=None):
+        """``prefill`` over MXFP4 pages [num_blocks, 8704] (``indexer_prefill_mxfp4``)."""
+        return self._prefill("indexer_prefill_mxfp4", 2, q, cu_seqlens_q, pages, page_table, seq_lens,
+                             max_seqlen_q, out, scores_dbg, stream)
+
+    def _decode(self, fn, pages_ndim, q, kv_pages, page_table, seq_lens, query_len, out, scores_dbg,
+                stream):
         import torch
         H = self.num_heads
         if q.dim() != 3 or q.shape[1] != H or q.shape[2] != 128:
@@ -143,17 +172,16 @@ class Plan:
         dbg_stride = 0
         if scores_dbg is not None:
             dbg_stride = int(scores_dbg.shape[-1])
-        _check(load_library().indexer_decode(
-            self._h, _ptr(q, torch.uint8, "q"), _ptr(kv_pages, torch.uint8, "kv_pages", 3),
+        _check(getattr(load_library(), fn)(
+            self._h, _ptr(q, torch.uint8, "q"), _ptr(kv_pages, torch.uint8, "kv_pages", pages_ndim),
             int(kv_pages.shape[0]), _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
             _ptr(seq_lens, torch.int32, "seq_lens", 1), num_reqs, int(query_len),
             _ptr(out, torch.int32, "out"), _ptr(scores_dbg, torch.float32, "scores_dbg"), dbg_stride,
             _stream_ptr(stream)))
         return out
 
-    def prefill(self, q, cu_seqlens_q, kv_pages, page_table, seq_lens, max_seqlen_q: int, out=None,
-                scores_dbg=None, stream=None):
-        """Top-k pages of ragged prefill rows; returns ``out`` int32 [total_q, H, 16]."""
+    def _prefill(self, fn, pages_ndim, q, cu_seqlens_q, kv_pages, page_table, seq_lens, max_seqlen_q,
+                 out, scores_dbg, stream):
         import torch
         H = self.num_heads
         if q.dim() != 3 or q.shape[1] != H or q.shape[2] != 128:
@@ -165,9 +193,9 @@ class Plan:
         if out is None:
             out = torch.empty((total_q, H, TOPK), dtype=torch.int32, device=q.device)
         dbg_stride = int(scores_dbg.shape[-1]) if scores_dbg is not None else 0
-        _check(load_library().indexer_prefill(
+        _check(getattr(load_library(), fn)(
             self._h, _ptr(q, torch.uint8, "q"), _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1),
-            num_reqs, total_q, int(max_seqlen_q), _ptr(kv_pages, torch.uint8, "kv_pages", 3),
+            num_reqs, total_q, int(max_seqlen_q), _ptr(kv_pages, torch.uint8, "kv_pages", pages_ndim),
             int(kv_pages.shape[0]), _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
             _ptr(seq_lens, torch.int32, "seq_lens", 1), _ptr(out, torch.int32, "out"),
             _ptr(scores_dbg, torch.float32, "scores_dbg"), dbg_stride, _stream_ptr(stream)))
@@ -183,7 +211,18 @@ class Plan:
 
 
 def insert(k_bf16, slot_mapping, kv_pages, status=None, stream=None):
-    """Quantise bf16 keys [n, 128] to NVFP4 and write them at ``slot_mapping``."""
+    """Quantise bf16 keys [n, 128] to NVFP4 and write them at ``slot_mapping``
+    (``nvfp4_insert``; pages [num_blocks, 128, 72])."""
+    return _insert("nvfp4_insert", 3, k_bf16, slot_mapping, kv_pages, status, stream)
+
+
+def mxfp4_insert(k_bf16, slot_mapping, pages, status=None, stream=None):
+    """Quantise bf16 keys [n, 128] to MXFP4 and write them at ``slot_mapping``
+    (``mxfp4_insert``; pages [num_blocks, 8704])."""
+    return _insert("mxfp4_insert", 2, k_bf16, slot_mapping, pages, status, stream)
+
+
+def _insert(fn, pages_ndim, k_bf16, slot_mapping, kv_pages, status, stream):
     import torch
     if k_bf16.dim() != 2 or k_bf16.shape[1] != 128:
         raise ValueError("k_bf16: expected [n, 128]")
@@ -191,9 +230,9 @@ def insert(k_bf16, slot_mapping, kv_pages, status=None, stream=None):
     n = int(kb.shape[0])
     if slot_mapping.shape[0] != n:
         raise ValueError("slot_mapping must have one entry per key")
-    _check(load_library().nvfp4_insert(
+    _check(getattr(load_library(), fn)(
         _ptr(kb, torch.int16, "k_bf16"), _ptr(slot_mapping, torch.int64, "slot_mapping", 1), n,
-        _ptr(kv_pages, torch.uint8, "kv_pages", 3), int(kv_pages.shape[0]),
+        _ptr(kv_pages, torch.uint8, "kv_pages", pages_ndim), int(kv_pages.shape[0]),
         _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
     return kv_pages
 

@@ -54,6 +54,126 @@ struct indexer_plan_s {
   int32_t* pslot = nullptr;    // [2 * num_sms][kPreSlotInts]
 };
 
+// One body per entry point family; page_format picks the page codec.
+static int decode_impl(const char* fn, int page_format, indexer_plan_t plan, const uint8_t* q,
+                       const uint8_t* kv_pages, int num_blocks, const int32_t* page_table, int pt_stride,
+                       const int32_t* seq_lens, int num_reqs, int query_len, int32_t* out,
+                       float* scores_dbg, int dbg_stride, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "%s: plan is NULL", fn);
+  if (!q || !kv_pages || !page_table || !seq_lens || !out)
+    return set_err(IDX_EINVAL, "%s: NULL array argument", fn);
+  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
+    return set_err(IDX_EINVAL, "%s: q, kv_pages and out must be 16-byte aligned", fn);
+  if (query_len < 1 || query_len > 8)
+    return set_err(IDX_EUNSUPPORTED, "%s: query_len=%d, supported 1..8", fn, query_len);
+  if (query_len > plan->max_query_len)
+    return set_err(IDX_ENOSPACE, "%s: query_len=%d > plan max %d", fn, query_len, plan->max_query_len);
+  if (num_reqs < 1 || num_reqs > plan->max_reqs)
+    return set_err(IDX_ENOSPACE, "%s: num_reqs=%d outside 1..%d", fn, num_reqs, plan->max_reqs);
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "%s: num_blocks=%d", fn, num_blocks);
+  if (pt_stride < 1 || pt_stride > plan->max_pages)
+    return set_err(IDX_ENOSPACE, "%s: pt_stride=%d outside 1..%d", fn, pt_stride, plan->max_pages);
+  if (scores_dbg && dbg_stride < pt_stride)
+    return set_err(IDX_EINVAL, "%s: dbg_stride=%d < pt_stride=%d", fn, dbg_stride, pt_stride);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != plan->device)
+    return set_err(IDX_EINVAL, "%s: current device %d, plan made on %d", fn, dev, plan->device);
+
+  DecodeParams p{};
+  p.q = q;
+  p.kv = kv_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.scores_dbg = scores_dbg;
+  p.cand = plan->cand;
+  p.slot_bad = plan->slot_bad;
+  p.req_info = plan->req_info;
+  p.status = plan->status;
+  p.num_blocks = num_blocks;
+  p.pt_stride = pt_stride;
+  p.num_reqs = num_reqs;
+  p.qlen = query_len;
+  p.H = plan->num_heads;
+  p.R = query_len * plan->num_heads;
+  p.dbg_stride = dbg_stride;
+  p.page_format = page_format;
+  cudaError_t e = launch_decode(p, plan->decode_grid, stream);
+  if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
+  return IDX_OK;
+}
+
+static int prefill_impl(const char* fn, int page_format, indexer_plan_t plan, const uint8_t* q,
+                        const int32_t* cu_seqlens_q, int num_reqs, int total_q, int max_seqlen_q,
+                        const uint8_t* kv_pages, int num_blocks, const int32_t* page_table, int pt_stride,
+                        const int32_t* seq_lens, int32_t* out, float* scores_dbg, int dbg_stride,
+                        cudaStream_t stream) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "%s: plan is NULL", fn);
+  if (!q || !cu_seqlens_q || !kv_pages || !page_table || !seq_lens || !out)
+    return set_err(IDX_EINVAL, "%s: NULL array argument", fn);
+  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
+    return set_err(IDX_EINVAL, "%s: q, kv_pages and out must be 16-byte aligned", fn);
+  if (num_reqs < 1 || num_reqs > plan->max_prefill_reqs)
+    return set_err(IDX_ENOSPACE, "%s: num_reqs=%d outside 1..%d", fn, num_reqs, plan->max_prefill_reqs);
+  if (total_q < 0 || total_q > plan->max_prefill_tokens)
+    return set_err(IDX_ENOSPACE, "%s: total_q=%d outside 0..%d", fn, total_q, plan->max_prefill_tokens);
+  if (max_seqlen_q < 0 || max_seqlen_q > total_q)
+    return set_err(IDX_EINVAL, "%s: max_seqlen_q=%d outside 0..total_q", fn, max_seqlen_q);
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "%s: num_blocks=%d", fn, num_blocks);
+  if (pt_stride < 1 || pt_stride > plan->max_pages)
+    return set_err(IDX_ENOSPACE, "%s: pt_stride=%d outside 1..%d", fn, pt_stride, plan->max_pages);
+  if (scores_dbg && dbg_stride < pt_stride)
+    return set_err(IDX_EINVAL, "%s: dbg_stride=%d < pt_stride=%d", fn, dbg_stride, pt_stride);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != plan->device)
+    return set_err(IDX_EINVAL, "%s: current device %d, plan made on %d", fn, dev, plan->device);
+  if (total_q == 0) return IDX_OK;
+
+  PrefillParams p{};
+  p.q = q;
+  p.kv = kv_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.out = out;
+  p.scores_dbg = scores_dbg;
+  p.status = plan->status;
+  p.num_blocks = num_blocks;
+  p.pt_stride = pt_stride;
+  p.num_reqs = num_reqs;
+  p.total_q = total_q;
+  p.H = plan->num_heads;
+  p.dbg_stride = dbg_stride;
+  p.pcand = plan->pcand;
+  p.pslot = plan->pslot;
+  const int grid = plan->num_sms;   // one prefill CTA per SM; the work is split evenly by pages
+  p.page_format = page_format;
+  cudaError_t e = launch_prefill(p, grid, stream);
+  if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
+  return IDX_OK;
+}
+
+static int insert_impl(const char* fn, int page_format, const uint16_t* k_bf16, const int64_t* slot_mapping,
+                       int n, uint8_t* kv_pages, int num_blocks, int32_t* status, cudaStream_t stream) {
+  g_last_error.clear();
+  if (n < 0) return set_err(IDX_EINVAL, "%s: n=%d", fn, n);
+  if (n == 0) return IDX_OK;
+  if (!k_bf16 || !slot_mapping || !kv_pages)
+    return set_err(IDX_EINVAL, "%s: NULL array argument", fn);
+  if (!aligned16(k_bf16) || !aligned16(kv_pages) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return set_err(IDX_EINVAL, "%s: k_bf16 and kv_pages must be 16-byte aligned, slot_mapping 8", fn);
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "%s: num_blocks=%d", fn, num_blocks);
+  cudaError_t e = page_format == kPagesMxfp4
+                      ? launch_insert_mxfp4(k_bf16, slot_mapping, n, kv_pages, num_blocks, status, stream)
+                      : launch_insert(k_bf16, slot_mapping, n, kv_pages, num_blocks, status, stream);
+  if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
+  return IDX_OK;
+}
+
 extern "C" {
 
 const char* indexer_version(void) { return "nvfp4_indexer 0.1 sm_103a"; }
@@ -129,117 +249,52 @@ int indexer_plan_destroy(indexer_plan_t plan) {
   return IDX_OK;
 }
 
+
+
+
 int indexer_decode(indexer_plan_t plan, const uint8_t* q, const uint8_t* kv_pages, int num_blocks,
                    const int32_t* page_table, int pt_stride, const int32_t* seq_lens, int num_reqs,
                    int query_len, int32_t* out, float* scores_dbg, int dbg_stride, cudaStream_t stream) {
-  g_last_error.clear();
-  if (!plan) return set_err(IDX_EINVAL, "indexer_decode: plan is NULL");
-  if (!q || !kv_pages || !page_table || !seq_lens || !out)
-    return set_err(IDX_EINVAL, "indexer_decode: NULL array argument");
-  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
-    return set_err(IDX_EINVAL, "indexer_decode: q, kv_pages and out must be 16-byte aligned");
-  if (query_len < 1 || query_len > 8)
-    return set_err(IDX_EUNSUPPORTED, "indexer_decode: query_len=%d, supported 1..8", query_len);
-  if (query_len > plan->max_query_len)
-    return set_err(IDX_ENOSPACE, "indexer_decode: query_len=%d > plan max %d", query_len, plan->max_query_len);
-  if (num_reqs < 1 || num_reqs > plan->max_reqs)
-    return set_err(IDX_ENOSPACE, "indexer_decode: num_reqs=%d outside 1..%d", num_reqs, plan->max_reqs);
-  if (num_blocks < 1) return set_err(IDX_EINVAL, "indexer_decode: num_blocks=%d", num_blocks);
-  if (pt_stride < 1 || pt_stride > plan->max_pages)
-    return set_err(IDX_ENOSPACE, "indexer_decode: pt_stride=%d outside 1..%d", pt_stride, plan->max_pages);
-  if (scores_dbg && dbg_stride < pt_stride)
-    return set_err(IDX_EINVAL, "indexer_decode: dbg_stride=%d < pt_stride=%d", dbg_stride, pt_stride);
-  int dev = -1;
-  cudaGetDevice(&dev);
-  if (dev != plan->device)
-    return set_err(IDX_EINVAL, "indexer_decode: current device %d, plan made on %d", dev, plan->device);
+  return decode_impl("indexer_decode", kPagesNvfp4, plan, q, kv_pages, num_blocks, page_table, pt_stride,
+                     seq_lens, num_reqs, query_len, out, scores_dbg, dbg_stride, stream);
+}
 
-  DecodeParams p{};
-  p.q = q;
-  p.kv = kv_pages;
-  p.page_table = page_table;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.scores_dbg = scores_dbg;
-  p.cand = plan->cand;
-  p.slot_bad = plan->slot_bad;
-  p.req_info = plan->req_info;
-  p.status = plan->status;
-  p.num_blocks = num_blocks;
-  p.pt_stride = pt_stride;
-  p.num_reqs = num_reqs;
-  p.qlen = query_len;
-  p.H = plan->num_heads;
-  p.R = query_len * plan->num_heads;
-  p.dbg_stride = dbg_stride;
-  cudaError_t e = launch_decode(p, plan->decode_grid, stream);
-  if (e != cudaSuccess) return cuda_err(e, "indexer_decode: launch");
-  return IDX_OK;
+int indexer_decode_mxfp4(indexer_plan_t plan, const uint8_t* q, const uint8_t* pages, int num_blocks,
+                         const int32_t* page_table, int pt_stride, const int32_t* seq_lens, int num_reqs,
+                         int query_len, int32_t* out, float* scores_dbg, int dbg_stride,
+                         cudaStream_t stream) {
+  return decode_impl("indexer_decode_mxfp4", kPagesMxfp4, plan, q, pages, num_blocks, page_table,
+                     pt_stride, seq_lens, num_reqs, query_len, out, scores_dbg, dbg_stride, stream);
 }
 
 int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seqlens_q, int num_reqs,
                     int total_q, int max_seqlen_q, const uint8_t* kv_pages, int num_blocks,
                     const int32_t* page_table, int pt_stride, const int32_t* seq_lens, int32_t* out,
                     float* scores_dbg, int dbg_stride, cudaStream_t stream) {
-  g_last_error.clear();
-  if (!plan) return set_err(IDX_EINVAL, "indexer_prefill: plan is NULL");
-  if (!q || !cu_seqlens_q || !kv_pages || !page_table || !seq_lens || !out)
-    return set_err(IDX_EINVAL, "indexer_prefill: NULL array argument");
-  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
-    return set_err(IDX_EINVAL, "indexer_prefill: q, kv_pages and out must be 16-byte aligned");
-  if (num_reqs < 1 || num_reqs > plan->max_prefill_reqs)
-    return set_err(IDX_ENOSPACE, "indexer_prefill: num_reqs=%d outside 1..%d", num_reqs, plan->max_prefill_reqs);
-  if (total_q < 0 || total_q > plan->max_prefill_tokens)
-    return set_err(IDX_ENOSPACE, "indexer_prefill: total_q=%d outside 0..%d", total_q, plan->max_prefill_tokens);
-  if (max_seqlen_q < 0 || max_seqlen_q > total_q)
-    return set_err(IDX_EINVAL, "indexer_prefill: max_seqlen_q=%d outside 0..total_q", max_seqlen_q);
-  if (num_blocks < 1) return set_err(IDX_EINVAL, "indexer_prefill: num_blocks=%d", num_blocks);
-  if (pt_stride < 1 || pt_stride > plan->max_pages)
-    return set_err(IDX_ENOSPACE, "indexer_prefill: pt_stride=%d outside 1..%d", pt_stride, plan->max_pages);
-  if (scores_dbg && dbg_stride < pt_stride)
-    return set_err(IDX_EINVAL, "indexer_prefill: dbg_stride=%d < pt_stride=%d", dbg_stride, pt_stride);
-  int dev = -1;
-  cudaGetDevice(&dev);
-  if (dev != plan->device)
-    return set_err(IDX_EINVAL, "indexer_prefill: current device %d, plan made on %d", dev, plan->device);
-  if (total_q == 0) return IDX_OK;
+  return prefill_impl("indexer_prefill", kPagesNvfp4, plan, q, cu_seqlens_q, num_reqs, total_q,
+                      max_seqlen_q, kv_pages, num_blocks, page_table, pt_stride, seq_lens, out, scores_dbg,
+                      dbg_stride, stream);
+}
 
-  PrefillParams p{};
-  p.q = q;
-  p.kv = kv_pages;
-  p.page_table = page_table;
-  p.seq_lens = seq_lens;
-  p.cu_seqlens_q = cu_seqlens_q;
-  p.out = out;
-  p.scores_dbg = scores_dbg;
-  p.status = plan->status;
-  p.num_blocks = num_blocks;
-  p.pt_stride = pt_stride;
-  p.num_reqs = num_reqs;
-  p.total_q = total_q;
-  p.H = plan->num_heads;
-  p.dbg_stride = dbg_stride;
-  p.pcand = plan->pcand;
-  p.pslot = plan->pslot;
-  const int grid = plan->num_sms;   // one prefill CTA per SM; the work is split evenly by pages
-  cudaError_t e = launch_prefill(p, grid, stream);
-  if (e != cudaSuccess) return cuda_err(e, "indexer_prefill: launch");
-  return IDX_OK;
+int indexer_prefill_mxfp4(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seqlens_q, int num_reqs,
+                          int total_q, int max_seqlen_q, const uint8_t* pages, int num_blocks,
+                          const int32_t* page_table, int pt_stride, const int32_t* seq_lens, int32_t* out,
+                          float* scores_dbg, int dbg_stride, cudaStream_t stream) {
+  return prefill_impl("indexer_prefill_mxfp4", kPagesMxfp4, plan, q, cu_seqlens_q, num_reqs, total_q,
+                      max_seqlen_q, pages, num_blocks, page_table, pt_stride, seq_lens, out, scores_dbg,
+                      dbg_stride, stream);
 }
 
 int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* kv_pages,
                  int num_blocks, int32_t* status, cudaStream_t stream) {
-  g_last_error.clear();
-  if (n < 0) return set_err(IDX_EINVAL, "nvfp4_insert: n=%d", n);
-  if (n == 0) return IDX_OK;
-  if (!k_bf16 || !slot_mapping || !kv_pages)
-    return set_err(IDX_EINVAL, "nvfp4_insert: NULL array argument");
-  if (!aligned16(k_bf16) || !aligned16(kv_pages) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
-    return set_err(IDX_EINVAL, "nvfp4_insert: k_bf16 and kv_pages must be 16-byte aligned, slot_mapping 8");
-  if (num_blocks < 1) return set_err(IDX_EINVAL, "nvfp4_insert: num_blocks=%d", num_blocks);
-  cudaError_t e = launch_insert(k_bf16, slot_mapping, n, kv_pages, num_blocks, status, stream);
-  if (e != cudaSuccess) return cuda_err(e, "nvfp4_insert: launch");
-  return IDX_OK;
+  return insert_impl("nvfp4_insert", kPagesNvfp4, k_bf16, slot_mapping, n, kv_pages, num_blocks, status,
+                     stream);
+}
+
+int mxfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* pages,
+                 int num_blocks, int32_t* status, cudaStream_t stream) {
+  return insert_impl("mxfp4_insert", kPagesMxfp4, k_bf16, slot_mapping, n, pages, num_blocks, status,
+                     stream);
 }
 
 int indexer_get_status(indexer_plan_t plan, cudaStream_t stream, int32_t* bits) {

@@ -61,6 +61,124 @@ __device__ __forceinline__ void dequant16(uint32_t c0, uint32_t c1, uint32_t s2,
   for (int i = 0; i < 8; ++i) o[i] = hmul2_u32(o[i], s2);
 }
 
+// ---------------------------------------------------------------- MXFP4
+// (page vllm.models.minimax_m3.amd.indexer_mxfp4: e2m1 codes with e8m0
+// scales, one per 32 elements.)  A code times 2^(s - 127) has at most two
+// significant bits and an exponent anywhere in E8M0's range, so the exact
+// operand type is bf16 (fp16's exponent range is too small); E4M3 queries
+// are exact in bf16 too.
+
+// f16x2 -> bf16x2 for values that bf16 holds exactly (all here do).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2) {
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));   // first source -> high half
+  return r;
+}
+// Two E8M0 bytes (low byte first) -> bf16x2 {2^(lo - 127), 2^(hi - 127)};
+// 0xFF -> NaN.  bf16 holds every E8M0 value (2^-127 as a subnormal).
+__device__ __forceinline__ uint32_t e8m0x2_to_bf16x2(uint32_t two_bytes) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.bf16x2.ue8m0x2 %0, h;\n\t}" : "=r"(out) : "r"(two_bytes));
+  return out;
+}
+// bf16x2 product, round-to-nearest (exact for the operands used here).
+__device__ __forceinline__ uint32_t bmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// 16 MXFP4 elements sharing one scale: 8 code bytes (two words) and the
+// scale already broadcast as bf16x2 -> 8 bf16x2 words (elements in order).
+__device__ __forceinline__ void dequant16_mx(uint32_t c0, uint32_t c1, uint32_t s2, uint32_t* o) {
+  uint32_t h[8];
+  e2m1x8_to_f16x2x4(c0, h[0], h[1], h[2], h[3]);
+  e2m1x8_to_f16x2x4(c1, h[4], h[5], h[6], h[7]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = bmul2_u32(f16x2_to_bf16x2(h[i]), s2);
+}
+// floor(log2(a)) of a positive finite fp32 (normal or subnormal).
+__device__ __forceinline__ int floor_log2_f32(float a) {
+  const uint32_t u = __float_as_uint(a);
+  const int e = (int)(u >> 23);
+  if (e > 0) return e - 127;
+  return (31 - __clz((int)(u & 0x7FFFFFu))) - 149;   // m * 2^-149
+}
+// 2^E as fp32 for E in [-127, 127] (2^-127 is a subnormal).
+__device__ __forceinline__ float exp2i_f32(int E) {
+  return E >= -126 ? __uint_as_float((uint32_t)(E + 127) << 23) : __uint_as_float(1u << 22);
+}
+
+// ------------------------------------------------------ page formats
+// What the scoring kernels need from a page format: the page size the TMA
+// unit copies, the MMA operand type, the queries widened to it, and one
+// token's 128 elements as 64 words of that type, 16 elements at a time.
+struct Nvfp4Pages {   // [num_blocks, 128, 72]: token rows of 64 code bytes + 8 E4M3 scales
+  static constexpr uint32_t kPageBytes = 128 * 72;
+  static constexpr bool kBf16 = false;
+  struct Row {
+    uint32_t w[16];   // code words
+    uint32_t sc[4];   // scale pairs as f16x2 {scale 2j, scale 2j+1}
+  };
+  __device__ static __forceinline__ void load(const uint8_t* page, int tok, Row& r) {
+    const uint2* src = reinterpret_cast<const uint2*>(page + tok * 72);
+    uint32_t s01 = 0, s23 = 0;
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const uint2 t2 = src[i];
+      if (i < 8) {
+        r.w[2 * i] = t2.x;
+        r.w[2 * i + 1] = t2.y;
+      } else {
+        s01 = t2.x;
+        s23 = t2.y;
+      }
+    }
+    r.sc[0] = e4m3x2_to_f16x2(s01 & 0xFFFFu);
+    r.sc[1] = e4m3x2_to_f16x2(s01 >> 16);
+    r.sc[2] = e4m3x2_to_f16x2(s23 & 0xFFFFu);
+    r.sc[3] = e4m3x2_to_f16x2(s23 >> 16);
+  }
+  __device__ static __forceinline__ void chunk16(const Row& r, int g8, uint32_t* o) {
+    const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(r.sc[g8 >> 1]) : f16x2_bcast_lo(r.sc[g8 >> 1]);
+    dequant16(r.w[2 * g8], r.w[2 * g8 + 1], s2, o);
+  }
+  __device__ static __forceinline__ uint32_t widen_q(uint32_t two_e4m3) { return e4m3x2_to_f16x2(two_e4m3); }
+};
+
+struct Mxfp4Pages {   // [num_blocks, 8704]: 128 x 64 code bytes, then 128 x 4 E8M0 scales
+  static constexpr uint32_t kPageBytes = 128 * 64 + 128 * 4;
+  static constexpr bool kBf16 = true;
+  struct Row {
+    uint32_t w[16];   // code words
+    uint32_t sc[4];   // scale j (elements 32j .. 32j+31) broadcast as bf16x2
+  };
+  __device__ static __forceinline__ void load(const uint8_t* page, int tok, Row& r) {
+    const uint4* src = reinterpret_cast<const uint4*>(page + tok * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 t4 = src[i];
+      r.w[4 * i] = t4.x;
+      r.w[4 * i + 1] = t4.y;
+      r.w[4 * i + 2] = t4.z;
+      r.w[4 * i + 3] = t4.w;
+    }
+    const uint32_t s4 = *reinterpret_cast<const uint32_t*>(page + 128 * 64 + tok * 4);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t b = (s4 >> (8 * j)) & 0xFFu;
+      r.sc[j] = e8m0x2_to_bf16x2(b | (b << 8));
+    }
+  }
+  __device__ static __forceinline__ void chunk16(const Row& r, int g8, uint32_t* o) {
+    dequant16_mx(r.w[2 * g8], r.w[2 * g8 + 1], r.sc[g8 >> 1], o);
+  }
+  __device__ static __forceinline__ uint32_t widen_q(uint32_t two_e4m3) {
+    return f16x2_to_bf16x2(e4m3x2_to_f16x2(two_e4m3));
+  }
+};
+
 // fp32 -> E4M3 byte, round-to-nearest-even, saturating to +-448.
 __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float x) {
   uint16_t r;

@@ -80,12 +80,12 @@ struct DecD {
   }
 };
 
-template <int NQ>
+template <int NQ, class PF>   // PF: page format (codec.cuh)
 struct DecLayout {
-  static constexpr uint32_t kQBytes = NQ * 256;                   // fp16 [2][NQ][64], SW128
+  static constexpr uint32_t kQBytes = NQ * 256;                   // 16-bit [2][NQ][64], SW128
   static constexpr uint32_t kQOff = 0;                             // two query tiles
   static constexpr uint32_t kStageOff = 2 * kQBytes;               // multiple of 1024
-  static constexpr uint32_t kListOff = kStageOff + kDecStages * kPageBytes;  // [4 warps][64 rows][15] (score, id)
+  static constexpr uint32_t kListOff = kStageOff + kDecStages * PF::kPageBytes;  // [4 warps][64 rows][15] (score, id)
   static constexpr uint32_t kPreOff = kListOff + 4 * kMaxRows * kHistK * 8;
   // one CTA per SM: it holds all 512 tensor-memory columns
   static size_t bytes(int num_reqs) {
@@ -93,7 +93,8 @@ struct DecLayout {
     return b < 120 * 1024 ? 120 * 1024 : b;
   }
 };
-static_assert(1024 + DecLayout<64>::kPreOff + (kMaxDecodeReqs + 1) * 4 + 1024 <= 227 * 1024,
+static_assert(1024 + DecLayout<64, Nvfp4Pages>::kPreOff + (kMaxDecodeReqs + 1) * 4 + 1024 <= 227 * 1024 &&
+                  1024 + DecLayout<64, Mxfp4Pages>::kPreOff + (kMaxDecodeReqs + 1) * 4 + 1024 <= 227 * 1024,
               "decode shared memory above the 227 KB a CTA may hold");
 
 __device__ __forceinline__ int hist_pages(int seq_len, int pt_stride) {
@@ -184,9 +185,9 @@ struct SegWalk {
   }
 };
 
-template <int NQ>
+template <int NQ, class PF>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const DecodeParams p) {
-  using Lay = DecLayout<NQ>;
+  using Lay = DecLayout<NQ, PF>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kDecStages], raw_empty[kDecStages];
   __shared__ __align__(8) uint64_t a_full[kDecSlices];
@@ -349,9 +350,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
                     atomicOr(p.status, kStatusBadPage);
                     mbar_arrive(fb);
                   } else {
-                    mbar_arrive_expect_tx(fb, kPageBytes);
-                    bulk_g2s(sbase + Lay::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-                             kPageBytes, fb);
+                    mbar_arrive_expect_tx(fb, PF::kPageBytes);
+                    bulk_g2s(sbase + Lay::kStageOff + s * PF::kPageBytes, p.kv + (int64_t)phys * PF::kPageBytes,
+                             PF::kPageBytes, fb);
                   }
                 }
               }
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       // Issuer m takes slices m and m + 2 of every quad.
       if (lane == 0) {
         const int m = warp - 1;
-        constexpr uint32_t idesc = idesc_f16_f32(128, NQ);
+        constexpr uint32_t idesc = idesc_f16_f32(128, NQ, PF::kBf16);
         int64_t kq = 0;
         uint32_t last_bar = 0, last_par = 0;
         int sq = 0;
@@ -453,10 +454,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         uint4 o = make_uint4(0, 0, 0, 0);
         if (row < R) {
           const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.q + ((int64_t)walk.r * R + row) * 128 + c8 * 8));
-          o.x = e4m3x2_to_f16x2(e.x & 0xFFFFu);
-          o.y = e4m3x2_to_f16x2(e.x >> 16);
-          o.z = e4m3x2_to_f16x2(e.y & 0xFFFFu);
-          o.w = e4m3x2_to_f16x2(e.y >> 16);
+          o.x = PF::widen_q(e.x & 0xFFFFu);
+          o.y = PF::widen_q(e.x >> 16);
+          o.z = PF::widen_q(e.y & 0xFFFFu);
+          o.w = PF::widen_q(e.y >> 16);
         }
         *reinterpret_cast<uint4*>(qt + (c8 >> 3) * (NQ * 128) + sw128_offset(row, c8 & 7)) = o;
       }
@@ -476,27 +477,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           break;
         }
         if (!has) mbar_arrive(smem_u32(&raw_empty[st]));
-        const uint2* const page = reinterpret_cast<const uint2*>(base + Lay::kStageOff + st * kPageBytes);
+        const uint8_t* const page = base + Lay::kStageOff + st * PF::kPageBytes;
 #pragma unroll 1
         for (int sl = 0; sl < kDecSlices; ++sl) {
           uint32_t a[64];
           if (has) {
-            uint32_t w[18];
-            const uint2* src = page + (sl * 32 + lane) * (kRowBytes / 8);
-#pragma unroll
-            for (int i = 0; i < 9; ++i) {
-              const uint2 t2 = src[i];
-              w[2 * i] = t2.x;
-              w[2 * i + 1] = t2.y;
-            }
+            typename PF::Row row;
+            PF::load(page, sl * 32 + lane, row);
             if (sl == kDecSlices - 1) mbar_arrive(smem_u32(&raw_empty[st]));
-            const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
-                                    e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
 #pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
-              const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
-              dequant16(w[2 * g8], w[2 * g8 + 1], s2, a + 8 * g8);
-            }
+            for (int g8 = 0; g8 < 8; ++g8) PF::chunk16(row, g8, a + 8 * g8);
           }
           // A buffer sl is free once the MMAs of quad kq - 1 are done
           if (kq >= 1 &&
@@ -724,25 +714,31 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   if (lane == 0) write_out_row(out_row, res, L, false);
 }
 
-template <int NQ>
+template <int NQ, class PF>
 static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = DecLayout<NQ>::bytes(p.num_reqs);
-  cudaError_t e = cudaFuncSetAttribute(decode_score_kernel<NQ>,
+  const size_t smem = DecLayout<NQ, PF>::bytes(p.num_reqs);
+  cudaError_t e = cudaFuncSetAttribute(decode_score_kernel<NQ, PF>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_score_kernel<NQ><<<grid, kDecThreads, smem, stream>>>(p);
+  decode_score_kernel<NQ, PF><<<grid, kDecThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;
   return launch_dependent(decode_merge_kernel, (unsigned)((warps + 7) / 8), 256u, 0, stream, p);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
+template <class PF>
+static cudaError_t launch_decode_pf(const DecodeParams& p, int grid, cudaStream_t stream) {
   switch (decode_nq(p.R)) {
-    case 16: return launch_decode_nq<16>(p, grid, stream);
-    case 32: return launch_decode_nq<32>(p, grid, stream);
-    default: return launch_decode_nq<64>(p, grid, stream);
+    case 16: return launch_decode_nq<16, PF>(p, grid, stream);
+    case 32: return launch_decode_nq<32, PF>(p, grid, stream);
+    default: return launch_decode_nq<64, PF>(p, grid, stream);
   }
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
+  return p.page_format == kPagesMxfp4 ? launch_decode_pf<Mxfp4Pages>(p, grid, stream)
+                                      : launch_decode_pf<Nvfp4Pages>(p, grid, stream);
 }
 
 }  // namespace nvfp4idx

@@ -15,6 +15,10 @@ constexpr int kMaxRows = 64;      // query_len (<= 8) x heads (<= 8) per request
 constexpr int kMaxDecodeReqs = 4096;   // per-request prefix sums live in shared memory
 constexpr int kMaxPrefillReqs = 4096;
 
+// index-K page formats
+constexpr int kPagesNvfp4 = 0;    // [num_blocks, 128, 72]: E2M1 codes + E4M3 scales per 16
+constexpr int kPagesMxfp4 = 1;    // [num_blocks, 8704]: E2M1 codes, then E8M0 scales per 32
+
 // device status bits (mirror IDX_STATUS_* in include/nvfp4_indexer.h)
 constexpr int32_t kStatusBadPage = 1;
 constexpr int32_t kStatusBadTable = 2;
@@ -33,6 +37,7 @@ struct DecodeParams {
   int2* req_info;              // [num_reqs] (first CTA, number of segments)
   int32_t* status;
   int num_blocks, pt_stride, num_reqs, qlen, H, R, dbg_stride;
+  int page_format;             // kPagesNvfp4 / kPagesMxfp4
 };
 
 struct PrefillParams {
@@ -50,6 +55,7 @@ struct PrefillParams {
   float2* pcand;
   int32_t* pslot;
   int num_blocks, pt_stride, num_reqs, total_q, H, dbg_stride;
+  int page_format;             // kPagesNvfp4 / kPagesMxfp4
 };
 constexpr int kPreSlotInts = 20;
 
@@ -74,6 +80,8 @@ cudaError_t launch_dependent(void (*kernel)(Args...), unsigned grid, unsigned bl
 
 cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
                           int num_blocks, int32_t* status, cudaStream_t stream);
+cudaError_t launch_insert_mxfp4(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
+                                int num_blocks, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream);   // + the merge
 

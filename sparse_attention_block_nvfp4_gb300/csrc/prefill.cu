@@ -60,15 +60,17 @@ constexpr uint32_t kRegsCtl = 56, kRegsDq = 88, kRegsEpi = 120;
 constexpr uint32_t kPreTmemCols = 512;     // tile A: D [0,128), [128,256); tile B: [256,384), [384,512)
 constexpr uint32_t kTileBytes = 128 * 256; // fp16 [2 K-blocks][128 rows][64], 128B swizzle
 
+template <class PF>   // page format (codec.cuh)
 struct PreLayout {
   static constexpr uint32_t kQOff = 0;                           // A tiles of tile A and tile B
   static constexpr uint32_t kBOff = 2 * kTileBytes;              // B tiles of dequant groups 0 and 1
   static constexpr uint32_t kStageOff = kBOff + 2 * kTileBytes;
-  static constexpr uint32_t kTpreOff = kStageOff + kPreStages * kPageBytes;
+  static constexpr uint32_t kTpreOff = kStageOff + kPreStages * PF::kPageBytes;
   // two prefix arrays per request: tiles and possible pairs
   static size_t bytes(int num_reqs) { return 1024 + kTpreOff + (size_t)(num_reqs + 1) * 8; }
 };
-static_assert(1024 + PreLayout::kTpreOff + (kMaxPrefillReqs + 1) * 8 + 1024 <= 227 * 1024,
+static_assert(1024 + PreLayout<Nvfp4Pages>::kTpreOff + (kMaxPrefillReqs + 1) * 8 + 1024 <= 227 * 1024 &&
+                  1024 + PreLayout<Mxfp4Pages>::kTpreOff + (kMaxPrefillReqs + 1) * 8 + 1024 <= 227 * 1024,
               "prefill shared memory above the 227 KB a CTA may hold");
 
 struct TileRows {
@@ -187,8 +189,9 @@ struct PreWalk {
   }
 };
 
-template <int H>
+template <int H, class PF>
 __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillParams p) {
+  using PreLayout = nvfp4idx::PreLayout<PF>;
   constexpr int TQ = 128 / H;     // tokens per tile
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kPreStages], raw_empty[kPreStages];
@@ -380,9 +383,9 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
             if (phys < 0 || phys >= p.num_blocks) {
               mbar_arrive(fb);
             } else {
-              mbar_arrive_expect_tx(fb, kPageBytes);
-              bulk_g2s(sbase + PreLayout::kStageOff + s * kPageBytes, p.kv + (int64_t)phys * kPageBytes,
-                       kPageBytes, fb);
+              mbar_arrive_expect_tx(fb, PF::kPageBytes);
+              bulk_g2s(sbase + PreLayout::kStageOff + s * PF::kPageBytes, p.kv + (int64_t)phys * PF::kPageBytes,
+                       PF::kPageBytes, fb);
             }
           }
         }
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       // Issuer x multiplies every page against tile x's queries.
       if (lane == 0) {
         const int x = warp - 1;
-        constexpr uint32_t idesc = idesc_f16_f32(128, 128);
+        constexpr uint32_t idesc = idesc_f16_f32(128, 128, PF::kBf16);
         const uint32_t qaddr = sbase + PreLayout::kQOff + (uint32_t)x * kTileBytes;
         int64_t g = 0;
         int ip = 0;                                   // pairs with pages so far
@@ -466,16 +469,8 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           ok = false;
           break;
         }
-        uint32_t w[18];
-        {
-          const uint2* src = reinterpret_cast<const uint2*>(base + PreLayout::kStageOff + s * kPageBytes + tok * kRowBytes);
-#pragma unroll
-          for (int i = 0; i < 9; ++i) {
-            const uint2 t2 = src[i];
-            w[2 * i] = t2.x;
-            w[2 * i + 1] = t2.y;
-          }
-        }
+        typename PF::Row row;
+        PF::load(base + PreLayout::kStageOff + s * PF::kPageBytes, tok, row);
         mbar_arrive(smem_u32(&raw_empty[s]));
         // the B tile is free once both tiles' MMAs of page g - 2 are done:
         // phase (g - 2) / 2 of d_full[0][grp] and d_full[1][grp] (this group
@@ -489,13 +484,10 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           ok = false;
           break;
         }
-        const uint32_t sc[4] = {e4m3x2_to_f16x2(w[16] & 0xFFFFu), e4m3x2_to_f16x2(w[16] >> 16),
-                                e4m3x2_to_f16x2(w[17] & 0xFFFFu), e4m3x2_to_f16x2(w[17] >> 16)};
 #pragma unroll
         for (int g8 = 0; g8 < 8; ++g8) {
-          const uint32_t s2 = (g8 & 1) ? f16x2_bcast_hi(sc[g8 >> 1]) : f16x2_bcast_lo(sc[g8 >> 1]);
           uint32_t o[8];
-          dequant16(w[2 * g8], w[2 * g8 + 1], s2, o);
+          PF::chunk16(row, g8, o);
           // elements 16*g8 .. +15 = 16-byte chunks 2*g8, 2*g8+1 of the row
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -552,8 +544,8 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
             uint32_t a[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              a[2 * k] = e4m3x2_to_f16x2(ew[k] & 0xFFFFu);
-              a[2 * k + 1] = e4m3x2_to_f16x2(ew[k] >> 16);
+              a[2 * k] = PF::widen_q(ew[k] & 0xFFFFu);
+              a[2 * k + 1] = PF::widen_q(ew[k] >> 16);
             }
             // 16 query bytes = elements 16i .. 16i+15 = 16-byte chunks 2i, 2i+1
 #pragma unroll
@@ -717,26 +709,32 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
   }
 }
 
-template <int H>
+template <int H, class PF>
 static cudaError_t launch_prefill_h(const PrefillParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = PreLayout::bytes(p.num_reqs);   // > 114 KB: one CTA per SM
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = PreLayout<PF>::bytes(p.num_reqs);   // > 114 KB: one CTA per SM
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<H, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<H><<<grid, kPreThreads, smem, stream>>>(p);
+  prefill_kernel<H, PF><<<grid, kPreThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prefill_merge_kernel<H><<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream) {
+template <class PF>
+static cudaError_t launch_prefill_pf(const PrefillParams& p, int grid, cudaStream_t stream) {
   switch (p.H) {
-    case 1: return launch_prefill_h<1>(p, grid, stream);
-    case 2: return launch_prefill_h<2>(p, grid, stream);
-    case 4: return launch_prefill_h<4>(p, grid, stream);
-    default: return launch_prefill_h<8>(p, grid, stream);
+    case 1: return launch_prefill_h<1, PF>(p, grid, stream);
+    case 2: return launch_prefill_h<2, PF>(p, grid, stream);
+    case 4: return launch_prefill_h<4, PF>(p, grid, stream);
+    default: return launch_prefill_h<8, PF>(p, grid, stream);
   }
+}
+
+cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream) {
+  return p.page_format == kPagesMxfp4 ? launch_prefill_pf<Mxfp4Pages>(p, grid, stream)
+                                      : launch_prefill_pf<Nvfp4Pages>(p, grid, stream);
 }
 
 }  // namespace nvfp4idx

@@ -268,11 +268,11 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major,
-// shape M x N (M = 128, N multiple of 16, 16..256).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+// Instruction descriptor, kind::f16: fp16 (or, with bf16, bf16) A and B,
+// fp32 D, both K-major, shape M x N (M = 128, N multiple of 16, 16..256).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool bf16 = false) {
   return (1u << 4)                               // D format: f32
-         | (0u << 7) | (0u << 10)                // A, B format: f16
+         | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10)   // A, B format: f16 (0) / bf16 (1)
          | (0u << 15) | (0u << 16)               // A, B K-major
          | ((uint32_t)(N >> 3) << 17)            // N / 8
          | ((uint32_t)(M >> 4) << 24);           // M / 16
