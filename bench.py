@@ -89,9 +89,11 @@ def work_counts(w: workloads.Workload) -> dict:
         R = ql * H
         out["dec_pages_scored"] = int(hist_rows.sum()) * H
         out["dec_bytes"] = int(req_pages.sum()) * (9216 + 4) + w.num_decode_reqs * (R * 128 + R * 64 + 4)
+        # the same over MXFP4 pages (8704 bytes)
+        out["dec_bytes_mx"] = int(req_pages.sum()) * (8704 + 4) + w.num_decode_reqs * (R * 128 + R * 64 + 4)
         out["dec_flops"] = int(req_pages.sum()) * 2 * 128 * 128 * R
     else:
-        out.update(dec_pages_scored=0, dec_bytes=0, dec_flops=0)
+        out.update(dec_pages_scored=0, dec_bytes=0, dec_bytes_mx=0, dec_flops=0)
     # prefill
     if w.num_prefill_reqs:
         tot = 0
@@ -319,6 +321,46 @@ def gpu_arm(args, w, rank, world, local):
         if i > 0:
             fill_ms.append(a.elapsed_time(b))
 
+    # ---- MXFP4 pages: the same decode / prefill calls over an MXFP4 copy of
+    # the cache (filled by mxfp4_insert, timed like the NVFP4 fill), each
+    # call timed alone with the L2 flushed before it; not part of the step
+    mx = None
+    if args.mxfp4:
+        idx = st.idx
+        pages = torch.zeros((w.num_blocks, 8704), dtype=torch.uint8, device=dev)
+        mx = {"fill": []}
+
+        def timed(fn, key, reps):
+            for i in range(reps):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                if key is not None and i >= 3:
+                    mx.setdefault(key, []).append(a.elapsed_time(b))
+        for i in range(4):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            idx.mxfp4_insert(st.k_all, st.slot_all, pages, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            if i > 0:
+                mx["fill"].append(a.elapsed_time(b))
+        d = st.d
+        reps = 3 + max(3, min(args.steps, 50))
+        if w.num_decode_reqs:
+            timed(lambda: st.plan.decode_mxfp4(d["q_dec"], pages, d["dec_table"], d["dec_seq"], w.query_len,
+                                               out=st.out[: st.nd], stream=stream), "decode", reps)
+        if w.num_prefill_reqs:
+            timed(lambda: st.plan.prefill_mxfp4(d["q_pre"], d["cu"], pages, d["pre_table"], d["pre_seq"],
+                                                st.max_q, out=st.out[st.nd:], stream=stream), "prefill", reps)
+        torch.cuda.synchronize()
+        mx["status"] = st.plan.status()
+        del pages
+
     # ---- end to end: host buffers in, ids out, through the same C ABI calls
     e2e = None
     if args.e2e:
@@ -349,7 +391,7 @@ def gpu_arm(args, w, rank, world, local):
         e2e = {"value": work["pages_scored"] * args.steps * world / e2e_s, "unit": "pages/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
     return dict(st=st, work=work, step_ms=step_ms, kern_ms=kern_ms, total_s=total_s, clk=clk.summary(),
-                e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2])
+                e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2], mx=mx)
 
 
 def roofline_block(res, w, wname, peaks, peak_kind):
@@ -380,7 +422,29 @@ def roofline_block(res, w, wname, peaks, peak_kind):
         kernels["insert_fill"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": gb / peaks["hbm_gbs"], "ms": res["fill_ms"], "keys": int(n_all),
                                   "note": "whole-cache insert, timed apart from the step"}
-    dom = max((k for k in kernels if k != "insert_fill"), key=lambda k: kernels[k]["ms"])
+    mx = res.get("mx")
+    if mx:
+        med = lambda v: sorted(v)[len(v) // 2]
+        if mx.get("prefill"):
+            ms = sum(mx["prefill"]) / len(mx["prefill"])
+            tf = work["pre_flops"] / (ms / 1e3) / 1e12
+            kernels["prefill_mxfp4"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "ms": ms,
+                                        "note": "MXFP4 pages, bf16 operands; timed alone, not part of the step"}
+        if mx.get("decode"):
+            ms = sum(mx["decode"]) / len(mx["decode"])
+            gb = work["dec_bytes_mx"] / (ms / 1e3) / 1e9
+            kernels["decode_mxfp4"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": gb / peaks["hbm_gbs"], "ms": ms,
+                                       "note": "MXFP4 pages (8704 B); timed alone, not part of the step"}
+        if mx.get("fill"):
+            ms = med(mx["fill"])
+            gb = n_all * (256 + 8 + 68) / (ms / 1e3) / 1e9
+            kernels["insert_fill_mxfp4"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"],
+                                            "unit": "GB/s", "frac": gb / peaks["hbm_gbs"], "ms": ms,
+                                            "keys": int(n_all), "note": "whole-cache MXFP4 insert"}
+    step_kernels = ("insert", "decode", "prefill")
+    dom = max((k for k in kernels if k in step_kernels), key=lambda k: kernels[k]["ms"])
     rl = dict(kernels[dom])
     rl.pop("ms", None)
     rl.pop("tensor_tflops", None)
@@ -472,6 +536,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-mxfp4", dest="mxfp4", action="store_false",
+                    help="skip the MXFP4-page timings (kernels decode_mxfp4 / prefill_mxfp4 / insert_fill_mxfp4)")
     ap.add_argument("--sweep", action="store_true", help="one line per named workload (no e2e / cpu)")
     ap.add_argument("--no-flush", dest="flush", action="store_false",
                     help="skip the L2 flush (profiling runs only; the timed numbers then see a warm L2)")
@@ -540,7 +606,7 @@ def main():
             "kernels": kernels,
             "gpu_launches": res["st"].launches_per_step * args.steps,
             "clocks": res["clk"],
-            "device_status": res["status"],
+            "device_status": res["status"] | ((res["mx"] or {}).get("status", 0)),
         }
         if res["e2e"] is not None:
             line["e2e"] = res["e2e"]
