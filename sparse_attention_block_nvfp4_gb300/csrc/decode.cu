@@ -385,6 +385,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           const int qs = sq & 1;
           if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
           const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
+          // B (query) descriptors of the 8 K steps of this segment
+          uint64_t bd[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            bd[kk] = desc_advance(smem_desc_sw128(qaddr), (uint32_t)((kk >> 2) * (NQ * 128) + (kk & 3) * 32));
           bool ok = true;
           for (; walk.j < je && ok; ++kq) {
             const int npq = min(4, je - walk.j);
@@ -402,14 +407,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
               }
               tc_fence_after();
               const uint32_t d_t = tbase + DecD<NQ>::col(kq, sl);
-              const uint32_t a_t = tbase + sl * 64;
+              uint32_t at[8];
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * (NQ * 128) + (kk & 3) * 32);
-                mma_f16_tmemA(d_t, a_t + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-              }
-              // d_full also tells the dequant warps that A buffer sl is free
-              mma_commit(smem_u32(&d_full[kq & 1][sl]));
+              for (int kk = 0; kk < 8; ++kk) at[kk] = tbase + sl * 64 + kk * 8;
+              // the slice's 8 MMAs and one commit: d_full also tells the
+              // dequant warps that A buffer sl is free
+              mma8_f16_ts_commit(d_t, at, bd, idesc, smem_u32(&d_full[kq & 1][sl]));
               last_bar = smem_u32(&d_full[kq & 1][sl]);
               last_par = (uint32_t)((kq >> 1) & 1);
             }

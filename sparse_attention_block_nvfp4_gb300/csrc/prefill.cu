@@ -73,6 +73,12 @@ static_assert(1024 + PreLayout<Nvfp4Pages>::kTpreOff + (kMaxPrefillReqs + 1) * 8
                   1024 + PreLayout<Mxfp4Pages>::kTpreOff + (kMaxPrefillReqs + 1) * 8 + 1024 <= 227 * 1024,
               "prefill shared memory above the 227 KB a CTA may hold");
 
+// Byte offset of K step kk (16 elements) inside a 128B-swizzled K-major tile
+// of 128 rows: two K-blocks of 64 elements, 32 bytes per step within one.
+__host__ __device__ constexpr uint32_t kstep_bytes(int kk) {
+  return (uint32_t)(kk >> 2) * (128u * 128u) + (uint32_t)(kk & 3) * 32u;
+}
+
 struct TileRows {
   int t0, nt, row0;   // first token of the tile within the request, tokens, first q row
 };
@@ -401,6 +407,12 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         const int x = warp - 1;
         constexpr uint32_t idesc = idesc_f16_f32(128, 128, PF::kBf16);
         const uint32_t qaddr = sbase + PreLayout::kQOff + (uint32_t)x * kTileBytes;
+        // operand descriptors of every K step, computed once
+        uint64_t ad[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) ad[kk] = desc_advance(smem_desc_sw128(qaddr), kstep_bytes(kk));
+        const uint64_t bdesc_t0 = smem_desc_sw128(sbase + PreLayout::kBOff);
+        const uint64_t bdesc_t1 = smem_desc_sw128(sbase + PreLayout::kBOff + kTileBytes);
         int64_t g = 0;
         int ip = 0;                                   // pairs with pages so far
         uint32_t last_bar = 0, last_par = 0;
@@ -422,17 +434,14 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
               break;
             }
             tc_fence_after();
-            const uint32_t bt = sbase + PreLayout::kBOff + (uint32_t)b * kTileBytes;
             const uint32_t dt = tbase + (uint32_t)(x * 256 + b * 128);
+            const uint64_t bdesc = b ? bdesc_t1 : bdesc_t0;     // B tile of the page's dequant group
+            uint64_t bd[8];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t koff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-              mma_f16_ss(dt, smem_desc_sw128(qaddr + koff), smem_desc_sw128(bt + koff), idesc,
-                         kk > 0 ? 1u : 0u);
-            }
-            // one commit per page: d_full[x][b] also tells dequant group b
-            // that tile x is done with its B tile
-            mma_commit(smem_u32(&d_full[x][b]));
+            for (int kk = 0; kk < 8; ++kk) bd[kk] = desc_advance(bdesc, kstep_bytes(kk));
+            // the page's 8 MMAs and one commit: d_full[x][b] also tells
+            // dequant group b that tile x is done with its B tile
+            mma8_f16_ss_commit(dt, ad, bd, idesc, smem_u32(&d_full[x][b]));
             last_bar = smem_u32(&d_full[x][b]);
             last_par = par;
           }
