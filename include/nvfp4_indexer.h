@@ -68,6 +68,12 @@ enum {
   IDX_STATUS_BAD_SLOT = 8      /* nvfp4_insert skipped a slot past the cache    */
 };
 
+/* Page formats (indexer_decode_partial). */
+enum {
+  IDX_PAGES_NVFP4 = 0,         /* [num_blocks][128][72]                         */
+  IDX_PAGES_MXFP4 = 1          /* [num_blocks][8704]                            */
+};
+
 typedef struct indexer_plan_s* indexer_plan_t;
 
 /*
@@ -206,6 +212,49 @@ int indexer_prefill_mxfp4(indexer_plan_t plan, const uint8_t* q, const int32_t* 
                           int num_blocks, const int32_t* page_table, int pt_stride,
                           const int32_t* seq_lens, int32_t* out, float* scores_dbg, int dbg_stride,
                           cudaStream_t stream);
+
+/*
+ * Decode context parallelism (page vllm.models.minimax_m3.nvidia.indexer_nvfp4:
+ * the per-layer decode-CP buffers and decode_cp.forward, which the indexer
+ * uses when the decode batch's history is spread over ranks).  Each rank holds
+ * a share of every request's history pages, scores only those, and keeps each
+ * row's 15 best (score, logical page id); one all-gather of 15 x 8 bytes per
+ * (row, head) and a merge under the same order (score descending, page id
+ * ascending) give exactly the rows indexer_decode computes over the whole
+ * history.  This library reads the split as a contiguous page range per
+ * request and rank (the pages do not show it).
+ *
+ * indexer_decode_partial -- one rank's share of a decode batch.
+ *   page_format  IDX_PAGES_NVFP4 or IDX_PAGES_MXFP4 (the layout of `pages`)
+ *   page_lo, page_hi  int32 [num_reqs]: the logical history pages this rank
+ *                scores for request r are [page_lo[r], page_hi[r]) cut to the
+ *                request's history; page_table[r][j] must map each such j to
+ *                this rank's `pages`
+ *   cand_out     float [num_reqs * query_len][H][15][2], 16-byte aligned:
+ *                (score, page id as int32 bits) pairs sorted by score
+ *                descending, page id ascending; id -1 = no candidate, id -2 in
+ *                entry 0 = the request has an unreadable page in this share
+ *   other arguments as indexer_decode (no scores_dbg); rows are not written.
+ */
+int indexer_decode_partial(indexer_plan_t plan, int page_format, const uint8_t* q, const uint8_t* pages,
+                           int num_blocks, const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
+                           const int32_t* page_lo, const int32_t* page_hi, int num_reqs, int query_len,
+                           float* cand_out, cudaStream_t stream);
+
+/*
+ * indexer_merge_candidates -- the final rows from `world` ranks' candidates.
+ *   cand_all   float [world][num_reqs * query_len][num_heads][15][2], rank
+ *              major (as an all-gather of every rank's cand_out lays them out),
+ *              16-byte aligned; the ranks' page ranges must be disjoint
+ *   seq_lens   int32 [num_reqs], as given to indexer_decode_partial
+ *   out        int32 [num_reqs * query_len][num_heads][16]: the 15 best
+ *              history pages over all ranks, the local page, then -1; all -1
+ *              for a row with negative position or an unreadable page
+ *   status     NULL, or a device int32 that gets IDX_STATUS_BAD_PAGE OR-ed in
+ *              when a rank marked a request unreadable
+ */
+int indexer_merge_candidates(const float* cand_all, int world, int num_reqs, int query_len, int num_heads,
+                             const int32_t* seq_lens, int32_t* out, int32_t* status, cudaStream_t stream);
 
 /*
  * indexer_decode_noalloc -- indexer_decode for callers that cannot allocate

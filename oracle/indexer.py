@@ -202,3 +202,52 @@ def prefill(q, cu_seqlens_q, kv_pages, page_table, seq_lens, num_heads: int,
     to seq_lens[r] (context = seq_len - query_len tokens before them)."""
     cu = np.asarray(cu_seqlens_q, dtype=np.int64)
     return _run(q, kv_pages, page_table, seq_lens, np.diff(cu), num_heads, rows, page_format)
+
+
+def partial_candidates(res: Result, page_lo, page_hi, query_len: int):
+    """One context-parallel rank's candidates (page
+    vllm.models.minimax_m3.nvidia.indexer_nvfp4: ``decode_cp.forward`` keeps
+    each rank's best pages per row and merges them): for every decode row and
+    head, the row's history pages j in [page_lo[r], page_hi[r]) ordered by
+    (S descending, j ascending), the first 15, then -1.  ``res`` is the
+    oracle over the whole history.  Returns ids int32 [rows, H, 15] and their
+    scores float64 (NaN where the id is -1)."""
+    rows, H = res.out.shape[:2]
+    ids = np.full((rows, H, HIST_TOPK), -1, dtype=np.int32)
+    sc = np.full((rows, H, HIST_TOPK), np.nan)
+    for t in range(rows):
+        r = t // query_len
+        Lr = int(res.L[t])
+        if Lr <= 0 or res.bad[t]:
+            continue
+        lo, hi = max(0, int(page_lo[r])), min(Lr, int(page_hi[r]))
+        if hi <= lo:
+            continue
+        js = np.arange(lo, hi)
+        for h in range(H):
+            S = res.S[t, h, lo:hi]
+            order = np.lexsort((js, -S))[:HIST_TOPK]
+            ids[t, h, :order.size] = js[order]
+            sc[t, h, :order.size] = S[order]
+    return ids, sc
+
+
+def merge_candidates(ids_list, sc_list, L):
+    """Final rows [rows, H, 16] from several ranks' candidates: the first
+    min(15, count) of all candidates by (score descending, id ascending),
+    then the local page L[row], then -1 (all -1 where L < 0)."""
+    ids = np.concatenate(ids_list, axis=2)
+    sc = np.concatenate(sc_list, axis=2)
+    rows, H = ids.shape[:2]
+    out = np.full((rows, H, TOPK), -1, dtype=np.int32)
+    for t in range(rows):
+        if L[t] < 0:
+            continue
+        for h in range(H):
+            ok = ids[t, h] >= 0
+            cid, cs = ids[t, h][ok], sc[t, h][ok]
+            order = np.lexsort((cid, -cs))[:HIST_TOPK]
+            m = order.size
+            out[t, h, :m] = cid[order]
+            out[t, h, m] = L[t]
+    return out

@@ -29,6 +29,7 @@ PAGE = 128
 TOPK = 16
 STATUS_BAD_PAGE, STATUS_BAD_TABLE, STATUS_TIMEOUT, STATUS_BAD_SLOT = 1, 2, 4, 8
 IDX_OK, IDX_EINVAL, IDX_EUNSUPPORTED, IDX_ECUDA, IDX_ENOSPACE, IDX_EDEVICE = 0, -1, -2, -3, -4, -5
+IDX_PAGES_NVFP4, IDX_PAGES_MXFP4 = 0, 1
 
 _lib = None
 
@@ -67,12 +68,14 @@ def load_library():
     lib.indexer_decode_mxfp4.argtypes = lib.indexer_decode.argtypes
     lib.indexer_prefill_mxfp4.argtypes = lib.indexer_prefill.argtypes
     lib.mxfp4_insert.argtypes = lib.nvfp4_insert.argtypes
+    lib.indexer_decode_partial.argtypes = [P, I, P, P, I, P, I, P, P, P, I, I, P, P]
+    lib.indexer_merge_candidates.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.indexer_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.indexer_last_error.restype = ctypes.c_char_p
     lib.indexer_version.restype = ctypes.c_char_p
     for name in ("indexer_plan", "indexer_plan_destroy", "indexer_decode", "indexer_prefill",
                  "nvfp4_insert", "indexer_get_status", "indexer_decode_mxfp4", "indexer_prefill_mxfp4",
-                 "mxfp4_insert"):
+                 "mxfp4_insert", "indexer_decode_partial", "indexer_merge_candidates"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -158,6 +161,28 @@ class Plan:
         return self._prefill("indexer_prefill_mxfp4", 2, q, cu_seqlens_q, pages, page_table, seq_lens,
                              max_seqlen_q, out, scores_dbg, stream)
 
+    def decode_partial(self, q, pages, page_table, seq_lens, page_lo, page_hi, query_len: int,
+                       page_format: str = "nvfp4", cand_out=None, stream=None):
+        """One context-parallel rank's share of a decode batch
+        (``indexer_decode_partial``): scores request r's history pages in
+        [page_lo[r], page_hi[r]) only and returns the rows' candidates, float32
+        [rows, H, 15, 2] of (score, page id bits)."""
+        import torch
+        H = self.num_heads
+        num_reqs = int(seq_lens.shape[0])
+        if q.dim() != 3 or q.shape[0] != num_reqs * query_len or q.shape[1] != H or q.shape[2] != 128:
+            raise ValueError(f"q: expected [{num_reqs * query_len}, {H}, 128], got {tuple(q.shape)}")
+        fmt = {"nvfp4": (IDX_PAGES_NVFP4, 3), "mxfp4": (IDX_PAGES_MXFP4, 2)}[page_format]
+        if cand_out is None:
+            cand_out = torch.empty((q.shape[0], H, 15, 2), dtype=torch.float32, device=q.device)
+        _check(load_library().indexer_decode_partial(
+            self._h, fmt[0], _ptr(q, torch.uint8, "q"), _ptr(pages, torch.uint8, "pages", fmt[1]),
+            int(pages.shape[0]), _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
+            _ptr(seq_lens, torch.int32, "seq_lens", 1), _ptr(page_lo, torch.int32, "page_lo", 1),
+            _ptr(page_hi, torch.int32, "page_hi", 1), num_reqs, int(query_len),
+            _ptr(cand_out, torch.float32, "cand_out", 4), _stream_ptr(stream)))
+        return cand_out
+
     def _decode(self, fn, pages_ndim, q, kv_pages, page_table, seq_lens, query_len, out, scores_dbg,
                 stream):
         import torch
@@ -235,6 +260,49 @@ def _insert(fn, pages_ndim, k_bf16, slot_mapping, kv_pages, status, stream):
         _ptr(kv_pages, torch.uint8, "kv_pages", pages_ndim), int(kv_pages.shape[0]),
         _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
     return kv_pages
+
+
+def merge_candidates(cand_all, seq_lens, query_len: int, num_heads: int, out=None, status=None, stream=None):
+    """``indexer_merge_candidates``: final rows [rows, H, 16] from the
+    candidates of ``world`` ranks, ``cand_all`` float32 [world, rows, H, 15, 2]."""
+    import torch
+    if cand_all.dim() != 5 or cand_all.shape[2] != num_heads or cand_all.shape[3] != 15:
+        raise ValueError(f"cand_all: expected [world, rows, {num_heads}, 15, 2], got {tuple(cand_all.shape)}")
+    num_reqs = int(seq_lens.shape[0])
+    if cand_all.shape[1] != num_reqs * query_len:
+        raise ValueError("cand_all rows != num_reqs * query_len")
+    if out is None:
+        out = torch.empty((cand_all.shape[1], num_heads, TOPK), dtype=torch.int32, device=cand_all.device)
+    _check(load_library().indexer_merge_candidates(
+        _ptr(cand_all, torch.float32, "cand_all", 5), int(cand_all.shape[0]), num_reqs, int(query_len),
+        int(num_heads), _ptr(seq_lens, torch.int32, "seq_lens", 1), _ptr(out, torch.int32, "out"),
+        _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
+    return out
+
+
+def gather_candidates(cand, group=None):
+    """All-gather every rank's candidates into one rank-major tensor
+    [world, rows, H, 15, 2] (torch.distributed; the one exchange of decode
+    context parallelism).  Without an initialised process group: one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return cand.unsqueeze(0)
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(cand) for _ in range(world)]
+    dist.all_gather(parts, cand.contiguous(), group=group)
+    return torch.stack(parts)
+
+
+def decode_cp(plan, q, pages, page_table, seq_lens, page_lo, page_hi, query_len: int, page_format="nvfp4",
+              group=None, out=None, stream=None):
+    """Decode context parallelism: this rank's share (``decode_partial``), one
+    all-gather of the candidates over ``group``, then the merge; returns the
+    final rows on every rank."""
+    cand = plan.decode_partial(q, pages, page_table, seq_lens, page_lo, page_hi, query_len,
+                               page_format=page_format, stream=stream)
+    return merge_candidates(gather_candidates(cand, group), seq_lens, query_len, plan.num_heads, out=out,
+                            stream=stream)
 
 
 def decode_noalloc(q, kv_pages, page_table, seq_lens, query_len: int, num_heads: int, out=None,

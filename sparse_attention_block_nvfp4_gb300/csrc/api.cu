@@ -58,12 +58,17 @@ struct indexer_plan_s {
 static int decode_impl(const char* fn, int page_format, indexer_plan_t plan, const uint8_t* q,
                        const uint8_t* kv_pages, int num_blocks, const int32_t* page_table, int pt_stride,
                        const int32_t* seq_lens, int num_reqs, int query_len, int32_t* out,
-                       float* scores_dbg, int dbg_stride, cudaStream_t stream) {
+                       float* scores_dbg, int dbg_stride, cudaStream_t stream,
+                       const int32_t* page_lo = nullptr, const int32_t* page_hi = nullptr,
+                       float* cand_out = nullptr) {
   g_last_error.clear();
   if (!plan) return set_err(IDX_EINVAL, "%s: plan is NULL", fn);
-  if (!q || !kv_pages || !page_table || !seq_lens || !out)
+  if (page_format != kPagesNvfp4 && page_format != kPagesMxfp4)
+    return set_err(IDX_EUNSUPPORTED, "%s: page_format=%d", fn, page_format);
+  if (!q || !kv_pages || !page_table || !seq_lens || (!out && !cand_out))
     return set_err(IDX_EINVAL, "%s: NULL array argument", fn);
-  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out))
+  if (cand_out && (!page_lo || !page_hi)) return set_err(IDX_EINVAL, "%s: page_lo / page_hi are NULL", fn);
+  if (!aligned16(q) || !aligned16(kv_pages) || (out && !aligned16(out)) || (cand_out && !aligned16(cand_out)))
     return set_err(IDX_EINVAL, "%s: q, kv_pages and out must be 16-byte aligned", fn);
   if (query_len < 1 || query_len > 8)
     return set_err(IDX_EUNSUPPORTED, "%s: query_len=%d, supported 1..8", fn, query_len);
@@ -100,6 +105,9 @@ static int decode_impl(const char* fn, int page_format, indexer_plan_t plan, con
   p.R = query_len * plan->num_heads;
   p.dbg_stride = dbg_stride;
   p.page_format = page_format;
+  p.page_lo = page_lo;
+  p.page_hi = page_hi;
+  p.cand_out = reinterpret_cast<float2*>(cand_out);
   cudaError_t e = launch_decode(p, plan->decode_grid, stream);
   if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
   return IDX_OK;
@@ -265,6 +273,32 @@ int indexer_decode_mxfp4(indexer_plan_t plan, const uint8_t* q, const uint8_t* p
                          cudaStream_t stream) {
   return decode_impl("indexer_decode_mxfp4", kPagesMxfp4, plan, q, pages, num_blocks, page_table,
                      pt_stride, seq_lens, num_reqs, query_len, out, scores_dbg, dbg_stride, stream);
+}
+
+int indexer_decode_partial(indexer_plan_t plan, int page_format, const uint8_t* q, const uint8_t* pages,
+                           int num_blocks, const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
+                           const int32_t* page_lo, const int32_t* page_hi, int num_reqs, int query_len,
+                           float* cand_out, cudaStream_t stream) {
+  return decode_impl("indexer_decode_partial", page_format, plan, q, pages, num_blocks, page_table, pt_stride,
+                     seq_lens, num_reqs, query_len, nullptr, nullptr, 0, stream, page_lo, page_hi, cand_out);
+}
+
+int indexer_merge_candidates(const float* cand_all, int world, int num_reqs, int query_len, int num_heads,
+                             const int32_t* seq_lens, int32_t* out, int32_t* status, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!cand_all || !seq_lens || !out) return set_err(IDX_EINVAL, "indexer_merge_candidates: NULL array argument");
+  if (!aligned16(cand_all) || !aligned16(out))
+    return set_err(IDX_EINVAL, "indexer_merge_candidates: cand_all and out must be 16-byte aligned");
+  if (world < 1) return set_err(IDX_EINVAL, "indexer_merge_candidates: world=%d", world);
+  if (!valid_heads(num_heads))
+    return set_err(IDX_EUNSUPPORTED, "indexer_merge_candidates: num_heads=%d, supported 1, 2, 4, 8", num_heads);
+  if (query_len < 1 || query_len > 8)
+    return set_err(IDX_EUNSUPPORTED, "indexer_merge_candidates: query_len=%d, supported 1..8", query_len);
+  if (num_reqs < 0) return set_err(IDX_EINVAL, "indexer_merge_candidates: num_reqs=%d", num_reqs);
+  cudaError_t e = launch_cp_merge(reinterpret_cast<const float2*>(cand_all), world, num_reqs, query_len,
+                                  num_heads, seq_lens, out, status, stream);
+  if (e != cudaSuccess) return cuda_err(e, "indexer_merge_candidates: launch");
+  return IDX_OK;
 }
 
 int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seqlens_q, int num_reqs,

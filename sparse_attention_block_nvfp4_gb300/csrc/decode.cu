@@ -102,6 +102,29 @@ __device__ __forceinline__ int hist_pages(int seq_len, int pt_stride) {
   return h > pt_stride ? 0 : h;   // a history wider than the table is finalised as bad by the merge
 }
 
+// First history page request r scores (0, or its context-parallel share's).
+__device__ __forceinline__ int req_lo(const DecodeParams& p, int r) {
+  return p.page_lo ? max(0, __ldg(p.page_lo + r)) : 0;
+}
+// Pages request r scores: its history, cut to [page_lo, page_hi) for a
+// context-parallel share.
+__device__ __forceinline__ int req_pages(const DecodeParams& p, int r) {
+  const int h = hist_pages(__ldg(p.seq_lens + r), p.pt_stride);
+  if (!p.page_lo) return h;
+  const int hi = min(h, __ldg(p.page_hi + r));
+  return max(0, hi - req_lo(p, r));
+}
+
+// A row's 15 candidates (score, page id), sorted, for a context-parallel
+// merge; an unreadable request marks its list with id -2 first.
+__device__ __forceinline__ void write_cand_row(float2* row, const float* s, const int* id, bool bad) {
+#pragma unroll
+  for (int k = 0; k < kHistK; ++k) {
+    const int i = bad ? (k == 0 ? -2 : -1) : id[k];
+    row[k] = make_float2(i >= 0 ? s[k] : 0.0f, __int_as_float(i));
+  }
+}
+
 // CTA owning global page x when T pages are split over G CTAs.
 __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
   return (int)(((x + 1) * G - 1) / T);
@@ -170,18 +193,18 @@ struct SegWalk {
   int NR;
   int64_t n;        // pages in the range
   int64_t g;        // pages walked
-  int r, j;         // current request, page
+  int r, j;         // current request, page (logical id)
   __device__ __forceinline__ bool more() const { return g < n; }
   // pages [j, j_end) of request r form the current segment
-  __device__ __forceinline__ int seg_end() const {
-    const int hist = pre[r + 1] - pre[r];
+  __device__ __forceinline__ int seg_end(const DecodeParams& p) const {
+    const int end = req_lo(p, r) + (pre[r + 1] - pre[r]);
     const int64_t left = n - g;
-    return (int)((int64_t)hist < (int64_t)j + left ? (int64_t)hist : (int64_t)j + left);
+    return (int)((int64_t)end < (int64_t)j + left ? (int64_t)end : (int64_t)j + left);
   }
-  __device__ __forceinline__ void next_request() {
+  __device__ __forceinline__ void next_request(const DecodeParams& p) {
     ++r;
     while (r < NR && pre[r + 1] - pre[r] == 0) ++r;
-    j = 0;
+    j = r < NR ? req_lo(p, r) : 0;
   }
 };
 
@@ -217,7 +240,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     const int per = (NR + kDecThreads - 1) / kDecThreads;
     const int r0 = tid * per, r1 = min(NR, r0 + per);
     int sum = 0;
-    for (int r = r0; r < r1; ++r) sum += hist_pages(__ldg(p.seq_lens + r), p.pt_stride);
+    for (int r = r0; r < r1; ++r) sum += req_pages(p, r);
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -231,7 +254,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     int run = off + incl - sum;
     for (int r = r0; r < r1; ++r) {
       pre[r] = run;
-      run += hist_pages(__ldg(p.seq_lens + r), p.pt_stride);
+      run += req_pages(p, r);
     }
     if (tid == kDecThreads - 1) {
       int tot = 0;
@@ -300,7 +323,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     r_start = lo;
     while (pre[r_start + 1] - pre[r_start] == 0) ++r_start;
   }
-  SegWalk walk{pre, NR, n, 0, r_start, (int)(x0 - pre[r_start])};
+  SegWalk walk{pre, NR, n, 0, r_start, req_lo(p, r_start) + (int)(x0 - pre[r_start])};
   auto fail = [&]() {
     if (!abort_s) {
       abort_s = 1;
@@ -326,7 +349,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       int64_t last = -1;                                // lane s < 16: last quad that filled stage s
       bool ok = true;
       while (walk.more() && ok) {
-        const int je = walk.seg_end();
+        const int je = walk.seg_end(p);
         const int32_t* row = p.page_table + (int64_t)walk.r * p.pt_stride;
         for (int jb = walk.j; jb < je && ok; jb += 32) {
           const int cnt = min(32, je - jb);
@@ -366,7 +389,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         }
         walk.g += je - walk.j;
         walk.j = je;
-        if (ok && walk.more()) walk.next_request();
+        if (ok && walk.more()) walk.next_request(p);
       }
       // drain issued copies before the CTA may exit
       if (!ok && lane < kDecStages && last >= 0)
@@ -381,7 +404,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         uint32_t last_bar = 0, last_par = 0;
         int sq = 0;
         while (walk.more() && !abort_s) {
-          const int je = walk.seg_end();
+          const int je = walk.seg_end(p);
           const int qs = sq & 1;
           if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
           const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
@@ -420,7 +443,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           if (!ok || abort_s) break;
           mma_commit(smem_u32(&q_empty[qs]));
           ++sq;
-          if (walk.more()) walk.next_request();
+          if (walk.more()) walk.next_request(p);
         }
         // a commit covers every MMA issued before it: drain the last one
         // before tensor memory is freed
@@ -443,7 +466,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     int sq = 0;
     bool ok = true;
     while (walk.more() && ok) {
-      const int je = walk.seg_end();
+      const int je = walk.seg_end(p);
       const int qs = sq & 1;
       // the request's queries -> fp16 B tile (128B swizzle, K-major)
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty[qs]),
@@ -509,7 +532,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         }
       }
       ++sq;
-      if (ok && walk.more()) walk.next_request();
+      if (ok && walk.more()) walk.next_request(p);
     }
   } else {
     // ================================================= epilogue warpgroup
@@ -532,7 +555,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     int64_t kq = 0;
     bool ok = true;                                   // uniform within the warp
     while (walk.more()) {
-      const int je = walk.seg_end();
+      const int je = walk.seg_end(p);
       const int r = walk.r;
       const int seq_r = __ldg(p.seq_lens + r);
       const int pos0 = seq_r - p.qlen + lane / p.H, pos1 = seq_r - p.qlen + (lane + 32) / p.H;
@@ -615,7 +638,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           merge4_top15(lists, ep, ts, ti);
           const int pe = seq_r - p.qlen + ep / p.H;
           if (cf == cl) {
-            write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, ti, pe >= 0 ? (pe >> 7) : -1, bad != 0);
+            if (p.cand_out) write_cand_row(p.cand_out + ((int64_t)r * R + ep) * kHistK, ts, ti, bad != 0);
+            else write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, ti, pe >= 0 ? (pe >> 7) : -1, bad != 0);
           } else {
             float2* dst = p.cand + ((int64_t)(c + r) * R + ep) * kHistK;
 #pragma unroll
@@ -625,7 +649,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         if (ep == 0 && cf != cl) p.slot_bad[c + r] = bad;
       }
       named_bar_sync(2, 128);                         // lists are read before the next reset
-      if (walk.more()) walk.next_request();
+      if (walk.more()) walk.next_request(p);
     }
   }
 
@@ -651,10 +675,16 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   const int L = pos >= 0 ? (pos >> 7) : -1;
   const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
   int32_t* out_row = p.out + gw * kTopK;
-  const int none[1] = {-1};
+  float2* cand_row = p.cand_out ? p.cand_out + gw * kHistK : nullptr;   // context-parallel share
+  const int none[kHistK] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+  const float zs[kHistK] = {};
+  auto finish = [&](const float* s, const int* id, bool bad) {   // lane 0
+    if (cand_row) write_cand_row(cand_row, s, id, bad);
+    else write_out_row(out_row, id, L, bad);
+  };
   if (hist > p.pt_stride) {
     if (lane == 0) {
-      write_out_row(out_row, none, L, true);
+      finish(zs, none, true);
       atomicOr(p.status, kStatusBadTable);
     }
     return;
@@ -662,15 +692,15 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   const int2 info = p.req_info[r];
   const int nseg = info.y;
   if (nseg == 1) return;                      // finalised by the scoring kernel
-  if (nseg == 0) {                            // no history page: local page only
-    if (lane == 0) write_out_row(out_row, none, L, false);
+  if (nseg == 0) {                            // no history page (in the share): local page only
+    if (lane == 0) finish(zs, none, false);
     return;
   }
   const int slot0 = info.x + r;
   int bad = 0;
   for (int k = lane; k < nseg; k += 32) bad |= p.slot_bad[slot0 + k];
   if (__any_sync(0xffffffffu, bad)) {
-    if (lane == 0) write_out_row(out_row, none, L, true);
+    if (lane == 0) finish(zs, none, true);
     return;
   }
   // lane-local sorted list: list `lane` when nseg <= 32, else a top-15 of
@@ -702,6 +732,58 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   }
   __syncwarp();
   int res[kHistK];
+  float rs[kHistK];
+  int cur = 0;
+#pragma unroll
+  for (int k = 0; k < kHistK; ++k) {
+    float2 e = make_float2(0.0f, __int_as_float(-1));
+    if (cur < kHistK) e = lists[warp][lane][cur];
+    const int id = __float_as_int(e.y);
+    const uint32_t key = id >= 0 ? order_key(e.x) : 0u;
+    const uint32_t kmax = warp_max_u32(key);
+    const uint32_t idmin = warp_min_u32(key == kmax && kmax != 0u ? (uint32_t)id : 0xFFFFFFFFu);
+    if (kmax != 0u && key == kmax && (uint32_t)id == idmin) ++cur;
+    res[k] = kmax != 0u ? (int)idmin : -1;
+    rs[k] = kmax != 0u ? key_to_float(kmax) : 0.0f;
+  }
+  if (lane == 0) finish(rs, res, false);
+}
+
+// One warp per (row, head): merge the `world` context-parallel ranks'
+// candidate lists of the row (each sorted by score desc, id asc; the ranks'
+// page ranges are disjoint) into its final row.  Lane k holds rank k's list
+// (ranks k, k+32, ... folded in when world > 32).
+__global__ void __launch_bounds__(256) cp_merge_kernel(const float2* __restrict__ cand_all, int world,
+                                                       int num_reqs, int query_len, int H,
+                                                       const int32_t* __restrict__ seq_lens,
+                                                       int32_t* __restrict__ out, int32_t* status) {
+  __shared__ float2 lists[8][32][kHistK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)num_reqs * query_len * H;
+  const int64_t gw = (int64_t)blockIdx.x * 8 + warp;
+  if (gw >= rows) return;
+  const int t = (int)(gw / H);                          // query row
+  const int r = t / query_len, i = t % query_len;
+  const int pos = __ldg(seq_lens + r) - query_len + i;
+  const int L = pos >= 0 ? (pos >> 7) : -1;
+  int bad = 0;
+  TopK15 tk;
+  tk.reset();
+  for (int k = lane; k < world; k += 32) {
+    const float2* src = cand_all + ((int64_t)k * rows + gw) * kHistK;
+    bad |= __float_as_int(src[0].y) == -2;
+#pragma unroll
+    for (int e = 0; e < kHistK; ++e) {
+      const float2 v = src[e];
+      if (__float_as_int(v.y) >= 0) tk.insert_any(v.x, __float_as_int(v.y));
+    }
+  }
+  float2(&mine)[kHistK] = lists[warp][lane];
+#pragma unroll
+  for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(tk.s[k], __int_as_float(tk.id[k]));
+  __syncwarp();
+  bad = __any_sync(0xffffffffu, bad);
+  int res[kHistK];
   int cur = 0;
 #pragma unroll
   for (int k = 0; k < kHistK; ++k) {
@@ -714,7 +796,19 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     if (kmax != 0u && key == kmax && (uint32_t)id == idmin) ++cur;
     res[k] = kmax != 0u ? (int)idmin : -1;
   }
-  if (lane == 0) write_out_row(out_row, res, L, false);
+  if (lane == 0) {
+    write_out_row(out + gw * kTopK, res, L, bad != 0);
+    if (bad && status) atomicOr(status, kStatusBadPage);
+  }
+}
+
+cudaError_t launch_cp_merge(const float2* cand_all, int world, int num_reqs, int query_len, int H,
+                            const int32_t* seq_lens, int32_t* out, int32_t* status, cudaStream_t stream) {
+  const int64_t warps = (int64_t)num_reqs * query_len * H;
+  if (warps <= 0) return cudaSuccess;
+  cp_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(cand_all, world, num_reqs, query_len, H,
+                                                                   seq_lens, out, status);
+  return cudaGetLastError();
 }
 
 template <int NQ, class PF>

@@ -38,6 +38,12 @@ struct DecodeParams {
   int32_t* status;
   int num_blocks, pt_stride, num_reqs, qlen, H, R, dbg_stride;
   int page_format;             // kPagesNvfp4 / kPagesMxfp4
+  // a context-parallel rank's share (indexer_decode_partial): request r
+  // scores only its history pages in [page_lo[r], page_hi[r]) (NULL: all)
+  // and leaves each row's 15 candidates in cand_out instead of a final row
+  const int32_t* page_lo;
+  const int32_t* page_hi;
+  float2* cand_out;            // [rows][15] (score, id); NULL = final rows in out
 };
 
 struct PrefillParams {
@@ -83,6 +89,10 @@ cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_
 cudaError_t launch_insert_mxfp4(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
                                 int num_blocks, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
+// Merge the candidate lists of `world` context-parallel ranks ([world][rows][15],
+// rank-major) into final rows [rows][16].
+cudaError_t launch_cp_merge(const float2* cand_all, int world, int num_reqs, int query_len, int H,
+                            const int32_t* seq_lens, int32_t* out, int32_t* status, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream);   // + the merge
 
 // smallest power-of-two >= 16 that holds R rows (the MMA N dimension)

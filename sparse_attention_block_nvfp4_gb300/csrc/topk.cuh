@@ -46,6 +46,28 @@ struct TopK15 {
       }
     }
   }
+
+  // Insert (v, j) in any id order: equal scores rank the lower id first
+  // (for merging lists that were built over different pages).
+  __device__ __forceinline__ void insert_any(float v, int j) {
+    if (v > s[14] || (v == s[14] && (id[14] < 0 || j < id[14]))) {
+      bool ge[15];
+#pragma unroll
+      for (int i = 0; i < 15; ++i) ge[i] = s[i] > v || (s[i] == v && id[i] >= 0 && id[i] < j);
+#pragma unroll
+      for (int i = 14; i > 0; --i) {
+        const bool here = !ge[i] && ge[i - 1];
+        const float si = ge[i] ? s[i] : (here ? v : s[i - 1]);
+        const int ii = ge[i] ? id[i] : (here ? j : id[i - 1]);
+        s[i] = si;
+        id[i] = ii;
+      }
+      if (!ge[0]) {
+        s[0] = v;
+        id[0] = j;
+      }
+    }
+  }
 };
 
 // -0.0 -> +0.0 so that equal scores compare equal in the integer key below.

@@ -294,3 +294,21 @@ def test_checker_accepts_near_ties_and_rejects_errors():
     m = min(15, int(res.L[r]))
     bad3[r, h, m] = -1
     assert checker.check_ids(bad3, res)["fails"] == 1
+
+
+def test_cp_merge_of_any_split_is_the_full_selection():
+    """Decode context parallelism: merging the per-rank candidates of any
+    split of the history into page ranges gives the whole-history selection
+    (the top-15 of a union is the top-15 of the parts' top-15s)."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    w = workloads.config(2, small=True)
+    kv = nvfp4.insert(w.k_bf16, w.slot_mapping, np.zeros((w.num_blocks, 128, 72), np.uint8))
+    res = indexer.decode(w.q_decode, kv, w.dec_page_table, w.dec_seq_lens, w.query_len, w.num_heads)
+    hist = (w.dec_seq_lens.astype(np.int64) - 1) // 128
+    for world in (1, 2, 3, 5):
+        cuts = np.sort(rng.integers(0, hist[:, None] + 1, size=(len(hist), world - 1)), axis=1)
+        bounds = np.concatenate([np.zeros((len(hist), 1), np.int64), cuts, hist[:, None]], axis=1)
+        parts = [indexer.partial_candidates(res, bounds[:, k], bounds[:, k + 1], w.query_len)
+                 for k in range(world)]
+        out = indexer.merge_candidates([p[0] for p in parts], [p[1] for p in parts], res.L)
+        assert np.array_equal(out, res.out), world
