@@ -192,23 +192,72 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-// E2M1 code of x for a positive scale s: round-to-nearest-even of x/s,
-// saturating at 6, sign kept.  Decided by exact comparisons of |x| with the
-// midpoints m*s (m in {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5}; every m*s is an
-// exact fp32 product of a <=3-bit and a 4-bit significand); at a midpoint the
-// even code wins, so the comparison is '>' where the even code is below and
-// '>=' where it is above.
-__device__ __forceinline__ uint32_t e2m1_code(float x, float s) {
-  const float a = fabsf(x);
-  uint32_t m = 0;
-  m += (a > 0.25f * s);
-  m += (a >= 0.75f * s);
-  m += (a > 1.25f * s);
-  m += (a >= 1.75f * s);
-  m += (a > 2.5f * s);
-  m += (a >= 3.5f * s);
-  m += (a > 5.0f * s);
-  return m | ((__float_as_uint(x) >> 28) & 8u);
+// Eight fp32 values -> eight E2M1 codes in one word (element 0 in the low
+// nibble), each the round-to-nearest-even of the value, saturating at +-6,
+// the sign kept (a negative value that rounds to zero gives -0).
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float* v) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"   // second source -> low nibble
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return out;
+}
+
+// Per bf16 half: max(|a|, |b|), exact; the half's sign bit is the xor of
+// the operands' signs (ignored by the callers).
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// The larger magnitude of the two bf16 halves of a word, as fp32.
+__device__ __forceinline__ float bf16x2_amax_f32(uint32_t m) {
+  return fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
+}
+
+// 1/s to within one ulp, for a positive normal fp32 s.
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// x / s for a bf16 value x and a positive E4M3 scale s, given r within one
+// ulp of 1/s, in a form whose E2M1 rounding is that of the exact quotient
+// t = |x| / s: one fused multiply-add rounds |x| r to a multiple of 2^-12
+// (3 * 2^10 added has an ulp of 2^-12 while |x| r < 2^10), the addend is
+// taken off exactly and the sign of x put back.
+// Why it is exact: |x| = X 2^a (X < 2^8) and m s = M S 2^(b-2) for an E2M1
+// midpoint m = M/4 (M <= 20) and s = S 2^b (S < 2^4) are multiples of
+// 2^min(a, b-2), so t is either a midpoint or at least 2^-9 m >= 2^-11 away
+// from each midpoint m nearer than m/2.  |x| r is within 2^-23 t < 2^-19 of
+// t there, so at a midpoint (a multiple of 2^-12) the rounding returns it
+// exactly, and elsewhere the result stays within 2^-19 + 2^-13 < 2^-11 of
+// t: never across a midpoint.  Past 2^10 the quotient saturates either way.
+__device__ __forceinline__ float nvfp4_ratio(float x, float r) {
+  const float g = __fsub_rn(__fmaf_rn(fabsf(x), r, 3072.0f), 3072.0f);
+  return __uint_as_float(__float_as_uint(g) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// E4M3 byte of amax / 6, round-to-nearest-even of the exact quotient,
+// saturating at 448, for a bf16 value amax >= 0.  v = amax * fl(1/6) is
+// within 2^-23 of amax / 6 (relative; clamped at 1024, past which every
+// value saturates); Veltkamp's split with the constant 2^12 + 1 rounds it to
+// 12 significant bits.  An E4M3 midpoint u = U 2^e (U < 2^5) gives
+// 6u = 3U 2^(e+1) with 3U < 2^7 and amax = A 2^a with A < 2^8, so amax / 6
+// is either a midpoint (kept exactly by the 12-bit rounding) or at least
+// 2^-9 away from it relative to its size, which the 2^-23 + 2^-12 moved
+// does not cross; the hardware conversion then rounds as the exact value.
+__device__ __forceinline__ uint32_t e4m3_scale_of_amax(float amax) {
+  const float v = fminf(__fmul_rn(amax, 1.0f / 6.0f), 1024.0f);
+  const float c = __fmul_rn(v, 4097.0f);
+  const float hi = __fadd_rn(c, __fsub_rn(v, c));
+  return f32_to_e4m3_satfinite(hi);
 }
 
 }  // namespace nvfp4idx

@@ -89,6 +89,84 @@ def test_insert_edge_values_bit_exact():
     assert int(status.item()) == 0
 
 
+def _finite_bf16():
+    from oracle.formats import bf16_value
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]             # exponent field 0xFF: inf / NaN
+    return bits, bf16_value(bits)
+
+
+def _bf16_floor(v):
+    """Bits of the largest bf16 value below the positive real v (v < 2^128)."""
+    from oracle.formats import bf16_value
+    b = np.uint16(np.float32(v).view(np.uint32) >> 16)
+    while bf16_value(np.array([b]))[0] >= v:
+        b = np.uint16(b - 1)
+    return b
+
+
+def _pack_groups(groups, width):
+    g = np.concatenate(groups)
+    per_row = 128 // width
+    pad = (-g.shape[0]) % per_row
+    g = np.concatenate([g, np.zeros((pad, width), np.uint16)])
+    return g.reshape(-1, 128)
+
+
+def _every_value_every_scale():
+    """Groups that pair every finite bf16 value with every positive E4M3
+    scale it can meet.  For each scale s two kinds of group: element 0 is
+    6 s (the group's scale is then exactly s) and the other 15 run over every
+    x with |x| <= 6 s; or element 0 is the largest bf16 amax still rounding to
+    s (just under 6 times the midpoint above s; the largest finite bf16 for
+    s = 448) and the others run over every x with 6 s < |x| <= amax, where the
+    quotient saturates or sits just under 6."""
+    from oracle.formats import E4M3_POS, bf16_value, e4m3_round_nonneg
+    bits, val = _finite_bf16()
+    pos = E4M3_POS[E4M3_POS > 0]
+    groups = []
+    for i, s in enumerate(pos):
+        a = 6.0 * s
+        a_bits = np.uint16(np.float32(a).view(np.uint32) >> 16)
+        assert bf16_value(np.array([a_bits]))[0] == a
+        top = _bf16_floor(3 * (s + pos[i + 1])) if i + 1 < pos.size else np.uint16(0x7F7F)
+        top_v = bf16_value(np.array([top]))[0]
+        assert e4m3_round_nonneg(np.array([top_v / 6.0]))[0] == i + 1     # byte i+1 holds pos[i]
+        for amax_bits, sel in ((a_bits, np.abs(val) <= a),
+                               (top, (np.abs(val) > a) & (np.abs(val) <= top_v))):
+            xs = bits[sel]
+            xs = np.concatenate([xs, np.zeros((-xs.size) % 15, np.uint16)]).reshape(-1, 15)
+            groups.append(np.concatenate([np.full((xs.shape[0], 1), amax_bits, np.uint16), xs], 1))
+    return _pack_groups(groups, 16)
+
+
+def _every_amax():
+    """One group per finite non-zero bf16 value, alone in its group: every
+    amax the scale rounding can see."""
+    bits, val = _finite_bf16()
+    bits = bits[val != 0]
+    g = np.zeros((bits.size, 16), np.uint16)
+    g[:, 0] = bits
+    return _pack_groups([g], 16)
+
+
+@pytest.mark.parametrize("kind", ["every_value_every_scale", "every_amax"])
+def test_insert_exhaustive_bit_exact(kind):
+    """Every finite bf16 key value against every E4M3 scale, and every
+    amax: the kernel's bytes equal the oracle's exact rounding."""
+    import torch
+    import sparse_attention_block_nvfp4_gb300 as idx
+    k = _every_value_every_scale() if kind == "every_value_every_scale" else _every_amax()
+    n = k.shape[0]
+    nb = (n + 127) // 128
+    slots = np.arange(n, dtype=np.int64)
+    kv = torch.zeros((nb, 128, 72), dtype=torch.uint8, device=torch_dev())
+    idx.insert(up(k.view(np.int16)), up(slots), kv)
+    want = onvfp4.insert(k, slots, np.zeros((nb, 128, 72), np.uint8))
+    got = kv.cpu().numpy()
+    assert np.array_equal(got, want), f"{np.count_nonzero(got != want)} bytes differ"
+
+
 def test_insert_out_of_range_slot_sets_status_and_skips():
     import torch
     import sparse_attention_block_nvfp4_gb300 as idx

@@ -81,6 +81,45 @@ def test_mxfp4_insert_edge_values():
     assert np.array_equal(pages.cpu().numpy(), want)
 
 
+def _every_value_every_exponent():
+    """Blocks that pair every finite bf16 value with every shared exponent
+    it can meet: for each biased exponent field e of amax (1 .. 254) the
+    block's element 0 is the largest bf16 with that field (E = e - 129,
+    clamped to -127) and the other 31 run over every x with |x| <= amax."""
+    from oracle.formats import bf16_value
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]
+    mag = np.abs(bf16_value(bits))
+    order = np.argsort(mag, kind="stable")
+    bits, mag = bits[order], mag[order]
+    blocks = []
+    for e in range(1, 255):
+        amax_bits = np.uint16((e << 7) | 0x7F)
+        amax = bf16_value(np.array([amax_bits]))[0]
+        xs = bits[:np.searchsorted(mag, amax, side="right")]
+        xs = np.concatenate([xs, np.zeros((-xs.size) % 31, np.uint16)]).reshape(-1, 31)
+        blocks.append(np.concatenate([np.full((xs.shape[0], 1), amax_bits, np.uint16), xs], 1))
+    g = np.concatenate(blocks)
+    g = np.concatenate([g, np.zeros(((-g.shape[0]) % 4, 32), np.uint16)])
+    return g.reshape(-1, 128)
+
+
+def test_mxfp4_insert_exhaustive_bit_exact():
+    """Every finite bf16 key value against every shared exponent: the
+    kernel's bytes equal the oracle's exact rounding."""
+    import torch
+    import sparse_attention_block_nvfp4_gb300 as idx
+    k = _every_value_every_exponent()
+    n = k.shape[0]
+    nb = (n + 127) // 128
+    slots = np.arange(n, dtype=np.int64)
+    pages = torch.zeros((nb, omx.PAGE_BYTES), dtype=torch.uint8, device=torch_dev())
+    idx.mxfp4_insert(up(k.view(np.int16)), up(slots), pages)
+    want = omx.insert(k, slots, np.zeros((nb, omx.PAGE_BYTES), np.uint8))
+    got = pages.cpu().numpy()
+    assert np.array_equal(got, want), f"{np.count_nonzero(got != want)} bytes differ"
+
+
 def _run_decode(plan, w, pages, dbg=True):
     import torch
     d = torch.full((w.num_decode_rows, w.num_heads, w.page_table.shape[1]), float("nan"),
