@@ -30,6 +30,8 @@ Modules:
   mxfp4    - MXFP4 page decoding and the OCP MX quantise-insert (page
              vllm.models.minimax_m3.amd.indexer_mxfp4: the same scores and
              top-k over [pages, 8704] e2m1 / e8m0 pages).
+  norm_rope - qk-norm (RMSNorm) and RoPE of the index key before the NVFP4
+             insert, in the fp32 order the fused insert uses.
   indexer  - positions, page scores, selection; decode and prefill oracles.
   brute    - scalar pure-Python brute force for tiny inputs (a pin).
   checker  - parity checker (ids modulo score ties within tolerance).
@@ -39,4 +41,4 @@ tests/golden/, exhaustive format tables against torch / ml_dtypes casts,
 scalar brute force, closed-form special cases, invariants, and planted
 mistakes that each pin must catch.  No function here is "parity unpinned".
 """
-from . import formats, nvfp4, indexer, checker, brute  # noqa: F401
+from . import formats, nvfp4, norm_rope, indexer, checker, brute  # noqa: F401
