@@ -96,11 +96,13 @@ def norm_rope_f32(k_bf16, positions, weight_bf16, eps, cos_sin_cache, rotary_dim
         raise ValueError("rotary_dim must be even and in [0, 128]")
     x = bf16_to_f32(k_bf16).reshape(-1, DIM)
     w = bf16_to_f32(weight_bf16).reshape(DIM)
+    y = (x * rms_scale(x, eps)[:, None]) * w[None, :]
+    if rotary_dim == 0:                     # norm only: positions and table unused
+        return y
     cache = np.asarray(cos_sin_cache, dtype=F32)
     pos = np.asarray(positions, dtype=np.int64)
     if np.any(pos < 0) or np.any(pos >= cache.shape[0]):
         raise ValueError("position outside the cos/sin table")
-    y = (x * rms_scale(x, eps)[:, None]) * w[None, :]
     h = rotary_dim // 2
     rows = cache[pos]
     return rotate(y, rows[:, :h], rows[:, h:rotary_dim], rotary_dim, bool(is_neox))
@@ -117,13 +119,16 @@ def insert(k_bf16, positions, slot_mapping, weight_bf16, eps, cos_sin_cache, rot
     """The fused insert: qk-norm, RoPE, bf16, NVFP4 quantise, scatter into
     ``kv_pages [num_blocks, 128, 72]`` (in place).  A negative slot is
     skipped (vLLM's padding convention), and so is a token whose position
-    lies outside the cos/sin table (the kernel flags it).  Returns kv_pages."""
+    lies outside the cos/sin table when rotary_dim > 0 (the kernel flags it;
+    with no rotation the positions are not read).  Returns kv_pages."""
     k_bf16 = np.asarray(k_bf16)
     pos = np.asarray(positions, dtype=np.int64)
     slots = np.asarray(slot_mapping, dtype=np.int64)
-    cache = np.asarray(cos_sin_cache, dtype=F32)
-    keep = (slots >= 0) & (pos >= 0) & (pos < cache.shape[0])
+    keep = slots >= 0
+    if int(rotary_dim) > 0:                 # a position is only read when there is a rotation
+        cache = np.asarray(cos_sin_cache, dtype=F32)
+        keep &= (pos >= 0) & (pos < cache.shape[0])
     if not np.any(keep):
         return kv_pages
-    kb = norm_rope_bf16(k_bf16[keep], pos[keep], weight_bf16, eps, cache, rotary_dim, is_neox)
+    kb = norm_rope_bf16(k_bf16[keep], pos[keep], weight_bf16, eps, cos_sin_cache, rotary_dim, is_neox)
     return nvfp4.insert(kb, slots[keep], kv_pages)
