@@ -22,9 +22,11 @@ conventions):
 Precision.  The pages fix none.  The arithmetic is fp32 in a fixed order,
 and this oracle takes every step in that precision and order, so that the
 bf16 keys, and the quantised codes they decide, can be compared bit for bit:
-  * ss = (s0 + s1) + (s2 + s3), where s_j is the running fp32 sum of x_e^2
-    over e = 32j .. 32j+31 in order.  The square of a bf16 value is exact
-    in fp32 while it stays in range;
+  * per 16-element group g (the quantiser's groups): t_g = e_g + o_g, where
+    e_g and o_g run over the group's even and odd elements in order, each
+    step fl(acc + x^2) with one rounding (a fused multiply-add; the square
+    of a bf16 value is exact anyway unless it leaves fp32's range); then
+    ss = ((t0 + t1) + (t2 + t3)) + ((t4 + t5) + (t6 + t7));
   * v = ss * (1/128) + eps (the product is exact); rs = 1 / sqrt(v), the
     square root and the division each correctly rounded;
   * y = (x * rs) * w, two fp32 roundings;
@@ -57,14 +59,29 @@ def f32_to_bf16(x: np.ndarray) -> np.ndarray:
     return r.astype(np.uint16)
 
 
+def fma_sq(acc: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """fl32(acc + x^2) with a single rounding, for float32 acc and bf16-valued
+    x: x^2 and the sum are exact in float64 whenever the two terms are
+    within 2^29 of each other, and otherwise the smaller one is far below
+    half an fp32 ulp of the larger, so rounding the float64 sum to float32
+    gives the single rounding."""
+    with np.errstate(over="ignore"):
+        return (acc.astype(np.float64) + x.astype(np.float64) ** 2).astype(np.float32)
+
+
 def rms_scale(x: np.ndarray, eps: float) -> np.ndarray:
     """1 / sqrt(mean(x^2) + eps) per row of float32 x [n, 128], in the fixed
-    fp32 order (four running sums of 32 squares, then (s0+s1)+(s2+s3))."""
-    sq = (x * x).reshape(-1, 4, 32)
-    s = np.zeros(sq.shape[:2], dtype=F32)
-    for i in range(32):
-        s = s + sq[:, :, i]
-    ss = (s[:, 0] + s[:, 1]) + (s[:, 2] + s[:, 3])
+    fp32 order: per 16-element group g, running sums e_g (even elements) and
+    o_g (odd elements) of fused squares, t_g = e_g + o_g, then
+    ((t0 + t1) + (t2 + t3)) + ((t4 + t5) + (t6 + t7))."""
+    g = x.reshape(-1, 8, 16)
+    e = np.zeros(g.shape[:2], dtype=F32)
+    o = np.zeros(g.shape[:2], dtype=F32)
+    for i in range(8):
+        e = fma_sq(e, g[:, :, 2 * i])
+        o = fma_sq(o, g[:, :, 2 * i + 1])
+    t = e + o
+    ss = ((t[:, 0] + t[:, 1]) + (t[:, 2] + t[:, 3])) + ((t[:, 4] + t[:, 5]) + (t[:, 6] + t[:, 7]))
     v = ss * F32(1.0 / 128.0) + F32(eps)
     return F32(1.0) / np.sqrt(v)
 
