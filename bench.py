@@ -321,6 +321,35 @@ def gpu_arm(args, w, rank, world, local):
         if i > 0:
             fill_ms.append(a.elapsed_time(b))
 
+    # ---- the fused qk-norm + RoPE insert over the whole cache (each
+    # request's keys at positions 0 .. seq_len - 1, NeoX RoPE over all 128
+    # elements, a seeded synthetic norm weight), into its own pages; outside
+    # the step
+    nr = None
+    if args.norm_rope:
+        seq = np.concatenate([w.dec_seq_lens, w.pre_seq_lens]).astype(np.int64)
+        h_pos = np.concatenate([np.arange(x, dtype=np.int64) for x in seq])
+        max_pos = int(seq.max())
+        inv = 10000.0 ** (-np.arange(64, dtype=np.float64) / 64.0)
+        ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+        table = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32)).to(dev)
+        rng_w = np.random.Generator(np.random.PCG64(7))
+        wts = torch.from_numpy(rng_w.uniform(0.5, 1.5, 128).astype(np.float32)).to(torch.bfloat16).to(dev)
+        pos_d = torch.from_numpy(h_pos).to(dev)
+        rope_pages = torch.zeros_like(st.kv)
+        nr = {"ms": [], "keys": int(h_pos.size), "table_bytes": max_pos * 128 * 4}
+        for i in range(4):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            st.idx.insert_norm_rope(st.k_all, pos_d, st.slot_all, wts, 1e-6, table, 128, True, rope_pages,
+                                    stream=stream)
+            b.record(stream)
+            b.synchronize()
+            if i > 0:
+                nr["ms"].append(a.elapsed_time(b))
+        del rope_pages, table, pos_d
+
     # ---- MXFP4 pages: the same decode / prefill calls over an MXFP4 copy of
     # the cache (filled by mxfp4_insert, timed like the NVFP4 fill), each
     # call timed alone with the L2 flushed before it; not part of the step
@@ -391,7 +420,7 @@ def gpu_arm(args, w, rank, world, local):
         e2e = {"value": work["pages_scored"] * args.steps * world / e2e_s, "unit": "pages/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
     return dict(st=st, work=work, step_ms=step_ms, kern_ms=kern_ms, total_s=total_s, clk=clk.summary(),
-                e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2], mx=mx)
+                e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2], mx=mx, nr=nr)
 
 
 def roofline_block(res, w, wname, peaks, peak_kind):
@@ -422,6 +451,15 @@ def roofline_block(res, w, wname, peaks, peak_kind):
         kernels["insert_fill"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": gb / peaks["hbm_gbs"], "ms": res["fill_ms"], "keys": int(n_all),
                                   "note": "whole-cache insert, timed apart from the step"}
+    nr = res.get("nr")
+    if nr and nr["ms"]:
+        ms = sorted(nr["ms"])[len(nr["ms"]) // 2]
+        gb = (nr["keys"] * (256 + 8 + 8 + 72) + nr["table_bytes"]) / (ms / 1e3) / 1e9
+        kernels["insert_norm_rope_fill"] = {
+            "bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gb / peaks["hbm_gbs"],
+            "ms": ms, "keys": nr["keys"],
+            "note": "whole-cache fused qk-norm + RoPE (NeoX, rotary_dim 128) + NVFP4 insert; bytes: "
+                    "key, slot, position and row per token plus the cos/sin table once"}
     mx = res.get("mx")
     if mx:
         med = lambda v: sorted(v)[len(v) // 2]
@@ -538,6 +576,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-mxfp4", dest="mxfp4", action="store_false",
                     help="skip the MXFP4-page timings (kernels decode_mxfp4 / prefill_mxfp4 / insert_fill_mxfp4)")
+    ap.add_argument("--no-norm-rope", dest="norm_rope", action="store_false",
+                    help="skip the timed whole-cache fused qk-norm + RoPE insert")
     ap.add_argument("--sweep", action="store_true", help="one line per named workload (no e2e / cpu)")
     ap.add_argument("--no-flush", dest="flush", action="store_false",
                     help="skip the L2 flush (profiling runs only; the timed numbers then see a warm L2)")

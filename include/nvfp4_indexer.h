@@ -65,7 +65,9 @@ enum {
   IDX_STATUS_BAD_PAGE = 1,     /* a page id outside the cache; rows set to -1  */
   IDX_STATUS_BAD_TABLE = 2,    /* history wider than pt_stride; rows set to -1 */
   IDX_STATUS_TIMEOUT = 4,      /* a bounded wait gave up; outputs undefined    */
-  IDX_STATUS_BAD_SLOT = 8      /* nvfp4_insert skipped a slot past the cache    */
+  IDX_STATUS_BAD_SLOT = 8,     /* an insert skipped a slot past the cache       */
+  IDX_STATUS_BAD_POSITION = 16 /* nvfp4_insert_norm_rope skipped a token whose
+                                  position lies outside the cos/sin table       */
 };
 
 /* Page formats (indexer_decode_partial). */
@@ -164,6 +166,39 @@ int indexer_prefill(indexer_plan_t plan, const uint8_t* q, const int32_t* cu_seq
  */
 int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uint8_t* kv_pages,
                  int num_blocks, int32_t* status, cudaStream_t stream);
+
+/*
+ * nvfp4_insert_norm_rope -- the fused insert that writes the index-K cache
+ * (page vllm.models.minimax_m3.nvidia.indexer_nvfp4, module description:
+ * "the fused qk-norm/rope insert"; the pages give no more, so this follows
+ * vLLM's RMSNorm and rotary-embedding conventions).  Per token:
+ *   y = x / sqrt(mean(x^2) + eps) * norm_weight            (RMSNorm, fp32)
+ *   rotary pairs (y1, y2) -> (y1 cos - y2 sin, y2 cos + y1 sin), angles from
+ *   row `position` of cos_sin_cache; elements past rotary_dim pass through;
+ *   the result rounded to bf16, then quantised and written as nvfp4_insert.
+ * fp32 order: four running sums of 32 squares (elements 32j..32j+31),
+ * combined as (s0 + s1) + (s2 + s3); v = ss / 128 + eps; rs = 1 / sqrt(v),
+ * square root and division correctly rounded; y = (x * rs) * w; every
+ * rotation product and sum rounded separately (no fused multiply-add).
+ *   k_bf16         [n][128] bf16 bit patterns, 16-byte aligned
+ *   positions      int64 [n] (unused, may be NULL, when rotary_dim == 0)
+ *   slot_mapping   int64 [n]: page * 128 + row; negative = skip
+ *   norm_weight    bf16 [128], 16-byte aligned
+ *   eps            finite, >= 0 (an all-zero key needs eps > 0)
+ *   cos_sin_cache  fp32 [max_pos][rotary_dim]: rotary_dim/2 cosines, then
+ *                  rotary_dim/2 sines (16-byte aligned for NeoX or when
+ *                  rotary_dim % 8 == 0, else 4)
+ *   rotary_dim     even, 0..128; 0 = norm only
+ *   is_neox        non-zero: pairs (i, i + rotary_dim/2), rotary_dim 64 or
+ *                  128 (others IDX_EUNSUPPORTED); zero: pairs (2i, 2i+1)
+ *   kv_pages       [num_blocks][128][72]
+ *   status         NULL, or a device int32 that gets IDX_STATUS_BAD_SLOT or
+ *                  IDX_STATUS_BAD_POSITION OR-ed in for a skipped token
+ */
+int nvfp4_insert_norm_rope(const uint16_t* k_bf16, const int64_t* positions, const int64_t* slot_mapping,
+                           int n, const uint16_t* norm_weight, float eps, const float* cos_sin_cache,
+                           int max_pos, int rotary_dim, int is_neox, uint8_t* kv_pages, int num_blocks,
+                           int32_t* status, cudaStream_t stream);
 
 /*
  * MXFP4 index-K pages (page vllm.models.minimax_m3.amd.indexer_mxfp4: its

@@ -17,8 +17,9 @@ import os
 import re
 from typing import Optional
 
-__all__ = ["Plan", "insert", "decode_noalloc", "IndexerError", "load_library", "library_path", "declared_symbols",
-           "STATUS_BAD_PAGE", "STATUS_BAD_TABLE", "STATUS_TIMEOUT", "STATUS_BAD_SLOT", "TOPK", "PAGE"]
+__all__ = ["Plan", "insert", "insert_norm_rope", "decode_noalloc", "IndexerError", "load_library", "library_path", "declared_symbols",
+           "STATUS_BAD_PAGE", "STATUS_BAD_TABLE", "STATUS_TIMEOUT", "STATUS_BAD_SLOT", "STATUS_BAD_POSITION",
+           "TOPK", "PAGE"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
@@ -27,7 +28,7 @@ _HEADER = os.path.join(_ROOT, "include", "nvfp4_indexer.h")
 
 PAGE = 128
 TOPK = 16
-STATUS_BAD_PAGE, STATUS_BAD_TABLE, STATUS_TIMEOUT, STATUS_BAD_SLOT = 1, 2, 4, 8
+STATUS_BAD_PAGE, STATUS_BAD_TABLE, STATUS_TIMEOUT, STATUS_BAD_SLOT, STATUS_BAD_POSITION = 1, 2, 4, 8, 16
 IDX_OK, IDX_EINVAL, IDX_EUNSUPPORTED, IDX_ECUDA, IDX_ENOSPACE, IDX_EDEVICE = 0, -1, -2, -3, -4, -5
 IDX_PAGES_NVFP4, IDX_PAGES_MXFP4 = 0, 1
 
@@ -68,6 +69,7 @@ def load_library():
     lib.indexer_decode_mxfp4.argtypes = lib.indexer_decode.argtypes
     lib.indexer_prefill_mxfp4.argtypes = lib.indexer_prefill.argtypes
     lib.mxfp4_insert.argtypes = lib.nvfp4_insert.argtypes
+    lib.nvfp4_insert_norm_rope.argtypes = [P, P, P, I, P, ctypes.c_float, P, I, I, I, P, I, P, P]
     lib.indexer_decode_partial.argtypes = [P, I, P, P, I, P, I, P, P, P, I, I, P, P]
     lib.indexer_merge_candidates.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.indexer_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
@@ -75,7 +77,7 @@ def load_library():
     lib.indexer_version.restype = ctypes.c_char_p
     for name in ("indexer_plan", "indexer_plan_destroy", "indexer_decode", "indexer_prefill",
                  "nvfp4_insert", "indexer_get_status", "indexer_decode_mxfp4", "indexer_prefill_mxfp4",
-                 "mxfp4_insert", "indexer_decode_partial", "indexer_merge_candidates"):
+                 "mxfp4_insert", "indexer_decode_partial", "indexer_merge_candidates", "nvfp4_insert_norm_rope"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -245,6 +247,36 @@ def mxfp4_insert(k_bf16, slot_mapping, pages, status=None, stream=None):
     """Quantise bf16 keys [n, 128] to MXFP4 and write them at ``slot_mapping``
     (``mxfp4_insert``; pages [num_blocks, 8704])."""
     return _insert("mxfp4_insert", 2, k_bf16, slot_mapping, pages, status, stream)
+
+
+def insert_norm_rope(k_bf16, positions, slot_mapping, norm_weight, eps, cos_sin_cache, rotary_dim: int,
+                     is_neox: bool, kv_pages, status=None, stream=None):
+    """qk-norm (RMSNorm with ``norm_weight`` bf16 [128] and ``eps``), RoPE
+    from ``cos_sin_cache`` float32 [max_pos, rotary_dim] at ``positions``
+    int64 [n], bf16 rounding, then the NVFP4 insert of keys [n, 128] into
+    ``kv_pages`` [num_blocks, 128, 72] (``nvfp4_insert_norm_rope``)."""
+    import torch
+    if k_bf16.dim() != 2 or k_bf16.shape[1] != 128:
+        raise ValueError("k_bf16: expected [n, 128]")
+    kb = k_bf16.view(torch.int16) if k_bf16.dtype == torch.bfloat16 else k_bf16
+    wb = norm_weight.view(torch.int16) if norm_weight.dtype == torch.bfloat16 else norm_weight
+    n = int(kb.shape[0])
+    if slot_mapping.shape[0] != n or (positions is not None and positions.shape[0] != n):
+        raise ValueError("slot_mapping and positions must have one entry per key")
+    if wb.numel() != 128:
+        raise ValueError("norm_weight: expected 128 elements")
+    max_pos = 0
+    if cos_sin_cache is not None:
+        if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rotary_dim:
+            raise ValueError(f"cos_sin_cache: expected [max_pos, {rotary_dim}]")
+        max_pos = int(cos_sin_cache.shape[0])
+    _check(load_library().nvfp4_insert_norm_rope(
+        _ptr(kb, torch.int16, "k_bf16"), _ptr(positions, torch.int64, "positions", 1),
+        _ptr(slot_mapping, torch.int64, "slot_mapping", 1), n, _ptr(wb, torch.int16, "norm_weight"),
+        float(eps), _ptr(cos_sin_cache, torch.float32, "cos_sin_cache"), max_pos, int(rotary_dim),
+        1 if is_neox else 0, _ptr(kv_pages, torch.uint8, "kv_pages", 3), int(kv_pages.shape[0]),
+        _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
+    return kv_pages
 
 
 def _insert(fn, pages_ndim, k_bf16, slot_mapping, kv_pages, status, stream):

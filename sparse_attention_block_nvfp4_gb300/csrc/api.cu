@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/nvfp4_indexer.h): argument checks, the plan
 // object and its device scratch, launches on the caller's stream.
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -329,6 +330,50 @@ int mxfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uin
                  int num_blocks, int32_t* status, cudaStream_t stream) {
   return insert_impl("mxfp4_insert", kPagesMxfp4, k_bf16, slot_mapping, n, pages, num_blocks, status,
                      stream);
+}
+
+int nvfp4_insert_norm_rope(const uint16_t* k_bf16, const int64_t* positions, const int64_t* slot_mapping,
+                           int n, const uint16_t* norm_weight, float eps, const float* cos_sin_cache,
+                           int max_pos, int rotary_dim, int is_neox, uint8_t* kv_pages, int num_blocks,
+                           int32_t* status, cudaStream_t stream) {
+  g_last_error.clear();
+  const char* fn = "nvfp4_insert_norm_rope";
+  if (n < 0) return set_err(IDX_EINVAL, "%s: n=%d", fn, n);
+  if (rotary_dim < 0 || rotary_dim > 128 || (rotary_dim & 1))
+    return set_err(IDX_EINVAL, "%s: rotary_dim=%d (even, 0..128)", fn, rotary_dim);
+  if (rotary_dim && is_neox && rotary_dim != 64 && rotary_dim != 128)
+    return set_err(IDX_EUNSUPPORTED, "%s: NeoX rotary_dim=%d (64 or 128)", fn, rotary_dim);
+  if (!(eps >= 0.0f) || !(eps < INFINITY)) return set_err(IDX_EINVAL, "%s: eps must be finite and >= 0", fn);
+  if (n == 0) return IDX_OK;
+  if (!k_bf16 || !slot_mapping || !norm_weight || !kv_pages)
+    return set_err(IDX_EINVAL, "%s: NULL array argument", fn);
+  if (rotary_dim && (!positions || !cos_sin_cache || max_pos < 1))
+    return set_err(IDX_EINVAL, "%s: rotary_dim > 0 needs positions, cos_sin_cache and max_pos >= 1", fn);
+  if (!aligned16(k_bf16) || !aligned16(norm_weight) || !aligned16(kv_pages) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(positions) & 7u))
+    return set_err(IDX_EINVAL, "%s: k_bf16, norm_weight and kv_pages must be 16-byte aligned, "
+                               "slot_mapping and positions 8", fn);
+  const uintptr_t cs_align = (is_neox || rotary_dim % 8 == 0) ? 16u : 4u;   // vector loads of the rows
+  if (rotary_dim && (reinterpret_cast<uintptr_t>(cos_sin_cache) & (cs_align - 1)))
+    return set_err(IDX_EINVAL, "%s: cos_sin_cache must be %d-byte aligned", fn, (int)cs_align);
+  if (num_blocks < 1) return set_err(IDX_EINVAL, "%s: num_blocks=%d", fn, num_blocks);
+  NormRopeArgs a;
+  a.k = k_bf16;
+  a.positions = positions;
+  a.slots = slot_mapping;
+  a.n = n;
+  a.weight = norm_weight;
+  a.eps = eps;
+  a.cos_sin = cos_sin_cache;
+  a.max_pos = max_pos;
+  a.rotary_dim = rotary_dim;
+  a.is_neox = is_neox ? 1 : 0;
+  a.pages = kv_pages;
+  a.num_slots = (int64_t)num_blocks * 128;
+  a.status = status;
+  cudaError_t e = launch_insert_norm_rope(a, stream);
+  if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
+  return IDX_OK;
 }
 
 int indexer_get_status(indexer_plan_t plan, cudaStream_t stream, int32_t* bits) {

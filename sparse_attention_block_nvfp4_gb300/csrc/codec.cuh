@@ -260,4 +260,23 @@ __device__ __forceinline__ uint32_t e4m3_scale_of_amax(float amax) {
   return f32_to_e4m3_satfinite(hi);
 }
 
+// One 16-element NVFP4 group of bf16-exact fp32 values xg (overwritten) with
+// its amax: returns the E4M3 scale byte and leaves the 16 codes in c0, c1
+// (element 0 in the low nibble of c0).  A zero scale gives sign-only codes.
+__device__ __forceinline__ uint32_t nvfp4_encode16(float* xg, float amax, uint32_t& c0, uint32_t& c1) {
+  const uint32_t sb = e4m3_scale_of_amax(amax);
+  const float s = e4m3_to_f32(sb);
+  if (s > 0.0f) {
+    const float r = rcp_approx(s);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xg[i] = nvfp4_ratio(xg[i], r);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xg[i] = __uint_as_float(__float_as_uint(xg[i]) & 0x80000000u);
+  }
+  c0 = f32x8_to_e2m1x8(xg);
+  c1 = f32x8_to_e2m1x8(xg + 8);
+  return sb;
+}
+
 }  // namespace nvfp4idx

@@ -24,6 +24,7 @@ constexpr int32_t kStatusBadPage = 1;
 constexpr int32_t kStatusBadTable = 2;
 constexpr int32_t kStatusTimeout = 4;
 constexpr int32_t kStatusBadSlot = 8;
+constexpr int32_t kStatusBadPosition = 16;
 
 struct DecodeParams {
   const uint8_t* q;            // [num_reqs * qlen][H][128] e4m3
@@ -88,6 +89,24 @@ cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_
                           int num_blocks, int32_t* status, cudaStream_t stream);
 cudaError_t launch_insert_mxfp4(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
                                 int num_blocks, int32_t* status, cudaStream_t stream);
+// Arguments of the fused qk-norm + RoPE + NVFP4 insert (all device pointers;
+// positions and cos_sin unused when rotary_dim == 0).
+struct NormRopeArgs {
+  const uint16_t* k;          // bf16 [n][128]
+  const int64_t* positions;   // [n]
+  const int64_t* slots;       // [n], negative = skip
+  int n;
+  const uint16_t* weight;     // bf16 [128]
+  float eps;
+  const float* cos_sin;       // [max_pos][rotary_dim]: cosines, then sines
+  int64_t max_pos;
+  int rotary_dim;
+  int is_neox;
+  uint8_t* pages;             // [num_blocks][128][72]
+  int64_t num_slots;          // num_blocks * 128
+  int32_t* status;
+};
+cudaError_t launch_insert_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
 // Merge the candidate lists of `world` context-parallel ranks ([world][rows][15],
 // rank-major) into final rows [rows][16].

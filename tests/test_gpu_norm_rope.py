@@ -1,0 +1,132 @@
+"""Fused qk-norm + RoPE + NVFP4 insert (nvfp4_insert_norm_rope) against the
+oracle (oracle/norm_rope.py + oracle/nvfp4.py): page bytes bit-exact."""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import norm_rope as onr
+from oracle import nvfp4 as onv
+from gpu_util import torch_dev, up
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def rope_table(max_pos, rotary_dim, base=10000.0):
+    """cos / sin table [max_pos, rotary_dim] of the standard RoPE frequencies
+    base^(-2i / rotary_dim), cosines first (an input of the insert)."""
+    h = rotary_dim // 2
+    inv = base ** (-np.arange(h, dtype=np.float64) * 2.0 / rotary_dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def case(n, seed, max_pos=4096):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((n, 128)).astype(np.float32)
+    x *= np.exp2(rng.integers(-6, 7, size=(n, 1))).astype(np.float32)     # spread of key norms
+    x[:, rng.integers(0, 128, 4)] *= 8.0                                   # outlier channels
+    k = workloads._to_bf16_bits(x)
+    w = workloads._to_bf16_bits(rng.uniform(0.25, 2.0, 128).astype(np.float32))
+    pos = rng.integers(0, max_pos, n).astype(np.int64)
+    return k, w, pos
+
+
+def run_gpu(k, pos, slots, w, eps, table, rd, neox, nb, fill=0):
+    import torch
+    import sparse_attention_block_nvfp4_gb300 as idx
+    kv = torch.full((nb, 128, 72), fill, dtype=torch.uint8, device=torch_dev())
+    status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+    idx.insert_norm_rope(up(k.view(np.int16)), up(pos), up(slots), up(w.view(np.int16)), eps,
+                         up(table) if table is not None else None, rd, neox, kv, status=status)
+    return kv.cpu().numpy(), int(status.item())
+
+
+@pytest.mark.parametrize("rd,neox", [(128, True), (64, True), (128, False), (64, False), (40, False),
+                                     (32, False), (6, False), (2, False), (0, True)])
+def test_norm_rope_insert_bit_exact(rd, neox):
+    n = 20000
+    k, w, pos = case(n, 40 + rd + neox)
+    nb = (n + 127) // 128 + 3
+    rng = np.random.Generator(np.random.PCG64(41))
+    slots = rng.permutation(nb * 128)[:n].astype(np.int64)
+    slots[::11] = -1
+    table = rope_table(4096, rd) if rd else None
+    got, st = run_gpu(k, pos, slots, w, 1e-6, table, rd, neox, nb, fill=0x5A)
+    want = np.full((nb, 128, 72), 0x5A, np.uint8)
+    onr.insert(k, pos, slots, w, 1e-6, table, rd, neox, want)
+    assert st == 0
+    assert np.array_equal(got, want), f"{np.count_nonzero(got != want)} bytes differ"
+
+
+def test_norm_rope_insert_eps_and_extremes():
+    """Large eps against small keys, zero keys, keys near bf16's range edges,
+    a weight with zeros and negatives: still bit-exact."""
+    rng = np.random.Generator(np.random.PCG64(42))
+    n = 512
+    x = rng.standard_normal((n, 128)).astype(np.float32)
+    x[:64] *= 1e-3
+    x[64:128] = 0.0
+    x[128:192] *= np.float32(2.0 ** 60)
+    x[192:256] *= np.float32(2.0 ** -60)
+    k = workloads._to_bf16_bits(x)
+    wv = rng.uniform(-2.0, 2.0, 128).astype(np.float32)
+    wv[::9] = 0.0
+    w = workloads._to_bf16_bits(wv)
+    pos = rng.integers(0, 300, n).astype(np.int64)
+    table = rope_table(300, 128)
+    slots = np.arange(n, dtype=np.int64)
+    for eps in (1e-6, 0.5):
+        got, st = run_gpu(k, pos, slots, w, eps, table, 128, True, 4)
+        want = onr.insert(k, pos, slots, w, eps, table, 128, True, np.zeros((4, 128, 72), np.uint8))
+        assert st == 0
+        assert np.array_equal(got, want), f"eps {eps}: {np.count_nonzero(got != want)} bytes differ"
+
+
+def test_norm_rope_insert_bad_positions_and_slots():
+    import torch
+    import sparse_attention_block_nvfp4_gb300 as idx
+    k, w, pos = case(8, 43, max_pos=64)
+    pos[2] = 64                                   # past the table
+    pos[5] = -3
+    slots = np.arange(8, dtype=np.int64)
+    slots[6] = 10 * 128                           # past the cache
+    table = rope_table(64, 128)
+    got, st = run_gpu(k, pos, slots, w, 1e-6, table, 128, True, 1, fill=0x77)
+    assert st == idx.STATUS_BAD_POSITION | idx.STATUS_BAD_SLOT
+    ok = np.array([0, 1, 3, 4, 7])
+    want = np.full((1, 128, 72), 0x77, np.uint8)
+    onr.insert(k[ok], pos[ok], slots[ok], w, 1e-6, table, 128, True, want)
+    assert np.array_equal(got, want)
+    with pytest.raises(idx.IndexerError) as e:
+        run_gpu(k, pos, slots, w, 1e-6, rope_table(64, 96), 96, True, 1)
+    assert e.value.code == idx.IDX_EUNSUPPORTED
+    with pytest.raises(idx.IndexerError):
+        run_gpu(k, pos, slots, w, -1.0, table, 128, True, 1)
+
+
+def test_norm_rope_insert_full_cache_sampled():
+    """The long mixed workload's whole cache (2.24 M keys, each request's
+    tokens at positions 0 .. seq_len - 1), in the launch configuration the
+    benchmark times; 16384 sampled rows checked against the oracle."""
+    w_ = workloads.config(4)
+    seq = np.concatenate([w_.dec_seq_lens, w_.pre_seq_lens]).astype(np.int64)
+    pos = np.concatenate([np.arange(s) for s in seq])
+    assert pos.size == w_.k_bf16.shape[0]
+    rng = np.random.Generator(np.random.PCG64(44))
+    wts = workloads._to_bf16_bits(rng.uniform(0.5, 1.5, 128).astype(np.float32))
+    table = rope_table(int(seq.max()), 128)
+    got, st = run_gpu(w_.k_bf16, pos, w_.slot_mapping, wts, 1e-6, table, 128, True, w_.num_blocks)
+    assert st == 0
+    pick = rng.choice(pos.size, size=16384, replace=False)
+    rows = np.empty((pick.size, 72), np.uint8)
+    for a in range(0, pick.size, 4096):
+        p = pick[a:a + 4096]
+        kb = onr.norm_rope_bf16(w_.k_bf16[p], pos[p], wts, 1e-6, table, 128, True)
+        rows[a:a + 4096] = onv.quantize_rows(kb)
+    assert np.array_equal(got.reshape(-1, 72)[w_.slot_mapping[pick]], rows)
