@@ -16,28 +16,30 @@
 // scores of 32 tokens of ITS page; after the 4 slices that warp has seen all
 // 128 tokens of the page and takes the max over them alone: an in-register
 // max over the slices, then a reduction over its 32 lanes, with no exchange
-// between warps.  One CTA per SM, 16 warps, one role per warpgroup (so that
+// between warps.  One CTA per SM, 16 or 20 warps, one role per warpgroup (so that
 // setmaxnreg can move registers to the epilogue), linked by mbarrier rings
 // (slice s of every quad uses A buffer s and D buffer s):
-//   * warpgroup 0 (88 registers): warp 0 reads page ids 32 at a time and has
+//   * warpgroup 0 (88 / 80 registers): warp 0 reads page ids 32 at a time and has
 //     the TMA unit copy each 9216-byte page into a 16-stage shared ring
 //     (cp.async.bulk, transaction-count completion); warps 1 / 2 (slices of
 //     even / odd index) each have one thread issue the 8 tcgen05.mma (K = 16)
 //     of a slice into D buffer s and commit once (a single thread cannot
 //     issue small-N MMAs as fast as the tensor core retires them); warp 3
 //     idles;
-//   * warpgroups 1 / 2 (dequant, 112 registers, quads of even / odd index): warp q reads the
+//   * warpgroups 1 / 2 (dequant, 112 / 96 registers, quads of even / odd index): warp q reads the
 //     72-byte rows of tokens 32s + lane of page q, dequantises them exactly to
 //     fp16 (E2M1 x E4M3 fits fp16) and stores them into its lane quarter of A
 //     buffer s (tcgen05.st), the MMA's A operand (M = 128 lanes, K = 128); at
 //     each segment start both widen the request's E4M3 queries to fp16 into a
 //     128B-swizzled B tile (double buffered);
-//   * warpgroup 3 (epilogue, 200 registers): warp q keeps the running max of
-//     its page's tokens over the 4 slices, reduces it over its lanes
+//   * warpgroup 3, and 4 when a request has 64 rows (epilogue, 200 / 104
+//     registers): warp q owns page q (with two warpgroups warps q and q + 4
+//     split its rows in two halves); it keeps the running max of the page's
+//     tokens over the 4 slices for its rows, reduces it over its lanes
 //     (butterfly shuffles that leave column k in lane k), and lane k inserts
-//     the page score of rows k and k + 32 into their running top-15 in
-//     registers; at a segment end the four warps' lists of each row are
-//     merged.
+//     the page score of its row into the row's running top-15 in registers;
+//     at a segment end the four warps' lists of each row are merged.
+//   The register figures are for 16 / 20 warps.
 // A request covered by one CTA is finalised in place; otherwise each segment
 // leaves its 15 candidates per row in scratch and decode_merge_kernel merges
 // them (and writes the rows of requests with no history page).
@@ -55,12 +57,27 @@ constexpr int kQuadSlots = 4;            // raw page ring: quad kq fills stages 
 constexpr int kDecStages = 4 * kQuadSlots;
 constexpr int kDecSlices = 4;            // slice s: A buffer s (columns [64s, 64s+64))
 // One role per warpgroup, so that setmaxnreg can move registers between
-// them: warpgroup 0 (88 registers) = warp 0 TMA, warps 1 / 2 MMA issue,
-// warp 3 idle; warpgroups 1 / 2 dequant (112); warpgroup 3 epilogue (200).
-// 4 x 88 + 8 x 112 + 4 x 200 registers x 32 lanes = 65536 = 512 x 128.
-constexpr int kDecThreads = 512;
-constexpr int kDqTid0 = 128, kEpTid0 = 384;
-constexpr uint32_t kDecRegsCtl = 88, kDecRegsDq = 112, kDecRegsEpi = 200;
+// them: warpgroup 0 = warp 0 TMA, warps 1 / 2 MMA issue, warp 3 idle;
+// warpgroups 1 / 2 dequant; then one epilogue warpgroup, or two when a
+// request has 64 rows (each then takes half of every page's rows).
+constexpr int kDqTid0 = 128, kEpTid0 = 384, kEpWarp0 = 12;
+constexpr int kDecMaxThreads = 640;
+template <int NQ>
+struct DecRoles {
+  static constexpr int kEpGroups = NQ == 64 ? 2 : 1;
+  static constexpr int kThreads = 384 + 128 * kEpGroups;
+  static constexpr int kEpThreads = 128 * kEpGroups;
+  // 512 threads launch with 128 registers each, 640 with 96; the role
+  // shares add up to at most the launch allocation:
+  // 128 x 88 + 256 x 112 + 128 x 200 = 65536 = 512 x 128 and
+  // 128 x 80 + 256 x 96 + 256 x 104 = 61440 = 640 x 96.
+  static constexpr uint32_t kRegsLaunch = kEpGroups == 2 ? 96 : 128;
+  static constexpr uint32_t kRegsCtl = kEpGroups == 2 ? 80 : 88;
+  static constexpr uint32_t kRegsDq = kEpGroups == 2 ? 96 : 112;
+  static constexpr uint32_t kRegsEpi = kEpGroups == 2 ? 104 : 200;
+  static_assert(128 * kRegsCtl + 256 * kRegsDq + kEpThreads * kRegsEpi <= kThreads * kRegsLaunch,
+                "setmaxnreg shares exceed the launch allocation");
+};
 constexpr uint32_t kDecTmemCols = 512;
 
 // D buffers in tensor memory from column 256: for NQ <= 32 two sets of four
@@ -134,8 +151,9 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
 // at step H each lane keeps half of its columns, sends the other half to
 // lane ^ H and takes the max with what it receives (H shuffles).  For N = 32
 // columns, lane l ends with column l (31 shuffles in all, against 32
-// warp-wide reductions column by column); for N = 16, lanes l and l ^ 16 end
-// with column l & 15.  v is overwritten.
+// warp-wide reductions column by column); for N = 16 (8), two (four) lanes
+// finish each column with one (two) more shuffles, and lane l ends with
+// column l & 15 (l & 7).  v is overwritten.
 template <int H>
 __device__ __forceinline__ void colmax_step(float* v, int lane) {
   const bool up = (lane & H) != 0;
@@ -148,14 +166,15 @@ __device__ __forceinline__ void colmax_step(float* v, int lane) {
 }
 template <int N>
 __device__ __forceinline__ float warp_colmax(float* v, int lane) {
-  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
   if constexpr (N == 32) colmax_step<16>(v, lane);
-  colmax_step<8>(v, lane);
+  if constexpr (N >= 16) colmax_step<8>(v, lane);
   colmax_step<4>(v, lane);
   colmax_step<2>(v, lane);
   colmax_step<1>(v, lane);
   float m = v[0];
-  if constexpr (N == 16) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  if constexpr (N == 8) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  if constexpr (N <= 16) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
   return m;
 }
 
@@ -209,8 +228,10 @@ struct SegWalk {
 };
 
 template <int NQ, class PF>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel(const DecodeParams p) {
   using Lay = DecLayout<NQ, PF>;
+  using Roles = DecRoles<NQ>;
+  constexpr int kDecThreads = Roles::kThreads;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kDecStages], raw_empty[kDecStages];
   __shared__ __align__(8) uint64_t a_full[kDecSlices];
@@ -223,7 +244,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
-  __shared__ int warp_sum[kDecThreads / 32];
+  __shared__ int warp_sum[kDecMaxThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_launch_dependents();                       // the merge kernel may be scheduled
@@ -297,8 +318,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       mbar_init(smem_u32(&a_full[b]), 128);     // the quad's dequant warpgroup
       mbar_init(smem_u32(&d_full[0][b]), 1);    // MMA commit
       mbar_init(smem_u32(&d_full[1][b]), 1);
-      mbar_init(smem_u32(&d_empty[0][b]), 128); // epilogue warpgroup
-      mbar_init(smem_u32(&d_empty[1][b]), 128);
+      mbar_init(smem_u32(&d_empty[0][b]), Roles::kEpThreads); // the epilogue warpgroup(s)
+      mbar_init(smem_u32(&d_empty[1][b]), Roles::kEpThreads);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&q_full[k]), 256);   // both dequant groups write the tile
@@ -334,7 +355,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
   if (warp < 4) {
     // warpgroup 0 gives registers back to the epilogue (executed by all
     // four warps of the warpgroup, warp 3 has no other role)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsCtl));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Roles::kRegsCtl));
     if (warp == 0) {
       // ================================================= producer (TMA)
       // Quad kq fills stages 4 * (kq % 4) + q, q < 4; a page missing from a
@@ -452,7 +473,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
     }
   } else if (warp < 12) {
     // ================================================= dequant warpgroups
-    if constexpr (kDecRegsDq < 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsDq));
+    if constexpr (Roles::kRegsDq < Roles::kRegsLaunch)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Roles::kRegsDq));
     // Group grp takes the quads of parity grp; warp q (tensor-memory lanes
     // [32q, 32q+32)) dequantises page q of the quad, one 32-token slice at a
     // time, into its lane quarter of A buffer s.  A warp of a partial quad
@@ -535,48 +557,51 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
       if (ok && walk.more()) walk.next_request(p);
     }
   } else {
-    // ================================================= epilogue warpgroup
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDecRegsEpi));
-    // Warp q owns page q of every quad: per slice it loads its lanes' NQ
-    // columns of D buffer s and keeps the running max over slices; after the
-    // 4th slice a butterfly transpose-reduction over the lanes gives the page
-    // score of every row (lane l gets rows l and l + 32).  Each lane keeps
-    // the running top-15 of its row(s) in registers (this warpgroup runs
-    // with 200); at a segment end the lists go through shared memory and
+    // ================================================= epilogue warpgroup(s)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Roles::kRegsEpi));
+    // Warp q of an epilogue warpgroup owns page q of every quad (tensor-
+    // memory lanes [32q, 32q+32)); with two warpgroups, warps q and q + 4
+    // split its NQ rows and half hf takes rows [hf * NH, (hf + 1) * NH).  Per
+    // slice a warp loads its lanes' NH columns of D buffer s and keeps the
+    // running max over slices; after the 4th slice a butterfly transpose-
+    // reduction over the lanes gives the page score of each of its rows (row
+    // hf * NH + k in lane k).  That lane keeps the running top-15 of its row
+    // in registers; at a segment end the lists go through shared memory and
     // the four warps' lists of each row are merged.  The walk is never left
     // early, so every barrier is always reached.
+    constexpr int NH = NQ / Roles::kEpGroups;         // rows per warp (<= 32)
     const int q = warp & 3;
-    const int ep = tid - kEpTid0;                     // 0..127: row owner at the merge
+    const int hf = (warp - kEpWarp0) >> 2;
+    const int ep = tid - kEpTid0;                     // row owner at the merge
+    const int myrow = hf * NH + (lane & (NH - 1));    // lanes < NH hold a distinct row
+    const bool row_lane = lane < NH;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float2* const lists = reinterpret_cast<float2*>(base + Lay::kListOff);   // [4][64][15]
-    float2* const my0 = lists + (q * kMaxRows + lane) * kHistK;              // row lane
-    float2* const my1 = my0 + 32 * kHistK;                                   // row lane + 32
-    constexpr int CW = NQ == 32 ? 32 : 16;            // columns per load + max pass
+    float2* const my = lists + (q * kMaxRows + myrow) * kHistK;
+    constexpr int CW = Roles::kEpGroups == 2 ? 16 : NH;   // columns per load + max pass
     int64_t kq = 0;
     bool ok = true;                                   // uniform within the warp
     while (walk.more()) {
       const int je = walk.seg_end(p);
       const int r = walk.r;
       const int seq_r = __ldg(p.seq_lens + r);
-      const int pos0 = seq_r - p.qlen + lane / p.H, pos1 = seq_r - p.qlen + (lane + 32) / p.H;
-      const int L0 = pos0 >= 0 ? (pos0 >> 7) : -1, L1 = pos1 >= 0 ? (pos1 >> 7) : -1;
+      const int pos = seq_r - p.qlen + myrow / p.H;
+      const int L = pos >= 0 ? (pos >> 7) : -1;
       // an unreadable page id anywhere in the segment: checked once, up front
       int seg_bad = 0;
-      for (int jj = walk.j + ep; jj < je; jj += 128) {
+      for (int jj = walk.j + ep; jj < je; jj += Roles::kEpThreads) {
         const int ph = __ldg(p.page_table + (int64_t)r * p.pt_stride + jj);
         seg_bad |= (ph < 0 || ph >= p.num_blocks);
       }
-      // rows lane (and lane + 32 when NQ = 64)
-      TopK15 top0, top1;
-      top0.reset();
-      if constexpr (NQ > 32) top1.reset();
+      TopK15 top;
+      top.reset();
       for (; walk.j < je; ++kq) {
         const int npq = min(4, je - walk.j);
         const int jp = walk.j + q;                    // this warp's page
         const bool has = q < npq;
         walk.j += npq;
         walk.g += npq;
-        float run[NQ];
+        float run[NH];
 #pragma unroll
         for (int sl = 0; sl < kDecSlices; ++sl) {
           if (ok) {
@@ -587,13 +612,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           if (ok) {
             tc_fence_after();
             if (has) {
-              const uint32_t ta = tbase + lane_base + DecD<NQ>::col(kq, sl);
+              const uint32_t ta = tbase + lane_base + DecD<NQ>::col(kq, sl) + (uint32_t)(hf * NH);
               if (sl == 0) {
-                tmem_ld_row<NQ>(ta, run);
+                tmem_ld_row<NH>(ta, run);
                 tmem_wait_ld();
               } else {
 #pragma unroll
-                for (int ch = 0; ch < NQ / CW; ++ch) {
+                for (int ch = 0; ch < NH / CW; ++ch) {
                   float t[CW];
                   tmem_ld_row<CW>(ta + ch * CW, t);
                   tmem_wait_ld();
@@ -607,29 +632,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
           }
         }
         if (ok && has) {
-          // rows lane and lane + 32: max over the warp's 32 token lanes
-          float m0 = warp_colmax<NQ < 32 ? NQ : 32>(run, lane), m1 = 0.0f;
-          if constexpr (NQ > 32) m1 = warp_colmax<32>(run + 32, lane);
-          m0 = canon_zero(m0);
-          m1 = canon_zero(m1);
-          if (lane < R && jp < L0) {
-            top0.insert(m0, jp);
-            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane) * p.dbg_stride + jp] = m0;
-          }
-          if (NQ > 32 && lane + 32 < R && jp < L1) {
-            top1.insert(m1, jp);
-            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane + 32) * p.dbg_stride + jp] = m1;
+          // the warp's rows: max over its 32 token lanes
+          const float m = canon_zero(warp_colmax<NH>(run, lane));
+          if (row_lane && myrow < R && jp < L) {
+            top.insert(m, jp);
+            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + myrow) * p.dbg_stride + jp] = m;
           }
         }
       }
       // ---- merge the four warps' lists of each row, finalise the segment
+      if (row_lane) {
 #pragma unroll
-      for (int k = 0; k < kHistK; ++k) {
-        my0[k] = make_float2(top0.s[k], __int_as_float(top0.id[k]));
-        if constexpr (NQ > 32) my1[k] = make_float2(top1.s[k], __int_as_float(top1.id[k]));
+        for (int k = 0; k < kHistK; ++k) my[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
       }
-      const int bad = named_bar_red_or(2, 128, seg_bad);
-      const int failed = named_bar_red_or(3, 128, (!ok || abort_s) ? 1 : 0);
+      const int bad = named_bar_red_or(2, Roles::kEpThreads, seg_bad);
+      const int failed = named_bar_red_or(3, Roles::kEpThreads, (!ok || abort_s) ? 1 : 0);
       if (!failed) {
         const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
         if (ep < R) {
@@ -648,7 +665,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_score_kernel(const Deco
         }
         if (ep == 0 && cf != cl) p.slot_bad[c + r] = bad;
       }
-      named_bar_sync(2, 128);                         // lists are read before the next reset
+      named_bar_sync(2, Roles::kEpThreads);           // lists are read before the next reset
       if (walk.more()) walk.next_request(p);
     }
   }
@@ -817,7 +834,7 @@ static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(decode_score_kernel<NQ, PF>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_score_kernel<NQ, PF><<<grid, kDecThreads, smem, stream>>>(p);
+  decode_score_kernel<NQ, PF><<<grid, DecRoles<NQ>::kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;

@@ -172,6 +172,18 @@ __device__ __forceinline__ void tmem_st_32x32b_x64(uint32_t taddr, const uint32_
       : "memory");
 }
 
+// Each thread loads 8 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Each thread loads 16 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float* v) {
   uint32_t r[16];
@@ -228,15 +240,18 @@ __device__ __forceinline__ float tmem_ld_red_max_32x32b_x32(uint32_t taddr, floa
   return r;
 }
 
-// Load `N` (multiple of 16) consecutive columns of the thread's lane.
+// Load `N` (multiple of 8) consecutive columns of the thread's lane.
 template <int N>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[N]) {
   if constexpr (N % 32 == 0) {
 #pragma unroll
     for (int c = 0; c < N; c += 32) tmem_ld_32x32b_x32(taddr + c, v + c);
-  } else {
+  } else if constexpr (N % 16 == 0) {
 #pragma unroll
     for (int c = 0; c < N; c += 16) tmem_ld_32x32b_x16(taddr + c, v + c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N; c += 8) tmem_ld_32x32b_x8(taddr + c, v + c);
   }
 }
 
