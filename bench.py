@@ -235,11 +235,12 @@ class GpuStep:
         self.launches_per_step = (1 if len(new) else 0) + (2 if w.num_decode_reqs else 0) + \
             (2 if w.num_prefill_reqs else 0)
 
-    def run(self, stream, d=None, events=None, k_new=None, slot_new=None):
+    def run(self, stream, d=None, events=None, k_new=None, slot_new=None, out=None):
         """Enqueue one step; events: dict name -> (start, end) recorded around each kernel."""
         d = d or self.d
         k_new = self.k_new if k_new is None else k_new
         slot_new = self.slot_new if slot_new is None else slot_new
+        out = self.out if out is None else out
         w = self.w
 
         def rec(name, i):
@@ -252,12 +253,12 @@ class GpuStep:
         if w.num_decode_reqs:
             rec("decode", 0)
             self.plan.decode(d["q_dec"], self.kv, d["dec_table"], d["dec_seq"], w.query_len,
-                             out=self.out[: self.nd], stream=stream)
+                             out=out[: self.nd], stream=stream)
             rec("decode", 1)
         if w.num_prefill_reqs:
             rec("prefill", 0)
             self.plan.prefill(d["q_pre"], d["cu"], self.kv, d["pre_table"], d["pre_seq"], self.max_q,
-                              out=self.out[self.nd:], stream=stream)
+                              out=out[self.nd:], stream=stream)
             rec("prefill", 1)
 
 
@@ -390,35 +391,64 @@ def gpu_arm(args, w, rank, world, local):
         mx["status"] = st.plan.status()
         del pages
 
-    # ---- end to end: host buffers in, ids out, through the same C ABI calls
+    # ---- end to end: host buffers in, ids out, through the same C ABI calls.
+    # Every step copies its inputs from pinned host memory and reads its ids
+    # back inside the timed region, pipelined as a serving loop runs it: two
+    # device buffer sets; a copy stream uploads step i + 1's inputs and reads
+    # step i's ids back while the compute stream runs the next step.  No L2
+    # flush inside the pipeline: a step reads more than L2 holds (the decode
+    # history alone is larger).
     e2e = None
     if args.e2e:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         hin = {k: pin(v) for k, v in st.h.items()}
         hk, hs = pin(st.h_k_new), pin(st.h_slot_new)
-        dbuf = {k: torch.empty_like(v) for k, v in st.d.items()}
-        dk, ds = torch.empty_like(st.k_new), torch.empty_like(st.slot_new)
-        hout = torch.empty(st.out.shape, dtype=torch.int32).pin_memory()
+        sets = [dict(d={k: torch.empty_like(v) for k, v in st.d.items()}, k=torch.empty_like(st.k_new),
+                     s=torch.empty_like(st.slot_new), out=torch.empty_like(st.out),
+                     h_out=torch.empty(st.out.shape, dtype=torch.int32).pin_memory()) for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in hin.values()) + hk.numel() * 2 + hs.numel() * 8
-        d2h = hout.numel() * 4
-        times = []
-        for i in range(args.warmup + args.steps):
-            flush.fill_(1)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+        d2h = st.out.numel() * 4
+        copy = torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def upload(b):
             for k in hin:
-                dbuf[k].copy_(hin[k], non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            ds.copy_(hs, non_blocking=True)
-            st.run(stream, d=dbuf, k_new=dk, slot_new=ds)
-            hout.copy_(st.out, non_blocking=True)
-            b.record(stream)
-            b.synchronize()
-            if i >= args.warmup:
-                times.append(a.elapsed_time(b))
-        e2e_s = max_over_ranks(sum(times) / 1e3, world, dev)
+                sets[b]["d"][k].copy_(hin[k], non_blocking=True)
+            sets[b]["k"].copy_(hk, non_blocking=True)
+            sets[b]["s"].copy_(hs, non_blocking=True)
+            ev_in[b].record(copy)
+
+        def pipeline(n):
+            with torch.cuda.stream(copy):
+                upload(0)
+            for i in range(n):
+                b = i & 1
+                stream.wait_event(ev_in[b])
+                st.run(stream, d=sets[b]["d"], k_new=sets[b]["k"], slot_new=sets[b]["s"], out=sets[b]["out"])
+                ev_done[b].record(stream)
+                with torch.cuda.stream(copy):
+                    if i + 1 < n:
+                        if i >= 1:
+                            copy.wait_event(ev_done[b ^ 1])     # step i - 1 is done with that set
+                        upload(b ^ 1)
+                    copy.wait_event(ev_done[b])
+                    sets[b]["h_out"].copy_(sets[b]["out"], non_blocking=True)
+
+        pipeline(max(args.warmup, 2))                            # warm-up, untimed
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(copy)
+        pipeline(args.steps)
+        stream.wait_stream(copy)
+        copy.wait_stream(stream)
+        t1.record(copy)
+        t1.synchronize()
+        e2e_s = max_over_ranks(t0.elapsed_time(t1) / 1e3, world, dev)
         e2e = {"value": work["pages_scored"] * args.steps * world / e2e_s, "unit": "pages/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "pipelined": "step i+1 uploaded and step i read back on a copy stream while the next step runs",
+               "l2": "not flushed inside the pipeline (a step reads more than L2 holds)"}
     return dict(st=st, work=work, step_ms=step_ms, kern_ms=kern_ms, total_s=total_s, clk=clk.summary(),
                 e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2], mx=mx, nr=nr)
 
