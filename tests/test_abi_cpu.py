@@ -65,3 +65,28 @@ def test_insert_argument_checks(lib):
 def test_status_rejects_null_plan(lib):
     bits = ctypes.c_int32(0)
     assert lib.indexer_get_status(None, None, ctypes.byref(bits)) == idx.IDX_EINVAL
+
+
+def test_insert_norm_rope_argument_checks(lib):
+    f = lib.nvfp4_insert_norm_rope
+    # k, positions, slots, n, weight, eps, cos_sin, max_pos, rotary_dim, is_neox, pages, num_blocks, status, stream
+    assert f(FAKE, FAKE, FAKE, -1, FAKE, 1e-6, FAKE, 16, 128, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, FAKE, 16, 96, 1, FAKE, 1, None, None) == idx.IDX_EUNSUPPORTED
+    assert b"NeoX" in lib.indexer_last_error()
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, FAKE, 16, 7, 0, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, FAKE, 16, 130, 0, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, -1.0, FAKE, 16, 128, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, float("nan"), FAKE, 16, 128, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert b"eps" in lib.indexer_last_error()
+    assert f(None, None, None, 0, None, 1e-6, None, 0, 0, 1, None, 0, None, None) == idx.IDX_OK   # n = 0
+    # a rotation needs positions and a table
+    assert f(FAKE, None, FAKE, 4, FAKE, 1e-6, FAKE, 16, 64, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, None, 16, 64, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    # the table's vector loads: 16-byte alignment for NeoX and rotary_dim % 8 == 0, 4 otherwise
+    odd = ctypes.c_void_p(0x100004)
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, odd, 16, 64, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert b"aligned" in lib.indexer_last_error()
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, odd, 16, 64, 0, FAKE, 1, None, None) == idx.IDX_EINVAL
+    misaligned = ctypes.c_void_p(0x100008)
+    assert f(misaligned, FAKE, FAKE, 4, FAKE, 1e-6, FAKE, 16, 128, 1, FAKE, 1, None, None) == idx.IDX_EINVAL
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, 1e-6, FAKE, 16, 128, 1, FAKE, 0, None, None) == idx.IDX_EINVAL
