@@ -43,6 +43,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 WORKLOAD_INDEX = {"tiny_decode": 0, "decode_batch": 1, "spec_decode": 2, "ragged_prefill": 3, "long_mixed": 4}
 KERNEL_SOURCES = ["csrc/prefill.cu", "csrc/decode.cu", "csrc/insert.cu", "csrc/ptx.cuh", "csrc/codec.cuh",
                   "csrc/topk.cuh", "csrc/internal.h"]
+# the files each timed kernel is compiled from (its own .cu and the headers it includes)
+_HEADERS = ["csrc/ptx.cuh", "csrc/codec.cuh", "csrc/topk.cuh", "csrc/internal.h"]
+KERNEL_DEPS = {"prefill": ["csrc/prefill.cu"] + _HEADERS, "decode": ["csrc/decode.cu"] + _HEADERS,
+               "insert": ["csrc/insert.cu", "csrc/codec.cuh", "csrc/internal.h"]}
 
 
 # ----------------------------------------------------------------------------- host-side logic
@@ -54,20 +58,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str = None) -> str:
+    """Hash of the kernel sources: all of them, or those `kernel` is built from."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (KERNEL_DEPS[kernel] if kernel else KERNEL_SOURCES):
         h.update(open(os.path.join(ROOT, "sparse_attention_block_nvfp4_gb300", rel), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = kernel_hash()
+    cur = kernel_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == cur:

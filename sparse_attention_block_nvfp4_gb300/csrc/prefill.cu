@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   __shared__ int warp_sum[kPreThreads / 32], warp_sum2[kPreThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();                       // the merge kernel may be scheduled
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   uint8_t* const base = smem_raw + (sbase - raw_u32);
@@ -657,25 +658,30 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   if (warp == 1) tmem_dealloc(tbase, kPreTmemCols);
 }
 
-// Merge a sorted top-15 list b (score desc, id asc; id -1 = empty) into (s, id).
+// Merge the sorted candidate list b (15 (score, id) entries from another
+// CTA, id < 0 = none) into the top 15 (s, id): the result is the first 15 of
+// both by (score descending, id ascending).  b is loaded in one go and its
+// entries go into the register list with insert_any (equal scores rank the
+// lower id first in any insertion order); the lists hold disjoint ids.
 __device__ __forceinline__ void merge_top15_list(float (&s)[kHistK], int (&id)[kHistK], const float2* b) {
-  float rs[kHistK];
-  int ri[kHistK];
-  int i = 0, j = 0;
+  float2 bb[kHistK];
+#pragma unroll
+  for (int k = 0; k < kHistK; ++k) bb[k] = b[k];
+  TopK15 t;
+#pragma unroll
   for (int k = 0; k < kHistK; ++k) {
-    const bool a_ok = i < kHistK && id[i] >= 0;
-    const float2 bj = b[j < kHistK ? j : kHistK - 1];
-    const int bi = __float_as_int(bj.y);
-    const bool b_ok = j < kHistK && bi >= 0;
-    const bool take_a = a_ok && (!b_ok || s[i] > bj.x || (s[i] == bj.x && id[i] < bi));
-    rs[k] = take_a ? s[i] : (b_ok ? bj.x : -CUDART_INF_F);
-    ri[k] = take_a ? id[i] : (b_ok ? bi : -1);
-    i += take_a ? 1 : 0;
-    j += (!take_a && b_ok) ? 1 : 0;
+    t.s[k] = id[k] >= 0 ? s[k] : -CUDART_INF_F;
+    t.id[k] = id[k];
   }
+#pragma unroll
   for (int k = 0; k < kHistK; ++k) {
-    s[k] = rs[k];
-    id[k] = ri[k];
+    const int bi = __float_as_int(bb[k].y);
+    if (bi >= 0) t.insert_any(bb[k].x, bi);
+  }
+#pragma unroll
+  for (int k = 0; k < kHistK; ++k) {
+    s[k] = t.s[k];
+    id[k] = t.id[k];
   }
 }
 
@@ -686,6 +692,7 @@ __device__ __forceinline__ void merge_top15_list(float (&s)[kHistK], int (&id)[k
 // tile (t / 128).
 template <int H>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
+  griddep_wait();                                    // the scoring grid's candidates are written
   const int c = blockIdx.x, G = gridDim.x;
   const int x = threadIdx.x >> 7, n = threadIdx.x & 127;
   for (int sh = 0; sh < 2; ++sh) {
@@ -727,8 +734,7 @@ static cudaError_t launch_prefill_h(const PrefillParams& p, int grid, cudaStream
   prefill_kernel<H, PF><<<grid, kPreThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_merge_kernel<H><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(prefill_merge_kernel<H>, (unsigned)grid, 256u, 0, stream, p);
 }
 
 template <class PF>
