@@ -89,8 +89,15 @@ def test_traffic_needs_current_kernel_hash(tmp_path, monkeypatch):
     os.makedirs(src)
     for rel in bench.KERNEL_SOURCES:
         (tmp_path / "sparse_attention_block_nvfp4_gb300" / rel).write_text("x")
-    h = bench.kernel_hash()
-    (tmp_path / "profiles" / "traffic.txt").write_text(f"prefill long_mixed {h} 12345\nprefill long_mixed deadbeef 1\n")
+    hp, hd = bench.kernel_hash("prefill"), bench.kernel_hash("decode")
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        f"prefill long_mixed {hp} 12345\nprefill long_mixed deadbeef 1\ndecode long_mixed {hd} 678\n")
     assert bench.recorded_traffic("prefill", "long_mixed") == 12345.0
+    assert bench.recorded_traffic("decode", "long_mixed") == 678.0
+    # a change to one kernel's own source voids only that kernel's record
     (tmp_path / "sparse_attention_block_nvfp4_gb300" / "csrc" / "prefill.cu").write_text("changed")
     assert bench.recorded_traffic("prefill", "long_mixed") is None
+    assert bench.recorded_traffic("decode", "long_mixed") == 678.0
+    # a shared header voids both
+    (tmp_path / "sparse_attention_block_nvfp4_gb300" / "csrc" / "ptx.cuh").write_text("changed")
+    assert bench.recorded_traffic("decode", "long_mixed") is None
