@@ -31,8 +31,12 @@ Modules:
              vllm.models.minimax_m3.amd.indexer_mxfp4: the same scores and
              top-k over [pages, 8704] e2m1 / e8m0 pages).
   norm_rope - qk-norm (RMSNorm) and RoPE of the index key before the NVFP4
-             insert, in the fp32 order the fused insert uses.
+             insert: the float64 definition, its bf16 rounding, the error
+             bound of an fp32 evaluation and the row check built on it.
   indexer  - positions, page scores, selection; decode and prefill oracles.
+  attend   - block-sparse attention over the selected pages of a bf16 main
+             KV cache (the consumer of the [T, H, 16] id buffer), float64,
+             with the error bound of an fp32 evaluation.
   brute    - scalar pure-Python brute force for tiny inputs (a pin).
   checker  - parity checker (ids modulo score ties within tolerance).
 
@@ -41,4 +45,4 @@ tests/golden/, exhaustive format tables against torch / ml_dtypes casts,
 scalar brute force, closed-form special cases, invariants, and planted
 mistakes that each pin must catch.  No function here is "parity unpinned".
 """
-from . import formats, nvfp4, norm_rope, indexer, checker, brute  # noqa: F401
+from . import formats, nvfp4, norm_rope, indexer, checker, brute, attend  # noqa: F401

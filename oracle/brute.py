@@ -120,3 +120,38 @@ def indexer_rows(q, kv_pages, page_table, seq_lens, qlens, num_heads, page_forma
             out.append(per_head)
             row += 1
     return out, scores
+
+
+def bf16(bits: int) -> float:
+    """bf16 from its fields: sign | 8-bit exponent (bias 127) | 7-bit mantissa."""
+    s = -1.0 if bits & 0x8000 else 1.0
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    if e == 0xFF:
+        return math.nan if m else s * math.inf
+    if e == 0:
+        return s * math.ldexp(m, -133)          # m/128 * 2^-126
+    return s * math.ldexp(128 + m, e - 134)     # (1 + m/128) * 2^(e-127)
+
+
+def attend_one(q_bits, k_cache, v_cache, page_table_row, pos: int, ids_row, hk: int, scale: float):
+    """Block-sparse attention of one query head (pure Python): walk every
+    position 0 .. pos of the request, keep those whose page (position // 128)
+    is among the selected ids, score q.k * scale with plain float loops,
+    softmax with the maximum subtracted, weighted sum of the v rows.  Returns
+    a list of 128 floats (all 0 when nothing is visible)."""
+    chosen = {int(j) for j in ids_row if int(j) >= 0}
+    q = [bf16(int(b)) for b in q_bits]
+    toks = []
+    for p in range(pos + 1):
+        if p // 128 in chosen:
+            blk = int(page_table_row[p // 128])
+            k = [bf16(int(b)) for b in k_cache[blk][p % 128][hk]]
+            v = [bf16(int(b)) for b in v_cache[blk][p % 128][hk]]
+            toks.append((scale * math.fsum(a * b for a, b in zip(q, k)), v))
+    if not toks:
+        return [0.0] * len(q)
+    m = max(s for s, _ in toks)
+    w = [math.exp(s - m) for s, _ in toks]
+    tot = math.fsum(w)
+    return [math.fsum(wi * v[d] for wi, (_, v) in zip(w, toks)) / tot for d in range(len(q))]

@@ -269,3 +269,86 @@ def random_pages(num_blocks: int, rng: np.random.Generator, nan_free: bool = Tru
 
 def random_q(rows: int, heads: int, rng: np.random.Generator) -> np.ndarray:
     return _to_e4m3_bytes(rng.standard_normal((rows, heads, DIM), dtype=np.float32)).reshape(rows, heads, DIM)
+
+
+# ----------------------------------------------------------------------------- block-sparse attend inputs
+# The main KV cache the attend reads: bf16 [num_blocks, 128, H, 128] for K and
+# for V.  It is as large as the index cache times H x 128 bf16 per token (about
+# 10 GB for the long mixed step), so its values come from a counter-based
+# hash of the element's coordinates: the CPU computes only the pages it
+# checks, the GPU fills the whole cache with the same bits (torch integer
+# ops, in chunks).  Hash: 32-bit murmur3 finalizer of
+# (element index XOR seed key); value: sign bit, exponent 124..127 and a
+# 7-bit mantissa from the hash, so |value| lies in [1/8, 2).
+_M32 = 0xFFFFFFFF
+
+
+def _mul32(x, c: int):
+    """(x * c) mod 2^32 for 0 <= x < 2^32 held in int64, without overflow."""
+    lo, hi = c & 0xFFFF, c >> 16
+    return (x * lo + (((x * hi) & 0xFFFF) << 16)) & _M32
+
+
+def _fmix32(x):
+    x = x ^ (x >> 16)
+    x = _mul32(x, 0x85EBCA6B)
+    x = x ^ (x >> 13)
+    x = _mul32(x, 0xC2B2AE35)
+    return x ^ (x >> 16)
+
+
+def _kv_key(seed: int, which: int) -> int:
+    return ((seed * 0x9E3779B1) ^ (which * 0x7F4A7C15) ^ 0x2545F491) & _M32
+
+
+def _hash_to_bf16(h):
+    return ((h >> 9) & 1) << 15 | (124 + ((h >> 7) & 3)) << 7 | (h & 0x7F)
+
+
+def attend_kv_pages(seed: int, which: int, blocks, H: int) -> np.ndarray:
+    """bf16 bits [len(blocks), 128, H, 128] of main-cache blocks ``blocks``
+    (which = 0 for K, 1 for V), numpy."""
+    b = np.asarray(blocks, dtype=np.int64).reshape(-1, 1, 1, 1)
+    t = np.arange(PAGE, dtype=np.int64).reshape(1, -1, 1, 1)
+    h = np.arange(H, dtype=np.int64).reshape(1, 1, -1, 1)
+    d = np.arange(DIM, dtype=np.int64).reshape(1, 1, 1, -1)
+    e = (((b * PAGE + t) * H + h) * DIM + d) & _M32
+    return _hash_to_bf16(_fmix32(e ^ _kv_key(seed, which))).astype(np.uint16)
+
+
+def attend_kv_fill(seed: int, which: int, num_blocks: int, H: int, device, chunk_blocks: int = 2048):
+    """The whole main cache [num_blocks, 128, H, 128] as an int16 torch tensor
+    on ``device`` (bf16 bits), the same values as ``attend_kv_pages``."""
+    import torch
+    out = torch.empty((num_blocks, PAGE, H, DIM), dtype=torch.int16, device=device)
+    per = PAGE * H * DIM
+    key = _kv_key(seed, which)
+    for b0 in range(0, num_blocks, chunk_blocks):
+        b1 = min(num_blocks, b0 + chunk_blocks)
+        e = (torch.arange(b0 * per, b1 * per, dtype=torch.int64, device=device) & _M32) ^ key
+        v = _hash_to_bf16(_fmix32(e))
+        out[b0:b1] = (v - ((v >> 15) << 16)).to(torch.int16).view(b1 - b0, PAGE, H, DIM)
+    return out
+
+
+def attend_q(rows: int, heads: int, rng: np.random.Generator) -> np.ndarray:
+    """Attention queries, bf16 bits [rows, heads, 128] from N(0, 1)."""
+    return _to_bf16_bits(rng.standard_normal((rows, heads, DIM), dtype=np.float32)).reshape(rows, heads, DIM)
+
+
+def attend_rows(w: "Workload"):
+    """(row_req, row_pos) int32 [rows] of the workload's rows: decode rows
+    first (request-major, query i at seq_len - query_len + i), then the
+    prefill rows (context first)."""
+    req, pos = [], []
+    for r in range(w.num_decode_reqs):
+        s = int(w.dec_seq_lens[r])
+        for i in range(w.query_len):
+            req.append(r)
+            pos.append(s - w.query_len + i)
+    for k in range(w.num_prefill_reqs):
+        s, ql = int(w.pre_seq_lens[k]), int(w.pre_query_lens[k])
+        for i in range(ql):
+            req.append(w.num_decode_reqs + k)
+            pos.append(s - ql + i)
+    return np.array(req, np.int32), np.array(pos, np.int32)
