@@ -13,8 +13,15 @@ history pages scored, per second of step time.  Timing: CUDA events on the
 launching stream around each step (and around each kernel, for the roofline),
 L2 flushed (a 2 x L2 write) between steps, W warm-up steps first.
 
+Besides the step, the line carries timings taken apart from it: the
+whole-cache inserts, MXFP4-page calls, the block-sparse attend over the
+decode rows' selected pages (``kernels.attend_decode``), and a ``workloads``
+record with every other named workload's kernels (time, achieved rate,
+fraction of the measured peak) beside the oracle's pages/s on a short
+sample of it.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--sweep]
+                  [--workload NAME] [--sweep] [--no-workloads] [--no-attend]
 
 Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own full
 batch (weak scaling, no data-path collective); value = all ranks' pages /
@@ -454,8 +461,10 @@ def gpu_arm(args, w, rank, world, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "pipelined": "step i+1 uploaded and step i read back on a copy stream while the next step runs",
                "l2": "not flushed inside the pipeline (a step reads more than L2 holds)"}
+    att = attend_leg(st, w, dev, flush, stream) if getattr(args, "attend", False) else None
     return dict(st=st, work=work, step_ms=step_ms, kern_ms=kern_ms, total_s=total_s, clk=clk.summary(),
-                e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2], mx=mx, nr=nr)
+                e2e=e2e, status=status, fill_ms=sorted(fill_ms)[len(fill_ms) // 2], mx=mx, nr=nr, att=att,
+                num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
 
 
 def roofline_block(res, w, wname, peaks, peak_kind):
@@ -516,6 +525,16 @@ def roofline_block(res, w, wname, peaks, peak_kind):
             kernels["insert_fill_mxfp4"] = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"],
                                             "unit": "GB/s", "frac": gb / peaks["hbm_gbs"], "ms": ms,
                                             "keys": int(n_all), "note": "whole-cache MXFP4 insert"}
+    att = res.get("att")
+    if att:
+        kernels["attend_decode"] = dict(att, peak=peaks["hbm_gbs"], frac=att["achieved"] / peaks["hbm_gbs"])
+    # the tensor pipes' own dense rate at the sampled clock, next to the
+    # cuBLAS-measured burst (a tuned kernel can exceed what cuBLAS reached)
+    tp = tensor_issue_peak((res.get("clk") or {}).get("sm_mhz"), res.get("num_sms", 0))
+    for k in ("prefill", "prefill_mxfp4"):
+        if k in kernels and tp:
+            kernels[k]["peak_issue"] = tp
+            kernels[k]["frac_issue"] = kernels[k]["achieved"] / tp
     step_kernels = ("insert", "decode", "prefill")
     dom = max((k for k in kernels if k in step_kernels), key=lambda k: kernels[k]["ms"])
     rl = dict(kernels[dom])
@@ -523,6 +542,9 @@ def roofline_block(res, w, wname, peaks, peak_kind):
     rl.pop("tensor_tflops", None)
     rl["kernel"] = dom
     rl["peak_source"] = f"{peak_kind} ({'bf16 dense burst; fp16 has the same dense rate' if rl['unit'] == 'TFLOP/s' else 'copy bandwidth'})"
+    if "peak_issue" in rl:
+        rl["peak_issue_source"] = ("8192 flop per clock per SM (dense fp16 MMA rate) x SMs x median sampled "
+                                   "SM clock; frac_issue = achieved / peak_issue")
     return rl, kernels
 
 
@@ -598,6 +620,89 @@ def cpu_block(w, budget_s):
                                         f"NumPy float64, BLAS on all host cores"}
 
 
+def tensor_issue_peak(sm_mhz, num_sms):
+    """Dense fp16 / bf16 rate of the tensor pipes at the sampled SM clock:
+    8192 flops per clock per SM (one M = 128, N = 256, K = 16 MMA per 128
+    clocks; measured 8148 on this GPU with back-to-back MMAs), TFLOP/s."""
+    if not sm_mhz:
+        return None
+    return 8192.0 * num_sms * sm_mhz * 1e6 / 1e12
+
+
+def workload_record(res, w, wname, peaks, cpu):
+    """Per-workload summary: kernel times, achieved rates and fractions of
+    the measured peaks, pages scored per second, the oracle's pages/s."""
+    work = res["work"]
+    _, kernels = roofline_block(res, w, wname, peaks, "measured")
+    rec = {"pages_scored_per_step": work["pages_scored"],
+           "pages_per_s": work["pages_scored"] * len(res["step_ms"]) / (sum(res["step_ms"]) / 1e3),
+           "ms_per_step": sum(res["step_ms"]) / len(res["step_ms"]), "kernels": {}}
+    for k in ("decode", "prefill", "insert", "insert_fill"):
+        if k in kernels:
+            e = kernels[k]
+            rec["kernels"][k] = {kk: e[kk] for kk in ("ms", "achieved", "unit", "frac", "bound") if kk in e}
+    if cpu is not None:
+        rec["oracle_pages_per_s"] = cpu["value"]
+        rec["oracle_sample"] = cpu["sample"]
+    return rec
+
+
+def attend_leg(st, w, dev, flush, stream, reps=20):
+    """The block-sparse attend over the decode rows' selected pages: bf16
+    main cache [num_blocks, 128, H, 128] (K and V, hashed values), one query
+    head per KV head, the ids the step's decode just wrote.  Timed alone,
+    L2 flushed before each call; not part of the step.  Algorithmic bytes:
+    every (request, KV head)'s union of selected pages' visible K and V rows
+    once, plus the queries and the fp32 output."""
+    import torch
+    nd = st.nd
+    if nd == 0:
+        return None
+    H, G = w.num_heads, 1
+    req, pos = workloads.attend_rows(w)
+    req, pos = req[:nd], pos[:nd]
+    kc = workloads.attend_kv_fill(11, 0, w.num_blocks, H, dev)
+    vc = workloads.attend_kv_fill(11, 1, w.num_blocks, H, dev)
+    q = torch.from_numpy(workloads.attend_q(nd, H * G, np.random.Generator(np.random.PCG64(11))).view(np.int16)).to(dev)
+    ids = st.out[:nd].clone()
+    d_req, d_pos = torch.from_numpy(req).to(dev), torch.from_numpy(pos).to(dev)
+    table = torch.from_numpy(w.page_table).to(dev)
+    out = torch.empty((nd, H * G, 128), dtype=torch.float32, device=dev)
+    ms = []
+    for i in range(3 + reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        st.idx.sparse_attend(q, kc, vc, table, d_req, d_pos, ids, 128 ** -0.5, out=out, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            ms.append(a.elapsed_time(b))
+    ids_np = ids.cpu().numpy()
+    uniq, gathered = 0, 0
+    for r in range(w.num_decode_reqs):
+        rows = np.arange(r * w.query_len, (r + 1) * w.query_len)
+        for h in range(H):
+            seen = {}
+            for t in rows:
+                for j in ids_np[t, h]:
+                    if j < 0:
+                        continue
+                    n = min(128, int(pos[t]) - 128 * int(j) + 1)
+                    gathered += n
+                    seen[int(j)] = max(seen.get(int(j), 0), n)
+            uniq += sum(seen.values())
+    per_tok = 2 * 128 * 2                                   # K and V rows of one head, bf16
+    alg = uniq * per_tok + nd * H * G * 128 * (2 + 4)
+    med = sorted(ms)[len(ms) // 2]
+    del kc, vc
+    return {"bound": "hbm", "ms": med, "achieved": alg / (med / 1e3) / 1e9, "unit": "GB/s",
+            "bytes": int(alg), "bytes_gathered_per_unit": int(gathered * per_tok),
+            "units": int(nd * H), "q_per_kv": G,
+            "note": "long_mixed decode rows (16 x 8 queries, 8 KV heads), ids from the step's decode; "
+                    "timed alone, not part of the step"}
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -614,6 +719,12 @@ def main():
     ap.add_argument("--no-norm-rope", dest="norm_rope", action="store_false",
                     help="skip the timed whole-cache fused qk-norm + RoPE insert")
     ap.add_argument("--sweep", action="store_true", help="one line per named workload (no e2e / cpu)")
+    ap.add_argument("--no-workloads", dest="all_workloads", action="store_false",
+                    help="skip the per-workload record of the other named workloads")
+    ap.add_argument("--cpu-budget-others", type=float, default=3.0,
+                    help="seconds of oracle work per other workload in the per-workload record")
+    ap.add_argument("--no-attend", dest="attend", action="store_false",
+                    help="skip the timed block-sparse attend over the decode rows")
     ap.add_argument("--no-flush", dest="flush", action="store_false",
                     help="skip the L2 flush (profiling runs only; the timed numbers then see a warm L2)")
     args = ap.parse_args()
@@ -665,6 +776,7 @@ def main():
         sweep_args = argparse.Namespace(**vars(args))
         if args.sweep:
             sweep_args.e2e = False
+        sweep_args.attend = args.attend and wname == "long_mixed"
         res = gpu_arm(sweep_args, w, rank, world, local)
         work = res["work"]
         value = work["pages_scored"] * args.steps * world / res["total_s"]
@@ -687,6 +799,23 @@ def main():
             line["e2e"] = res["e2e"]
         if rank == 0 and world == 1 and args.cpu_baseline and not args.sweep:
             line["cpu_baseline"] = cpu_block(w, args.cpu_budget)
+        if world == 1 and args.all_workloads and not args.sweep:
+            # every named workload: its kernels and the oracle's rate beside them
+            recs = {wname: workload_record(res, w, wname, peaks, line.get("cpu_baseline"))}
+            del res
+            for other in WORKLOAD_INDEX:
+                if other == wname:
+                    continue
+                wo = workloads.config(WORKLOAD_INDEX[other])
+                oa = argparse.Namespace(**vars(args))
+                oa.e2e = oa.mxfp4 = oa.norm_rope = oa.attend = False
+                oa.steps, oa.warmup = min(args.steps, 20), 3
+                ro = gpu_arm(oa, wo, rank, world, local)
+                line["device_status"] |= ro["status"]
+                cpu = cpu_block(wo, args.cpu_budget_others) if args.cpu_baseline else None
+                recs[other] = workload_record(ro, wo, other, peaks, cpu)
+                del ro
+            line["workloads"] = recs
         if rank == 0:
             print(json.dumps(line), flush=True)
     if world > 1:

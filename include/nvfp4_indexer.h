@@ -64,7 +64,7 @@ enum {
 enum {
   IDX_STATUS_BAD_PAGE = 1,     /* a page id outside the cache; rows set to -1  */
   IDX_STATUS_BAD_TABLE = 2,    /* history wider than pt_stride; rows set to -1 */
-  IDX_STATUS_TIMEOUT = 4,      /* a bounded wait gave up; outputs undefined    */
+  IDX_STATUS_TIMEOUT = 4,      /* a bounded wait gave up; unfinished rows -1   */
   IDX_STATUS_BAD_SLOT = 8,     /* an insert skipped a slot past the cache       */
   IDX_STATUS_BAD_POSITION = 16 /* nvfp4_insert_norm_rope skipped a token whose
                                   position lies outside the cos/sin table       */
@@ -103,6 +103,21 @@ int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_quer
 int indexer_plan_destroy(indexer_plan_t plan);
 
 /*
+ * indexer_plan_set_wait_limit -- wall-time limit of every bounded wait
+ * inside the decode and prefill kernels run with this plan (no counterpart
+ * in the pages: failure detection of this library).  Each wait between the
+ * kernels' roles (copy landed, operands ready, accumulator free) gives up
+ * after wait_ns nanoseconds; the kernel then sets IDX_STATUS_TIMEOUT in the
+ * plan's status word, stops issuing work, waits (bounded, 2 s) for its own
+ * copies and tensor-core work in flight, frees its tensor memory and
+ * returns; the rows whose scores it could not finish are written as -1
+ * (decode and prefill alike), the others are exact.  wait_ns = 0 restores
+ * the default of 2 s.  Applies to calls queued after it; the plan's other
+ * state is unchanged.  IDX_EINVAL for a NULL plan.
+ */
+int indexer_plan_set_wait_limit(indexer_plan_t plan, uint64_t wait_ns);
+
+/*
  * indexer_decode -- top-k pages for uniform decode batches
  * (MiniMaxM3IndexerNvfp4Impl.forward, decode branch; the Q8KV4 indexer reads
  * the 1..8 queries of each request in place and writes straight to out).
@@ -139,7 +154,10 @@ int indexer_decode(indexer_plan_t plan, const uint8_t* q, const uint8_t* kv_page
  *                request r owns rows cu[r] .. cu[r+1]-1 at positions
  *                seq_lens[r] - (cu[r+1]-cu[r]) + i (context first)
  *   num_reqs     1..plan max_prefill_reqs;  total_q <= plan max_prefill_tokens
- *   max_seqlen_q host upper bound of cu[r+1]-cu[r] (sizes the grid)
+ *   max_seqlen_q host upper bound of cu[r+1]-cu[r]: checked to lie in
+ *                0..total_q, otherwise advisory (the grid is one CTA per
+ *                SM and the split of the work is computed on the device
+ *                from cu_seqlens_q, so a captured graph stays valid)
  *   out          int32 [total_q][H][16] (pass decode out + num_decode_rows*H*16
  *                for a mixed step; decode rows come first, as in forward)
  *   scores_dbg   NULL, or fp32 [total_q][H][dbg_stride], dbg_stride >= pt_stride
@@ -176,10 +194,15 @@ int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uin
  *   rotary pairs (y1, y2) -> (y1 cos - y2 sin, y2 cos + y1 sin), angles from
  *   row `position` of cos_sin_cache; elements past rotary_dim pass through;
  *   the result rounded to bf16, then quantised and written as nvfp4_insert.
- * fp32 order: four running sums of 32 squares (elements 32j..32j+31),
- * combined as (s0 + s1) + (s2 + s3); v = ss / 128 + eps; rs = 1 / sqrt(v),
- * square root and division correctly rounded; y = (x * rs) * w; every
- * rotation product and sum rounded separately (no fused multiply-add).
+ * fp32 order of this kernel: per 16-element group g, running sums e_g and
+ * o_g of the even and odd elements' squares (one fused multiply-add per
+ * step), t_g = e_g + o_g, ss = ((t0 + t1) + (t2 + t3)) + ((t4 + t5) +
+ * (t6 + t7)); v = ss / 128 + eps; rs = 1 / sqrt(v), square root and
+ * division correctly rounded; y = (x * rs) * w; every rotation product and
+ * sum rounded separately (no fused multiply-add).  The bf16 keys are
+ * therefore those of the exact RMSNorm + RoPE up to that fp32 error (an
+ * element whose exact value lies that close to a bf16 rounding boundary
+ * may round to the other neighbour).
  *   k_bf16         [n][128] bf16 bit patterns, 16-byte aligned
  *   positions      int64 [n] (unused, may be NULL, when rotary_dim == 0)
  *   slot_mapping   int64 [n]: page * 128 + row; negative = skip
@@ -312,14 +335,58 @@ int indexer_merge_candidates(const float* cand_all, int world, int num_reqs, int
  * call that needs more than 4 MiB returns IDX_ENOSPACE and launches nothing
  * (about 390 requests at query_len*num_heads = 64 on a 152-SM GPU).
  * The first call on a device looks up the array's device address with
- * cudaGetSymbolAddress (once per device, that device current): make that
- * first call before any stream capture.  All calls share the array, so calls
- * whose kernels overlap on the GPU race and must be serialised by the caller.
+ * cudaGetSymbolAddress (once per device, that device current) and checks
+ * that the device is sm_103 (else IDX_EUNSUPPORTED): make that first call
+ * before any stream capture.  The address is cached for the life of the
+ * process; after cudaDeviceReset on a device, do not call this entry point
+ * on it again.  All calls share the array, so calls whose kernels overlap
+ * on the GPU race and must be serialised by the caller.  If a wait inside
+ * the kernels runs out (2 s without progress), the affected rows are -1 and
+ * IDX_STATUS_TIMEOUT goes to *status; with status NULL the rows are still
+ * -1 but the reason is not reported anywhere.
  */
 int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages, int num_blocks,
                            const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
                            int num_reqs, int query_len, int num_heads, int32_t* out,
                            int32_t* status, cudaStream_t stream);
+
+/*
+ * indexer_sparse_attend -- block-sparse attention over the selected pages,
+ * the consumer of the [T, H, 16] id buffer (page
+ * vllm.models.minimax_m3.nvidia.indexer_nvfp4, MiniMaxM3IndexerNvfp4Impl
+ * .forward: the ids go "straight into the shared [T, H, 16] buffer the
+ * attend reads"; page vllm.models.minimax_m3.nvidia.indexer_flashinfer,
+ * forward: "The attend reads the shared buffer directly").  The pages do not
+ * describe the attend; this library reads it as the usual paged sparse
+ * attention: per row t and KV head hk (one per index head), query heads
+ * hk*G .. hk*G+G-1 attend over the tokens of the pages ids[t][hk][0..15]
+ * (-1 skipped) whose position is at most the row's (causal cut inside the
+ * local page): o = sum_s softmax_s(scale * q.k_s) v_s, in fp32 (bf16
+ * products exact, exp2f on log2e-scaled scores, online softmax page by
+ * page); a row with no visible token gets o = 0.
+ *   q          bf16 [num_rows][num_kv_heads * q_per_kv][128], 16-byte aligned
+ *   k_cache    bf16 [num_blocks][128][num_kv_heads][128] (token-major pages,
+ *              logical page j of request r = block page_table[r][j])
+ *   v_cache    same layout as k_cache
+ *   page_table int32 [num_reqs][pt_stride] (the indexer's table)
+ *   row_req    int32 [num_rows]: the request of each row
+ *   row_pos    int32 [num_rows]: the position of each row (decode: seq_len
+ *              - query_len + i; prefill: seq_len - new tokens + i)
+ *   topk_ids   int32 [num_rows][num_kv_heads][16]: indexer output
+ *   num_kv_heads 1, 2, 4 or 8; q_per_kv (G) 1, 2, 4 or 8
+ *   scale      finite (1/sqrt(128) for the usual scaling)
+ *   out        fp32 [num_rows][num_kv_heads * q_per_kv][128]
+ *   status     NULL, or a device int32: IDX_STATUS_BAD_TABLE (a request
+ *              outside 0..num_reqs-1, an id >= pt_stride) or
+ *              IDX_STATUS_BAD_PAGE (a block outside the cache) is OR-ed in
+ *              and that (row, head)'s output is all zeros
+ * All pointers are device pointers; nothing is allocated; the call does
+ * not synchronise.
+ */
+int indexer_sparse_attend(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, int num_blocks,
+                          const int32_t* page_table, int pt_stride, int num_reqs, const int32_t* row_req,
+                          const int32_t* row_pos, const int32_t* topk_ids, int num_rows, int num_kv_heads,
+                          int q_per_kv, float scale, float* out, int32_t* status, cudaStream_t stream);
 
 /* Synchronise `stream`, read and clear the plan's device status word.
  * Returns IDX_OK, or IDX_EDEVICE with the IDX_STATUS_* bits in *bits. */

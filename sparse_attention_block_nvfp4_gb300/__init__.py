@@ -17,7 +17,7 @@ import os
 import re
 from typing import Optional
 
-__all__ = ["Plan", "insert", "insert_norm_rope", "decode_noalloc", "IndexerError", "load_library", "library_path", "declared_symbols",
+__all__ = ["Plan", "insert", "insert_norm_rope", "decode_noalloc", "sparse_attend", "IndexerError", "load_library", "library_path", "declared_symbols",
            "STATUS_BAD_PAGE", "STATUS_BAD_TABLE", "STATUS_TIMEOUT", "STATUS_BAD_SLOT", "STATUS_BAD_POSITION",
            "TOPK", "PAGE"]
 
@@ -73,11 +73,13 @@ def load_library():
     lib.indexer_decode_partial.argtypes = [P, I, P, P, I, P, I, P, P, P, I, I, P, P]
     lib.indexer_merge_candidates.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.indexer_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.indexer_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
     lib.indexer_last_error.restype = ctypes.c_char_p
     lib.indexer_version.restype = ctypes.c_char_p
     for name in ("indexer_plan", "indexer_plan_destroy", "indexer_decode", "indexer_prefill",
                  "nvfp4_insert", "indexer_get_status", "indexer_decode_mxfp4", "indexer_prefill_mxfp4",
-                 "mxfp4_insert", "indexer_decode_partial", "indexer_merge_candidates", "nvfp4_insert_norm_rope"):
+                 "mxfp4_insert", "indexer_decode_partial", "indexer_merge_candidates", "nvfp4_insert_norm_rope",
+                 "indexer_plan_set_wait_limit"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -228,6 +230,12 @@ class Plan:
             _ptr(scores_dbg, torch.float32, "scores_dbg"), dbg_stride, _stream_ptr(stream)))
         return out
 
+    def set_wait_limit(self, wait_ns: int = 0):
+        """Wall-time limit (ns) of every bounded wait inside the decode and
+        prefill kernels of later calls (``indexer_plan_set_wait_limit``);
+        0 restores the default of 2 s."""
+        _check(load_library().indexer_plan_set_wait_limit(self._h, int(wait_ns)))
+
     def status(self, stream=None) -> int:
         """Synchronise, read and clear the device status word (IDX_STATUS_* bits)."""
         bits = ctypes.c_int32(0)
@@ -335,6 +343,42 @@ def decode_cp(plan, q, pages, page_table, seq_lens, page_lo, page_hi, query_len:
                                page_format=page_format, stream=stream)
     return merge_candidates(gather_candidates(cand, group), seq_lens, query_len, plan.num_heads, out=out,
                             stream=stream)
+
+
+def sparse_attend(q, k_cache, v_cache, page_table, row_req, row_pos, topk_ids, scale: float, out=None,
+                  status=None, stream=None):
+    """``indexer_sparse_attend``: block-sparse attention of bf16 queries
+    [rows, H * G, 128] over the pages in ``topk_ids`` [rows, H, 16] of a bf16
+    main cache [num_blocks, 128, H, 128] (K and V); returns fp32
+    [rows, H * G, 128]."""
+    import torch
+    lib = load_library()
+    fn = lib.indexer_sparse_attend
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [P, P, P, I, P, I, I, P, P, P, I, I, I, ctypes.c_float, P, P, P]
+    fn.restype = I
+    if k_cache.dim() != 4 or k_cache.shape[1] != PAGE or k_cache.shape[3] != 128 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache / v_cache: expected the same shape [num_blocks, 128, H, 128]")
+    H = int(k_cache.shape[2])
+    rows = int(topk_ids.shape[0])
+    if topk_ids.dim() != 3 or topk_ids.shape[1] != H or topk_ids.shape[2] != TOPK:
+        raise ValueError(f"topk_ids: expected [rows, {H}, 16], got {tuple(topk_ids.shape)}")
+    if q.dim() != 3 or q.shape[0] != rows or q.shape[1] % H or q.shape[2] != 128:
+        raise ValueError(f"q: expected [{rows}, {H} * G, 128], got {tuple(q.shape)}")
+    if row_req.shape[0] != rows or row_pos.shape[0] != rows:
+        raise ValueError("row_req / row_pos must have one entry per row")
+    qb = q.view(torch.int16) if q.dtype == torch.bfloat16 else q
+    kb = k_cache.view(torch.int16) if k_cache.dtype == torch.bfloat16 else k_cache
+    vb = v_cache.view(torch.int16) if v_cache.dtype == torch.bfloat16 else v_cache
+    if out is None:
+        out = torch.empty(tuple(q.shape), dtype=torch.float32, device=q.device)
+    _check(fn(_ptr(qb, torch.int16, "q"), _ptr(kb, torch.int16, "k_cache"), _ptr(vb, torch.int16, "v_cache"),
+              int(k_cache.shape[0]), _ptr(page_table, torch.int32, "page_table", 2), int(page_table.shape[1]),
+              int(page_table.shape[0]), _ptr(row_req, torch.int32, "row_req", 1),
+              _ptr(row_pos, torch.int32, "row_pos", 1), _ptr(topk_ids, torch.int32, "topk_ids", 3), rows, H,
+              int(q.shape[1]) // H, float(scale), _ptr(out, torch.float32, "out", 3),
+              _ptr(status, torch.int32, "status"), _stream_ptr(stream)))
+    return out
 
 
 def decode_noalloc(q, kv_pages, page_table, seq_lens, query_len: int, num_heads: int, out=None,

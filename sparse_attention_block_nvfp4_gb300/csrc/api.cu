@@ -47,6 +47,7 @@ struct indexer_plan_s {
   int num_heads = 0, max_reqs = 0, max_query_len = 0, max_pages = 0;
   int max_prefill_tokens = 0, max_prefill_reqs = 0;
   int decode_grid = 0;
+  uint64_t wait_ns = kWaitLimitNs;   // limit of each bounded wait inside the kernels
   float2* cand = nullptr;      // [(decode_grid + max_reqs)][<= 64 rows][15]
   int32_t* slot_bad = nullptr; // [decode_grid + max_reqs]
   int2* req_info = nullptr;    // [max_reqs]
@@ -109,6 +110,7 @@ static int decode_impl(const char* fn, int page_format, indexer_plan_t plan, con
   p.page_lo = page_lo;
   p.page_hi = page_hi;
   p.cand_out = reinterpret_cast<float2*>(cand_out);
+  p.wait_ns = plan->wait_ns;
   cudaError_t e = launch_decode(p, plan->decode_grid, stream);
   if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
   return IDX_OK;
@@ -161,6 +163,7 @@ static int prefill_impl(const char* fn, int page_format, indexer_plan_t plan, co
   p.pslot = plan->pslot;
   const int grid = plan->num_sms;   // one prefill CTA per SM; the work is split evenly by pages
   p.page_format = page_format;
+  p.wait_ns = plan->wait_ns;
   cudaError_t e = launch_prefill(p, grid, stream);
   if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
   return IDX_OK;
@@ -243,6 +246,13 @@ int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_quer
     return cuda_err(e, "indexer_plan: allocation");
   }
   *plan = pl;
+  return IDX_OK;
+}
+
+int indexer_plan_set_wait_limit(indexer_plan_t plan, uint64_t wait_ns) {
+  g_last_error.clear();
+  if (!plan) return set_err(IDX_EINVAL, "indexer_plan_set_wait_limit: plan is NULL");
+  plan->wait_ns = wait_ns ? wait_ns : kWaitLimitNs;
   return IDX_OK;
 }
 
@@ -372,6 +382,48 @@ int nvfp4_insert_norm_rope(const uint16_t* k_bf16, const int64_t* positions, con
   a.num_slots = (int64_t)num_blocks * 128;
   a.status = status;
   cudaError_t e = launch_insert_norm_rope(a, stream);
+  if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
+  return IDX_OK;
+}
+
+int indexer_sparse_attend(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, int num_blocks,
+                          const int32_t* page_table, int pt_stride, int num_reqs, const int32_t* row_req,
+                          const int32_t* row_pos, const int32_t* topk_ids, int num_rows, int num_kv_heads,
+                          int q_per_kv, float scale, float* out, int32_t* status, cudaStream_t stream) {
+  g_last_error.clear();
+  const char* fn = "indexer_sparse_attend";
+  if (num_rows < 0) return set_err(IDX_EINVAL, "%s: num_rows=%d", fn, num_rows);
+  if (!valid_heads(num_kv_heads))
+    return set_err(IDX_EUNSUPPORTED, "%s: num_kv_heads=%d, supported 1, 2, 4, 8", fn, num_kv_heads);
+  if (!(q_per_kv == 1 || q_per_kv == 2 || q_per_kv == 4 || q_per_kv == 8))
+    return set_err(IDX_EUNSUPPORTED, "%s: q_per_kv=%d, supported 1, 2, 4, 8", fn, q_per_kv);
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return set_err(IDX_EINVAL, "%s: scale must be finite", fn);
+  if (num_rows == 0) return IDX_OK;
+  if (!q || !k_cache || !v_cache || !page_table || !row_req || !row_pos || !topk_ids || !out)
+    return set_err(IDX_EINVAL, "%s: NULL array argument", fn);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return set_err(IDX_EINVAL, "%s: q, k_cache, v_cache and out must be 16-byte aligned", fn);
+  if (num_blocks < 1 || pt_stride < 1 || num_reqs < 1)
+    return set_err(IDX_EINVAL, "%s: num_blocks=%d pt_stride=%d num_reqs=%d", fn, num_blocks, pt_stride, num_reqs);
+  AttendParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.page_table = page_table;
+  p.row_req = row_req;
+  p.row_pos = row_pos;
+  p.ids = topk_ids;
+  p.out = out;
+  p.status = status;
+  p.num_blocks = num_blocks;
+  p.pt_stride = pt_stride;
+  p.num_reqs = num_reqs;
+  p.num_rows = num_rows;
+  p.H = num_kv_heads;
+  p.G = q_per_kv;
+  p.scale = scale;
+  cudaError_t e = launch_attend(p, stream);
   if (e != cudaSuccess) return set_err(IDX_ECUDA, "%s: launch: %s", fn, cudaGetErrorString(e));
   return IDX_OK;
 }

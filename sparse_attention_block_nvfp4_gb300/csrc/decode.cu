@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
   __shared__ int warp_sum[kDecMaxThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t lim = p.wait_ns;                    // limit of every bounded wait
   griddep_launch_dependents();                       // the merge kernel may be scheduled
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
               int issued = 1;
               if (lane == 0) {
                 if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((kq / kQuadSlots) & 1) ^ 1),
-                                        &abort_s)) {
+                                        &abort_s, lim)) {
                   fail();
                   issued = 0;
                 } else {
@@ -412,8 +413,9 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         walk.j = je;
         if (ok && walk.more()) walk.next_request(p);
       }
-      // drain issued copies before the CTA may exit
-      if (!ok && lane < kDecStages && last >= 0)
+      // wait for every copy this warp issued before the CTA may exit: the
+      // readers of a stage stop waiting once another role's wait ran out
+      if (lane < kDecStages && last >= 0)
         mbar_wait(smem_u32(&raw_full[lane]), (uint32_t)((last / kQuadSlots) & 1));
     } else if (warp == 1 || warp == 2) {
       // ================================================= MMA issuers
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         while (walk.more() && !abort_s) {
           const int je = walk.seg_end(p);
           const int qs = sq & 1;
-          if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s)) { fail(); break; }
+          if (!mbar_wait_or_abort(smem_u32(&q_full[qs]), (uint32_t)((sq >> 1) & 1), &abort_s, lim)) { fail(); break; }
           const uint32_t qaddr = sbase + Lay::kQOff + qs * Lay::kQBytes;
           // B (query) descriptors of the 8 K steps of this segment
           uint64_t bd[8];
@@ -442,9 +444,9 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int sl = m + 2 * h;
-              if (!mbar_wait_or_abort(smem_u32(&a_full[sl]), (uint32_t)(kq & 1), &abort_s) ||
+              if (!mbar_wait_or_abort(smem_u32(&a_full[sl]), (uint32_t)(kq & 1), &abort_s, lim) ||
                   !mbar_wait_or_abort(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]), DecD<NQ>::phase(kq) ^ 1u,
-                                      &abort_s)) {
+                                      &abort_s, lim)) {
                 fail();
                 ok = false;
                 break;
@@ -466,9 +468,10 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           ++sq;
           if (walk.more()) walk.next_request(p);
         }
-        // a commit covers every MMA issued before it: drain the last one
-        // before tensor memory is freed
-        if (abort_s && last_bar != 0) mbar_wait(last_bar, last_par);
+        // a commit covers every MMA issued before it: wait for the last one
+        // before tensor memory may be freed (the epilogue stops waiting once
+        // another role's wait ran out)
+        if (last_bar != 0) mbar_wait(last_bar, last_par);
       }
     }
   } else if (warp < 12) {
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
       const int qs = sq & 1;
       // the request's queries -> fp16 B tile (128B swizzle, K-major)
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty[qs]),
-                                                       (uint32_t)(((sq >> 1) & 1) ^ 1), &abort_s))) {
+                                                       (uint32_t)(((sq >> 1) & 1) ^ 1), &abort_s, lim))) {
         fail();
         break;
       }
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         const bool has = q < npq;
         const int st = 4 * (int)(kq % kQuadSlots) + q;  // this warp's stage (see the producer)
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[st]),
-                                                         (uint32_t)((kq / kQuadSlots) & 1), &abort_s))) {
+                                                         (uint32_t)((kq / kQuadSlots) & 1), &abort_s, lim))) {
           fail();
           ok = false;
           break;
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           // A buffer sl is free once the MMAs of quad kq - 1 are done
           if (kq >= 1 &&
               !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[(kq - 1) & 1][sl]),
-                                                           (uint32_t)(((kq - 1) >> 1) & 1), &abort_s))) {
+                                                           (uint32_t)(((kq - 1) >> 1) & 1), &abort_s, lim))) {
             fail();
             ok = false;
             break;
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         for (int sl = 0; sl < kDecSlices; ++sl) {
           if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[kq & 1][sl]),
-                                                             (uint32_t)((kq >> 1) & 1), &abort_s));
+                                                             (uint32_t)((kq >> 1) & 1), &abort_s, lim));
             if (!ok) fail();
           }
           if (ok) {
@@ -664,6 +667,19 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           }
         }
         if (ep == 0 && cf != cl) p.slot_bad[c + r] = bad;
+      } else {
+        // a wait ran out: the scores are incomplete, so the segment's rows
+        // become -1 (a request this CTA finalises) or its slot is flagged
+        // bad, so that the merge writes -1 rows instead of reading
+        // candidates this call never wrote
+        const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+        if (cf == cl && ep < R) {
+          const float zs[kHistK] = {};
+          const int none[kHistK] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+          if (p.cand_out) write_cand_row(p.cand_out + ((int64_t)r * R + ep) * kHistK, zs, none, true);
+          else write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, none, -1, true);
+        }
+        if (ep == 0 && cf != cl) p.slot_bad[c + r] = 1;
       }
       named_bar_sync(2, Roles::kEpThreads);           // lists are read before the next reset
       if (walk.more()) walk.next_request(p);

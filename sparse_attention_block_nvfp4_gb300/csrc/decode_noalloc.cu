@@ -13,13 +13,17 @@
 //
 // Host code may only use the array's symbol as a handle: its device address
 // is looked up with cudaGetSymbolAddress, once per device, by the first call
-// made with that device current, and cached.  Make that first call before
-// any stream capture.
+// made with that device current, and cached (with the device's SM count)
+// for the life of the process.  Make that first call before any stream
+// capture.  The cache does not survive cudaDeviceReset on that device: a
+// process that resets a device must not call this entry point on it again.
 //
 // Every call uses the same array, so two calls whose kernels overlap on the
 // GPU (different streams, or different host threads) corrupt each other's
 // results: serialise them.  Nothing in the array has to start at zero: every
-// word a call reads was written earlier by the same call.
+// word a call reads was written earlier by the same call, and a call whose
+// wait ran out (a GPU that stopped making progress for 2 s) writes -1 rows
+// rather than merging what the array held before.
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -53,11 +57,6 @@ std::mutex g_mu;
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
-
-// Defined in api.cu: lets indexer_last_error() report this file's messages.
-namespace nvfp4idx {
-void set_last_error_text(const char* msg);
-}
 
 extern "C" int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages, int num_blocks,
                                       const int32_t* page_table, int pt_stride, const int32_t* seq_lens,
@@ -95,10 +94,15 @@ extern "C" int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages,
       e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
       if (e != cudaSuccess)
         return ret(IDX_ECUDA, std::string("indexer_decode_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-      int sms = 0;
+      int sms = 0, major = 0, minor = 0;
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
       if (e != cudaSuccess)
         return ret(IDX_ECUDA, std::string("indexer_decode_noalloc: device query: ") + cudaGetErrorString(e));
+      if (major != 10 || minor != 3)
+        return ret(IDX_EUNSUPPORTED, "indexer_decode_noalloc: device is sm_" + std::to_string(major) +
+                                         std::to_string(minor) + ", the kernels are built for sm_103a");
       s.scratch = static_cast<unsigned char*>(ptr);
       s.num_sms = sms;
       s.ready = true;
@@ -142,6 +146,7 @@ extern "C" int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages,
   p.H = num_heads;
   p.R = R;
   p.dbg_stride = 0;
+  p.wait_ns = kWaitLimitNs;
   e = launch_decode(p, grid, stream);
   if (e != cudaSuccess)
     return ret(IDX_ECUDA, std::string("indexer_decode_noalloc: launch: ") + cudaGetErrorString(e));

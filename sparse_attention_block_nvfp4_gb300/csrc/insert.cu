@@ -207,7 +207,8 @@ __device__ __forceinline__ uint32_t norm_rope_encode_group(float (&x)[16], uint3
 // module description).  Per token: RMSNorm over the 128 elements with a bf16
 // weight, RoPE from the caller's cos/sin table at the token's position, the
 // result rounded to bf16, then the NVFP4 quantiser above.  The fp32 steps
-// run in one fixed order so that the rounded keys are reproducible: per
+// run in one fixed order, so the keys are the same from run to run and
+// differ from the exact qk-norm + RoPE by fp32 rounding only: per
 // 16-element group g, running sums e_g / o_g of the even / odd elements'
 // squares (one rounding per step: FFMA), t_g = e_g + o_g, ss = ((t0 + t1) +
 // (t2 + t3)) + ((t4 + t5) + (t6 + t7)); v = ss/128 + eps; rs = 1 / sqrt(v),

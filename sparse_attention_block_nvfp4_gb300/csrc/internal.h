@@ -14,6 +14,7 @@ constexpr int kHistK = 15;        // score-ranked history pages per row
 constexpr int kMaxRows = 64;      // query_len (<= 8) x heads (<= 8) per request
 constexpr int kMaxDecodeReqs = 4096;   // per-request prefix sums live in shared memory
 constexpr int kMaxPrefillReqs = 4096;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // default limit of a bounded wait: 2 s
 
 // index-K page formats
 constexpr int kPagesNvfp4 = 0;    // [num_blocks, 128, 72]: E2M1 codes + E4M3 scales per 16
@@ -45,6 +46,7 @@ struct DecodeParams {
   const int32_t* page_lo;
   const int32_t* page_hi;
   float2* cand_out;            // [rows][15] (score, id); NULL = final rows in out
+  uint64_t wait_ns;            // wall-time limit of each bounded wait
 };
 
 struct PrefillParams {
@@ -63,8 +65,25 @@ struct PrefillParams {
   int32_t* pslot;
   int num_blocks, pt_stride, num_reqs, total_q, H, dbg_stride;
   int page_format;             // kPagesNvfp4 / kPagesMxfp4
+  uint64_t wait_ns;            // wall-time limit of each bounded wait
 };
-constexpr int kPreSlotInts = 20;
+constexpr int kPreSlotInts = 21;
+
+// Block-sparse attention over the selected pages (indexer_sparse_attend).
+struct AttendParams {
+  const uint16_t* q;           // bf16 [num_rows][H * G][128]
+  const uint16_t* k_cache;     // bf16 [num_blocks][128][H][128]
+  const uint16_t* v_cache;     // bf16 [num_blocks][128][H][128]
+  const int32_t* page_table;   // [num_reqs][pt_stride]
+  const int32_t* row_req;      // [num_rows] request of each row
+  const int32_t* row_pos;      // [num_rows] position of each row
+  const int32_t* ids;          // [num_rows][H][16] logical page ids, -1 = none
+  float* out;                  // fp32 [num_rows][H * G][128]
+  int32_t* status;             // nullable
+  int num_blocks, pt_stride, num_reqs, num_rows, H, G;
+  float scale;
+};
+cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream);   // [19 + x]: tile x of the unit failed (a wait ran out)
 
 // Launch `kernel` so that it may be scheduled while the kernel before it on
 // the stream is still running (programmatic dependent launch); the kernel
@@ -84,6 +103,10 @@ cudaError_t launch_dependent(void (*kernel)(Args...), unsigned grid, unsigned bl
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// Error text for entry points defined outside api.cu (read back by
+// indexer_last_error()).
+void set_last_error_text(const char* msg);
 
 cudaError_t launch_insert(const uint16_t* k, const int64_t* slots, int n, uint8_t* pages,
                           int num_blocks, int32_t* status, cudaStream_t stream);

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
   __shared__ int warp_sum[kPreThreads / 32], warp_sum2[kPreThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t lim = p.wait_ns;                    // limit of every bounded wait
   griddep_launch_dependents();                       // the merge kernel may be scheduled
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           for (int j = ja; j < jb; ++j, ++g) {
             const int s = (int)(g % kPreStages);
             if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
-                                    &abort_s)) {
+                                    &abort_s, lim)) {
               fail();
               break;
             }
@@ -396,10 +397,10 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
             }
           }
         }
-        if (abort_s) {   // drain issued copies before the CTA may exit
-          for (int64_t k = (g > kPreStages ? g - kPreStages : 0); k < g; ++k)
-            mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
-        }
+        // wait for every copy issued before the CTA may exit: the readers of
+        // a stage stop waiting once another role's wait ran out
+        for (int64_t k = (g > kPreStages ? g - kPreStages : 0); k < g; ++k)
+          mbar_wait(smem_u32(&raw_full[k % kPreStages]), (uint32_t)((k / kPreStages) & 1));
       }
     } else if (warp == 1 || warp == 2) {
       // ================================================= MMA issuers
@@ -423,13 +424,13 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           sw.get<H>(p, sched, pi, w, ja, jb);
           sw.next(w, pi.L_max);
           if (jb <= ja) continue;                     // no pages of this unit here
-          if (!mbar_wait_or_abort(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s)) { fail(); break; }
+          if (!mbar_wait_or_abort(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s, lim)) { fail(); break; }
           bool ok = true;
           for (int j = ja; j < jb; ++j, ++g) {
             const int b = (int)(g & 1);
             const uint32_t par = (uint32_t)((g >> 1) & 1);
-            if (!mbar_wait_or_abort(smem_u32(&b_full[b]), par, &abort_s) ||
-                !mbar_wait_or_abort(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s)) {
+            if (!mbar_wait_or_abort(smem_u32(&b_full[b]), par, &abort_s, lim) ||
+                !mbar_wait_or_abort(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s, lim)) {
               fail();
               ok = false;
               break;
@@ -450,9 +451,10 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           mma_commit(smem_u32(&q_empty));
           ++ip;
         }
-        // a commit covers every MMA issued before it: drain the last one
-        // before tensor memory is freed
-        if (abort_s && last_bar != 0) mbar_wait(last_bar, last_par);
+        // a commit covers every MMA issued before it: wait for the last one
+        // before tensor memory may be freed (the epilogues stop waiting once
+        // another role's wait ran out)
+        if (last_bar != 0) mbar_wait(last_bar, last_par);
       }
     }
   } else if (warp < 12) {
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         if ((int)(g & 1) != grp) continue;
         const int s = (int)(g % kPreStages);
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
-                                                         (uint32_t)((g / kPreStages) & 1), &abort_s))) {
+                                                         (uint32_t)((g / kPreStages) & 1), &abort_s, lim))) {
           fail();
           ok = false;
           break;
@@ -488,8 +490,8 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         // phase needs this page)
         const uint32_t fpar = (uint32_t)((((g >> 1) - 1)) & 1);
         if (g >= 2 &&
-            !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[0][grp]), fpar, &abort_s) &&
-                                         mbar_wait_or_abort(smem_u32(&d_full[1][grp]), fpar, &abort_s))) {
+            !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[0][grp]), fpar, &abort_s, lim) &&
+                                         mbar_wait_or_abort(smem_u32(&d_full[1][grp]), fpar, &abort_s, lim))) {
           fail();
           ok = false;
           break;
@@ -524,9 +526,10 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
     int64_t g = 0;
     int ip = 0;
     for (PreWalk sw(&rg); sw.more();) {
-      // every warp of the group takes the same decision to stop (a barrier it
-      // skipped would otherwise hold the others)
-      if (named_bar_red_or(bar_id, 128, (!ok || abort_s) ? 1 : 0)) break;
+      // every warp of the group takes the same decision (a barrier it skipped
+      // would otherwise hold the others): once a wait has run out, the walk
+      // goes on without waiting, only to mark the remaining rows as failed
+      if (named_bar_red_or(bar_id, 128, (!ok || abort_s) ? 1 : 0)) ok = false;
       PairInfo pi;
       int w, ja, jb;
       sw.get<H>(p, sched, pi, w, ja, jb);
@@ -540,8 +543,8 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       if (jb > ja) {
         // this tile's queries -> fp16 A tile, once the MMAs of the previous
         // unit are done with it
-        if (ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty),
-                                                                    (uint32_t)((ip - 1) & 1), &abort_s))) {
+        if (ok && ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty),
+                                                                    (uint32_t)((ip - 1) & 1), &abort_s, lim))) {
           fail();
           ok = false;
         }
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         const int b = (int)(g & 1);
         if (!ok) continue;
         if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
-                                                         &abort_s))) {
+                                                         &abort_s, lim))) {
           fail();
           ok = false;
           continue;
@@ -612,17 +615,24 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           if (p.scores_dbg) p.scores_dbg[((int64_t)tr.row0 * H + n) * p.dbg_stride + j] = m;
         }
       }
-      if (!ok) continue;
+      // after a wait ran out the unit's rows are -1: written here, or by the
+      // merge for a unit cut by a CTA boundary (its slot says so, for the
+      // whole tile: the warps' outcomes are combined first)
+      const bool tile_failed = named_bar_red_or(bar_id, 128, ok ? 0 : 1) != 0;
       if (ja == 0 && jb == pi.L_max) {
-        if (n < rows) write_out_row(p.out + ((int64_t)tr.row0 * H + n) * kTopK, top.id, L, tile_bad != 0);
+        if (n < rows)
+          write_out_row(p.out + ((int64_t)tr.row0 * H + n) * kTopK, top.id, L, tile_bad != 0 || !ok);
       } else {
         // cut by a CTA boundary: this CTA's candidates go to its slot of the
         // unit (2c for its first unit, 2c + 1 for its last) and
         // prefill_merge_kernel writes the rows
         const int slot = 2 * c + (u == rg.ua ? 0 : 1);
         float2* dst = p.pcand + (((int64_t)slot * 2 + x) * 128 + n) * kHistK;
+        if (!tile_failed) {
 #pragma unroll
-        for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+          for (int k = 0; k < kHistK; ++k) dst[k] = make_float2(top.s[k], __int_as_float(top.id[k]));
+        }
+        if (n == 0) p.pslot[slot * kPreSlotInts + 19 + x] = tile_failed ? 1 : 0;
         if (x == 0 && n == 0) {
           int32_t* m = p.pslot + slot * kPreSlotInts;
           m[1] = ja;
@@ -708,6 +718,8 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
     if (n >= nt * H) continue;
     float s[kHistK];
     int id[kHistK];
+    // m[19 + x]: tile x's candidates are incomplete (a wait ran out)
+    bool failed = m[19 + x] != 0;
     {
       const float2* own = p.pcand + (((int64_t)slot * 2 + x) * 128 + n) * kHistK;
       for (int k = 0; k < kHistK; ++k) {
@@ -717,11 +729,12 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
     }
     for (int cc = c + 1; cc <= cl && cc < G; ++cc) {
       if (p.pslot[(2 * cc) * kPreSlotInts] != u) continue;   // none of the unit's pages there
-      merge_top15_list(s, id, p.pcand + (((int64_t)(2 * cc) * 2 + x) * 128 + n) * kHistK);
+      if (p.pslot[(2 * cc) * kPreSlotInts + 19 + x]) failed = true;
+      else merge_top15_list(s, id, p.pcand + (((int64_t)(2 * cc) * 2 + x) * 128 + n) * kHistK);
     }
     const int pos = m[5] + t0 + n / H;
     const int Lrow = (pos >= 0 && !m[18]) ? (pos >> 7) : -1;
-    write_out_row(p.out + ((int64_t)row0 * H + n) * kTopK, id, Lrow, m[12] != 0);
+    write_out_row(p.out + ((int64_t)row0 * H + n) * kTopK, id, Lrow, m[12] != 0 || failed);
   }
 }
 

@@ -2,15 +2,15 @@
 // (TMA engine, non-tensor form), tcgen05 tensor-memory alloc / load / store,
 // tcgen05.mma with A in tensor memory, and bounded waits.
 //
-// Every wait here is bounded by wall time (%globaltimer): after
-// kWaitLimitNs it reports failure instead of spinning forever, so a kernel
-// can record a status, drain and return.
+// Every wait here is bounded by wall time (%globaltimer): after a limit
+// (kWaitLimitNs, or the caller's) it reports failure instead of spinning
+// forever, so a kernel can record a status, drain and return.
 #pragma once
 #include <cstdint>
 
-namespace nvfp4idx {
+#include "internal.h"
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+namespace nvfp4idx {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -102,14 +102,16 @@ __device__ __forceinline__ int named_bar_red_or(uint32_t id, uint32_t nthreads, 
 }
 
 // Wait for the phase with the given parity; gives up (false) when *abort
-// becomes non-zero or after the wall-time limit.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort) {
+// becomes non-zero or after `limit_ns` of wall time (the caller's limit,
+// kWaitLimitNs unless the plan set another).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -1,11 +1,15 @@
 """Fused qk-norm + RoPE + NVFP4 insert (nvfp4_insert_norm_rope) against the
-oracle (oracle/norm_rope.py + oracle/nvfp4.py): page bytes bit-exact."""
+oracle (oracle/norm_rope.py + oracle/nvfp4.py): every written row equals
+the NVFP4 quantisation of the float64 qk-norm + RoPE key rounded to bf16,
+except where an element of the key lies within the fp32 error bound of a
+bf16 rounding boundary, where the row of the other neighbour is accepted
+too (``norm_rope.check_rows``; the number of rows that needed it is
+printed).  Rows of skipped tokens keep the cache's old bytes."""
 import numpy as np
 import pytest
 
 import workloads
 from oracle import norm_rope as onr
-from oracle import nvfp4 as onv
 from gpu_util import torch_dev, up
 
 pytestmark = pytest.mark.gpu
@@ -37,6 +41,22 @@ def case(n, seed, max_pos=4096):
     return k, w, pos
 
 
+def assert_rows(got, k, pos, slots, w, eps, table, rd, neox, fill, label):
+    """Rows written for the kept tokens pass the oracle's row check; every
+    other row still holds ``fill``."""
+    keep = onr.kept_tokens(pos, slots, table, rd)
+    flat = got.reshape(-1, 72)
+    rep = onr.check_rows(flat[slots[keep]], k[keep], pos[keep], w, eps, table, rd, neox)
+    print(f"{label}: {rep['rows']} rows, {rep['exact']} exact, {rep['allowance']} within the bf16 "
+          f"boundary allowance, {rep['fails']} failed {rep['fail_rows']}")
+    assert rep["fails"] == 0, rep
+    assert rep["allowance"] <= max(2, rep["rows"] // 1000), rep
+    untouched = np.ones(flat.shape[0], bool)
+    untouched[slots[keep]] = False
+    assert np.all(flat[untouched] == fill)
+    return rep
+
+
 def run_gpu(k, pos, slots, w, eps, table, rd, neox, nb, fill=0):
     import torch
     import sparse_attention_block_nvfp4_gb300 as idx
@@ -49,7 +69,7 @@ def run_gpu(k, pos, slots, w, eps, table, rd, neox, nb, fill=0):
 
 @pytest.mark.parametrize("rd,neox", [(128, True), (64, True), (128, False), (64, False), (40, False),
                                      (32, False), (6, False), (2, False), (0, True)])
-def test_norm_rope_insert_bit_exact(rd, neox):
+def test_norm_rope_insert_matches_oracle(rd, neox):
     n = 20000
     k, w, pos = case(n, 40 + rd + neox)
     nb = (n + 127) // 128 + 3
@@ -58,15 +78,13 @@ def test_norm_rope_insert_bit_exact(rd, neox):
     slots[::11] = -1
     table = rope_table(4096, rd) if rd else None
     got, st = run_gpu(k, pos, slots, w, 1e-6, table, rd, neox, nb, fill=0x5A)
-    want = np.full((nb, 128, 72), 0x5A, np.uint8)
-    onr.insert(k, pos, slots, w, 1e-6, table, rd, neox, want)
     assert st == 0
-    assert np.array_equal(got, want), f"{np.count_nonzero(got != want)} bytes differ"
+    assert_rows(got, k, pos, slots, w, 1e-6, table, rd, neox, 0x5A, f"rd {rd} neox {neox}")
 
 
 def test_norm_rope_insert_eps_and_extremes():
     """Large eps against small keys, zero keys, keys near bf16's range edges,
-    a weight with zeros and negatives: still bit-exact."""
+    a weight with zeros and negatives: still within the oracle's check."""
     rng = np.random.Generator(np.random.PCG64(42))
     n = 512
     x = rng.standard_normal((n, 128)).astype(np.float32)
@@ -83,9 +101,8 @@ def test_norm_rope_insert_eps_and_extremes():
     slots = np.arange(n, dtype=np.int64)
     for eps in (1e-6, 0.5):
         got, st = run_gpu(k, pos, slots, w, eps, table, 128, True, 4)
-        want = onr.insert(k, pos, slots, w, eps, table, 128, True, np.zeros((4, 128, 72), np.uint8))
         assert st == 0
-        assert np.array_equal(got, want), f"eps {eps}: {np.count_nonzero(got != want)} bytes differ"
+        assert_rows(got, k, pos, slots, w, eps, table, 128, True, 0, f"eps {eps}")
 
 
 def test_norm_rope_insert_bad_positions_and_slots():
@@ -100,9 +117,8 @@ def test_norm_rope_insert_bad_positions_and_slots():
     got, st = run_gpu(k, pos, slots, w, 1e-6, table, 128, True, 1, fill=0x77)
     assert st == idx.STATUS_BAD_POSITION | idx.STATUS_BAD_SLOT
     ok = np.array([0, 1, 3, 4, 7])
-    want = np.full((1, 128, 72), 0x77, np.uint8)
-    onr.insert(k[ok], pos[ok], slots[ok], w, 1e-6, table, 128, True, want)
-    assert np.array_equal(got, want)
+    assert np.array_equal(np.nonzero(onr.kept_tokens(pos, np.where(slots < 128, slots, -1), table, 128))[0], ok)
+    assert_rows(got, k[ok], pos[ok], slots[ok], w, 1e-6, table, 128, True, 0x77, "bad positions and slots")
     with pytest.raises(idx.IndexerError) as e:
         run_gpu(k, pos, slots, w, 1e-6, rope_table(64, 96), 96, True, 1)
     assert e.value.code == idx.IDX_EUNSUPPORTED
@@ -124,9 +140,8 @@ def test_norm_rope_insert_full_cache_sampled():
     got, st = run_gpu(w_.k_bf16, pos, w_.slot_mapping, wts, 1e-6, table, 128, True, w_.num_blocks)
     assert st == 0
     pick = rng.choice(pos.size, size=16384, replace=False)
-    rows = np.empty((pick.size, 72), np.uint8)
-    for a in range(0, pick.size, 4096):
-        p = pick[a:a + 4096]
-        kb = onr.norm_rope_bf16(w_.k_bf16[p], pos[p], wts, 1e-6, table, 128, True)
-        rows[a:a + 4096] = onv.quantize_rows(kb)
-    assert np.array_equal(got.reshape(-1, 72)[w_.slot_mapping[pick]], rows)
+    rep = onr.check_rows(got.reshape(-1, 72)[w_.slot_mapping[pick]], w_.k_bf16[pick], pos[pick], wts, 1e-6,
+                         table, 128, True)
+    print(f"full cache, 16384 sampled rows: {rep}")
+    assert rep["fails"] == 0, rep
+    assert rep["allowance"] <= 16, rep

@@ -67,6 +67,67 @@ def test_noalloc_matches_indexer_decode_on_two_calls_in_a_row(lib):
         plan.close()
 
 
+def _call_raw(lib, q, kv, table, seq, num_reqs, query_len, num_heads, out, status):
+    import torch
+    stream = torch.cuda.current_stream()
+    rc = lib.indexer_decode_noalloc(q.data_ptr(), kv.data_ptr(), int(kv.shape[0]), table.data_ptr(),
+                                    int(table.shape[1]), seq.data_ptr(), num_reqs, query_len, num_heads,
+                                    out.data_ptr(), status.data_ptr() if status is not None else None,
+                                    stream.cuda_stream)
+    torch.cuda.synchronize()
+    return rc
+
+
+def test_noalloc_same_layout_new_data_and_null_status(lib):
+    """Two calls with the same shape (so the second reuses exactly the parts
+    of the array the first wrote), the second with other queries and another
+    page table over the same cache, checked against the oracle; then the
+    same call with status NULL."""
+    import torch
+    w = workloads.config(2, small=True)
+    kv = gpu_cache(w)
+    cache = oracle_cache(w)
+    rng = np.random.Generator(np.random.PCG64(78))
+    out = torch.empty((w.num_decode_rows, w.num_heads, 16), dtype=torch.int32, device=torch_dev())
+    status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+    seq = up(w.dec_seq_lens)
+    calls = [(w.q_decode, w.dec_page_table)]
+    table2 = w.dec_page_table.copy()
+    for r in range(table2.shape[0]):                 # another valid table: each row's pages permuted
+        n = int((w.dec_seq_lens[r] + 127) // 128)
+        table2[r, :n] = table2[r, :n][rng.permutation(n)]
+    calls.append((workloads.random_q(w.num_decode_rows, w.num_heads, rng), table2))
+    for q_np, t_np in calls:
+        out.fill_(-77)
+        assert _call_raw(lib, up(q_np), kv, up(t_np), seq, w.num_decode_reqs, w.query_len, w.num_heads, out,
+                         status) == 0, lib.indexer_last_error()
+        assert int(status.item()) == 0
+        ref = oidx.decode(q_np, cache, t_np, w.dec_seq_lens, w.query_len, w.num_heads)
+        assert_ids(out.cpu().numpy(), ref, "same layout, new data")
+    out.fill_(-77)
+    assert _call_raw(lib, up(q_np), kv, up(t_np), seq, w.num_decode_reqs, w.query_len, w.num_heads, out,
+                     None) == 0, lib.indexer_last_error()
+    assert_ids(out.cpu().numpy(), ref, "status NULL")
+
+
+def test_noalloc_bad_page_with_null_status_gives_empty_rows(lib):
+    """An unreadable page id in one request's history: with status NULL the
+    call still returns its rows, -1 for that request, exact for the others."""
+    import torch
+    w = workloads.config(1, small=True)
+    kv = gpu_cache(w)
+    table = w.dec_page_table.copy()
+    table[2, 1] = w.num_blocks + 5                   # request 2 reads past the cache
+    ref = oidx.decode(w.q_decode, oracle_cache(w), table, w.dec_seq_lens, w.query_len, w.num_heads)
+    assert ref.bad[2 * w.query_len]
+    out = torch.full((w.num_decode_rows, w.num_heads, 16), -77, dtype=torch.int32, device=torch_dev())
+    assert _call_raw(lib, up(w.q_decode), kv, up(table), up(w.dec_seq_lens), w.num_decode_reqs, w.query_len,
+                     w.num_heads, out, None) == 0, lib.indexer_last_error()
+    got = out.cpu().numpy()
+    assert np.all(got[2 * w.query_len:3 * w.query_len] == -1)
+    assert_ids(got, ref, "bad page, status NULL")
+
+
 def test_noalloc_rejects_calls_beyond_its_fixed_scratch(lib):
     import torch
     rng = np.random.Generator(np.random.PCG64(77))
