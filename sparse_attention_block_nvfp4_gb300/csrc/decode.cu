@@ -313,17 +313,20 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
   if (tid == 0) {
     for (int s = 0; s < kDecStages; ++s) {
       mbar_init(smem_u32(&raw_full[s]), 1);
-      mbar_init(smem_u32(&raw_empty[s]), 32);   // one dequant warp reads a page
+      mbar_init(smem_u32(&raw_empty[s]), 1);    // one dequant warp reads a page (lane 0 arrives)
     }
+    // one arrival per warp: its lanes synchronise first (__syncwarp), then
+    // lane 0 arrives, which keeps the barrier's shared-memory atomics to one
+    // per warp instead of one per thread
     for (int b = 0; b < kDecSlices; ++b) {
-      mbar_init(smem_u32(&a_full[b]), 128);     // the quad's dequant warpgroup
+      mbar_init(smem_u32(&a_full[b]), 4);       // the quad's dequant warpgroup
       mbar_init(smem_u32(&d_full[0][b]), 1);    // MMA commit
       mbar_init(smem_u32(&d_full[1][b]), 1);
-      mbar_init(smem_u32(&d_empty[0][b]), Roles::kEpThreads); // the epilogue warpgroup(s)
-      mbar_init(smem_u32(&d_empty[1][b]), Roles::kEpThreads);
+      mbar_init(smem_u32(&d_empty[0][b]), Roles::kEpThreads / 32); // the epilogue warpgroup(s)
+      mbar_init(smem_u32(&d_empty[1][b]), Roles::kEpThreads / 32);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&q_full[k]), 256);   // both dequant groups write the tile
+      mbar_init(smem_u32(&q_full[k]), 8);     // both dequant groups write the tile
       mbar_init(smem_u32(&q_empty[k]), 2);    // both MMA issuers commit
     }
     abort_s = 0;
@@ -513,7 +516,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         *reinterpret_cast<uint4*>(qt + (c8 >> 3) * (NQ * 128) + sw128_offset(row, c8 & 7)) = o;
       }
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&q_full[qs]));
+      mbar_arrive_warp(smem_u32(&q_full[qs]));
       for (; walk.j < je && ok; ++kq) {
         const int npq = min(4, je - walk.j);
         walk.j += npq;
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           ok = false;
           break;
         }
-        if (!has) mbar_arrive(smem_u32(&raw_empty[st]));
+        if (!has) mbar_arrive_warp(smem_u32(&raw_empty[st]));
         const uint8_t* const page = base + Lay::kStageOff + st * PF::kPageBytes;
 #pragma unroll 1
         for (int sl = 0; sl < kDecSlices; ++sl) {
@@ -535,7 +538,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           if (has) {
             typename PF::Row row;
             PF::load(page, sl * 32 + lane, row);
-            if (sl == kDecSlices - 1) mbar_arrive(smem_u32(&raw_empty[st]));
+            if (sl == kDecSlices - 1) mbar_arrive_warp(smem_u32(&raw_empty[st]));
 #pragma unroll
             for (int g8 = 0; g8 < 8; ++g8) PF::chunk16(row, g8, a + 8 * g8);
           }
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
             tmem_wait_st();
           }
           tc_fence_before();
-          mbar_arrive(smem_u32(&a_full[sl]));
+          mbar_arrive_warp(smem_u32(&a_full[sl]));
         }
       }
       ++sq;
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
               }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]));
+            mbar_arrive_warp(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]));
           }
         }
         if (ok && has) {
