@@ -53,7 +53,8 @@ KERNEL_SOURCES = ["csrc/prefill.cu", "csrc/decode.cu", "csrc/insert.cu", "csrc/p
 # the files each timed kernel is compiled from (its own .cu and the headers it includes)
 _HEADERS = ["csrc/ptx.cuh", "csrc/codec.cuh", "csrc/topk.cuh", "csrc/internal.h"]
 KERNEL_DEPS = {"prefill": ["csrc/prefill.cu"] + _HEADERS, "decode": ["csrc/decode.cu"] + _HEADERS,
-               "insert": ["csrc/insert.cu", "csrc/codec.cuh", "csrc/internal.h"]}
+               "insert": ["csrc/insert.cu", "csrc/codec.cuh", "csrc/internal.h"],
+               "attend": ["csrc/attend.cu", "csrc/internal.h"]}
 
 
 # ----------------------------------------------------------------------------- host-side logic
@@ -698,9 +699,9 @@ def attend_leg(st, w, dev, flush, stream, reps=20):
     del kc, vc
     return {"bound": "hbm", "ms": med, "achieved": alg / (med / 1e3) / 1e9, "unit": "GB/s",
             "bytes": int(alg), "bytes_gathered_per_unit": int(gathered * per_tok),
-            "units": int(nd * H), "q_per_kv": G,
-            "note": "long_mixed decode rows (16 x 8 queries, 8 KV heads), ids from the step's decode; "
-                    "timed alone, not part of the step"}
+            "units": int(nd * H), "q_per_kv": G, "traffic": recorded_traffic("attend", w.name),
+            "note": f"the decode rows ({w.num_decode_reqs} requests x {w.query_len} queries, {H} KV heads, "
+                    f"one query head each), ids from the step's decode; timed alone, not part of the step"}
 
 
 # ----------------------------------------------------------------------------- main
@@ -776,7 +777,7 @@ def main():
         sweep_args = argparse.Namespace(**vars(args))
         if args.sweep:
             sweep_args.e2e = False
-        sweep_args.attend = args.attend and wname == "long_mixed"
+        sweep_args.attend = args.attend and w.num_decode_reqs > 0
         res = gpu_arm(sweep_args, w, rank, world, local)
         work = res["work"]
         value = work["pages_scored"] * args.steps * world / res["total_s"]
