@@ -14,21 +14,31 @@
 // of K and as much of V (1 MB) for 4 G flops per K/V byte pair: G = 1 is
 // 1 flop per byte, far below the tensor cores' ratio, so the scores and the
 // weighted sums run on the CUDA cores in fp32 (bf16 products are exact).
-// One CTA of 128 threads per unit; per page:
-//   * scores: thread i takes token i (16-byte loads of its K row, the
-//     row's 128-element dot products with the G queries held in shared
-//     memory as fp32);
+// A unit is split over a cluster of 4 CTAs of 128 threads: CTA q takes the
+// unit's pages q, q + 4, ... with its own online softmax, so four pages'
+// loads are in flight per unit and the 4 x units CTAs spread over every SM;
+// the CTAs' states meet in the first CTA's shared memory (distributed
+// shared memory, no global scratch).  Per page, in a CTA:
+//   * scores: thread i takes token i (all sixteen 16-byte loads of its K
+//     row in flight for G = 1, eight or four for larger G, the row's
+//     128-element dot products with the G queries held in shared memory as
+//     fp32);
 //   * online softmax: the page's maximum per head (warp redux + shared
 //     memory), the running maximum M, rescale factor alpha = exp(M_old -
 //     M), weights p_i = exp(s_i - M) (exp2f on log2e-scaled scores);
 //   * weighted sum: warp w takes tokens w, w + 4, ...; lane l holds dims
-//     4l .. 4l + 3 (8-byte loads of the V row, coalesced across the warp),
-//     a fresh per-page partial (at most 32 terms), added to the running
-//     accumulator after its rescale by alpha;
-//   * at the end the 4 warps' accumulators and the per-thread weight sums
-//     are added in shared memory and o = acc / l is written.
-// The longest chain of sequential additions in any sum is 32 + 16 + 4
-// (page partial, pages, warps), scores excepted (128 terms).
+//     4l .. 4l + 3 (8-byte loads of the V row, coalesced across the warp,
+//     eight tokens' loads in flight), a fresh per-page partial (at most 32
+//     terms), added to the running accumulator after its rescale by alpha;
+//   * at the end every CTA stores its maximum, its warps' weight sums and
+//     accumulators into the first CTA, which merges them in a fixed order:
+//     M the largest maximum, each CTA's sums scaled by exp(M_q - M), then
+//     o = acc / l.
+// The longest chain of sequential additions in any sum is 32 + 4 + 4 + 4
+// (page partial, pages of a CTA, warps, CTAs), scores excepted (128 terms);
+// a weight carries at most 5 exponentials (its own, 3 rescalings, its CTA's
+// merge factor).  The two cluster barriers are hardware barriers every
+// thread of the cluster passes unconditionally.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -37,6 +47,7 @@
 
 namespace nvfp4idx {
 
+constexpr int kAttSplit = 4;          // CTAs (a cluster) per unit
 constexpr int kAttThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -54,17 +65,63 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
   return v;
 }
 
+// ------------------------------------------------ cluster (distributed shared memory)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* smem_ptr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(d)
+               : "r"((uint32_t)__cvta_generic_to_shared(smem_ptr)), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Registers grow with G (accumulators, scores): fewer K loads in flight and
+// fewer resident CTAs for the larger groups.
 template <int G>
-__global__ void __launch_bounds__(kAttThreads) sparse_attend_kernel(const AttendParams p) {
-  __shared__ __align__(16) float q_s[G][kDim];      // the unit's queries, scaled by scale * log2e
-  __shared__ float p_s[G][kPage];                   // this page's weights
+struct AttCfg {
+  static constexpr int kKUnroll = G == 1 ? 16 : (G <= 4 ? 8 : 4);
+  static constexpr int kMinBlocks = G == 1 ? 8 : (G == 2 ? 6 : (G == 4 ? 3 : 2));
+  static constexpr int kSmemAcc = kAttSplit * 4 * G * kDim * 4;   // the leader's [CTA][warp][G][kDim]
+};
+
+template <int G>
+__global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads, AttCfg<G>::kMinBlocks)
+    sparse_attend_kernel(const AttendParams p) {
+  extern __shared__ __align__(16) float acc_all[];     // [kAttSplit * 4 warps][G][kDim], used in CTA 0
+  __shared__ __align__(16) float q_s[G][kDim];         // the unit's queries, scaled by scale * log2e
+  __shared__ float p_s[G][kPage];                      // this page's weights
   __shared__ float red_s[4][G];
-  __shared__ __align__(16) float acc_s[4][G][kDim];
+  __shared__ float lq_all[kAttSplit][4][G];            // CTA 0: every warp's weight sum
+  __shared__ float mq_all[kAttSplit][G];               // CTA 0: every CTA's running maximum
   __shared__ int page_s[16];
   __shared__ int npages_s;
+  cluster_arrive_relaxed();                            // this CTA runs: its shared memory may be written
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t unit = blockIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t unit = blockIdx.x / kAttSplit;
   const int t = (int)(unit / p.H), hk = (int)(unit % p.H);
   const int HQ = p.H * G;
   const int r = __ldg(p.row_req + t), pos = __ldg(p.row_pos + t);
@@ -103,7 +160,7 @@ __global__ void __launch_bounds__(kAttThreads) sparse_attend_kernel(const Attend
       }
     }
     npages_s = bad ? 0 : n;
-    if (bad && p.status) atomicOr(p.status, bad);
+    if (bad && p.status && rank == 0) atomicOr(p.status, bad);
   }
   __syncthreads();
   const int npages = npages_s;
@@ -117,7 +174,7 @@ __global__ void __launch_bounds__(kAttThreads) sparse_attend_kernel(const Attend
     for (int c = 0; c < 4; ++c) acc[g][c] = 0.0f;
   }
 
-  for (int pi = 0; pi < npages; ++pi) {
+  for (int pi = (int)rank; pi < npages; pi += kAttSplit) {
     const int j = page_s[pi];
     const int phys = __ldg(p.page_table + (int64_t)r * p.pt_stride + j);
     const int n = min(kPage, pos - j * kPage + 1);                // visible tokens of the page
@@ -130,7 +187,7 @@ __global__ void __launch_bounds__(kAttThreads) sparse_attend_kernel(const Attend
       const uint4* krow = reinterpret_cast<const uint4*>(p.k_cache + (base + (int64_t)tid * p.H) * kDim);
 #pragma unroll
       for (int g = 0; g < G; ++g) s[g] = 0.0f;
-#pragma unroll 4
+#pragma unroll AttCfg<G>::kKUnroll
       for (int c = 0; c < kDim / 8; ++c) {
         const uint4 kv = __ldg(krow + c);
         const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
@@ -176,6 +233,7 @@ __global__ void __launch_bounds__(kAttThreads) sparse_attend_kernel(const Attend
     for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int c = 0; c < 4; ++c) part[g][c] = 0.0f;
+#pragma unroll 8
     for (int i = warp; i < n; i += 4) {
       const uint2 vv = __ldg(reinterpret_cast<const uint2*>(p.v_cache + (base + (int64_t)i * p.H) * kDim) + lane);
       const float v0 = bf16_lo(vv.x), v1 = bf16_hi(vv.x), v2 = bf16_lo(vv.y), v3 = bf16_hi(vv.y);
@@ -195,32 +253,56 @@ __global__ void __launch_bounds__(kAttThreads) sparse_attend_kernel(const Attend
     __syncthreads();                                  // p_s and red_s are rewritten by the next page
   }
 
-  // ---- combine the warps' accumulators and the threads' weight sums
+  // ---- every CTA's state into CTA 0 of the cluster, which merges them
+  cluster_wait_acquire();                             // (the start barrier) every CTA of the cluster runs
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    *reinterpret_cast<float4*>(&acc_s[warp][g][4 * lane]) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+    st_cluster_v4(cluster_map(&acc_all[((rank * 4 + warp) * G + g) * kDim + 4 * lane], 0),
+                  make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]));
     const float lw = warp_sum_f32(l_thr[g]);
-    if (lane == 0) red_s[warp][g] = lw;
+    if (lane == 0) st_cluster_f32(cluster_map(&lq_all[rank][warp][g], 0), lw);
+    if (tid == 0) st_cluster_f32(cluster_map(&mq_all[rank][g], 0), m_run[g]);
   }
-  __syncthreads();
+  cluster_arrive_release();
+  if (rank != 0) return;                              // only CTA 0's shared memory is read from here on
+  cluster_wait_acquire();
   for (int i = tid; i < G * kDim; i += kAttThreads) {
     const int g = i / kDim, d = i % kDim;
-    const float l = (red_s[0][g] + red_s[1][g]) + (red_s[2][g] + red_s[3][g]);
-    const float a = (acc_s[0][g][d] + acc_s[1][g][d]) + (acc_s[2][g][d] + acc_s[3][g][d]);
+    float M = mq_all[0][g];
+#pragma unroll
+    for (int q = 1; q < kAttSplit; ++q) M = fmaxf(M, mq_all[q][g]);
+    float l = 0.0f, a = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kAttSplit; ++q) {
+      const float f = mq_all[q][g] == -CUDART_INF_F ? 0.0f : exp2f(mq_all[q][g] - M);
+      const float lq = (lq_all[q][0][g] + lq_all[q][1][g]) + (lq_all[q][2][g] + lq_all[q][3][g]);
+      const float* aq = acc_all + ((4 * q) * G + g) * kDim + d;     // warp w of CTA q at aq + w * G * kDim
+      const float sq = (aq[0] + aq[G * kDim]) + (aq[2 * G * kDim] + aq[3 * G * kDim]);
+      l = fmaf(f, lq, l);
+      a = fmaf(f, sq, a);
+    }
     p.out[((int64_t)t * HQ + hk * G + g) * kDim + d] = l > 0.0f ? a / l : 0.0f;
   }
+}
+
+template <int G>
+static cudaError_t launch_attend_g(const AttendParams& p, int64_t units, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(sparse_attend_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       AttCfg<G>::kSmemAcc);
+  if (e != cudaSuccess) return e;
+  sparse_attend_kernel<G><<<(unsigned)(units * kAttSplit), kAttThreads, AttCfg<G>::kSmemAcc, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream) {
   const int64_t units = (int64_t)p.num_rows * p.H;
   if (units <= 0) return cudaSuccess;
   switch (p.G) {
-    case 1: sparse_attend_kernel<1><<<(unsigned)units, kAttThreads, 0, stream>>>(p); break;
-    case 2: sparse_attend_kernel<2><<<(unsigned)units, kAttThreads, 0, stream>>>(p); break;
-    case 4: sparse_attend_kernel<4><<<(unsigned)units, kAttThreads, 0, stream>>>(p); break;
-    default: sparse_attend_kernel<8><<<(unsigned)units, kAttThreads, 0, stream>>>(p); break;
+    case 1: return launch_attend_g<1>(p, units, stream);
+    case 2: return launch_attend_g<2>(p, units, stream);
+    case 4: return launch_attend_g<4>(p, units, stream);
+    default: return launch_attend_g<8>(p, units, stream);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace nvfp4idx

@@ -82,6 +82,34 @@ def test_norm_rope_insert_matches_oracle(rd, neox):
     assert_rows(got, k, pos, slots, w, 1e-6, table, rd, neox, 0x5A, f"rd {rd} neox {neox}")
 
 
+@pytest.mark.parametrize("rd,neox", [(64, True), (128, False), (6, False), (0, True)])
+def test_norm_rope_insert_many_blocks(rd, neox):
+    """Some 49 000 keys (many blocks of 64 tokens and a ragged last one),
+    skipped slots and positions past the table: 4096 sampled kept rows
+    checked against the oracle, every other row of the cache untouched."""
+    n = 152 * 32 * 10 + 19
+    k, w, pos = case(n, 60 + rd + neox, max_pos=2048)
+    nb = (n + 127) // 128 + 2
+    rng = np.random.Generator(np.random.PCG64(61))
+    slots = rng.permutation(nb * 128)[:n].astype(np.int64)
+    slots[::13] = -1
+    table = rope_table(2000, rd) if rd else None
+    got, st = run_gpu(k, pos, slots, w, 1e-6, table, rd, neox, nb, fill=0x33)
+    import sparse_attention_block_nvfp4_gb300 as idx
+    assert st == (idx.STATUS_BAD_POSITION if rd else 0)
+    keep = onr.kept_tokens(pos, slots, table, rd)
+    assert 0.9 * n < keep.sum() < n
+    flat = got.reshape(-1, 72)
+    untouched = np.ones(flat.shape[0], bool)
+    untouched[slots[keep]] = False
+    assert np.all(flat[untouched] == 0x33)
+    pick = rng.choice(np.nonzero(keep)[0], size=4096, replace=False)
+    rep = onr.check_rows(flat[slots[pick]], k[pick], pos[pick], w, 1e-6, table, rd, neox)
+    print(f"rd {rd} neox {neox}, 4096 sampled rows: {rep}")
+    assert rep["fails"] == 0, rep
+    assert rep["allowance"] <= 4, rep
+
+
 def test_norm_rope_insert_eps_and_extremes():
     """Large eps against small keys, zero keys, keys near bf16's range edges,
     a weight with zeros and negatives: still within the oracle's check."""
