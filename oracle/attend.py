@@ -40,11 +40,15 @@ def bf16_value(bits) -> np.ndarray:
 def visible_tokens(ids_row, page_table_row, pos: int):
     """(physical block, slot-in-page) of every visible token of the selected
     pages, in id order then position order: ids_row [16] logical page ids
-    (-1 = none), the request's page-table row, the query position."""
+    (-1 = none), the request's page-table row, the query position.  The
+    visible set is the union of the selected pages' visible tokens, so an id
+    listed twice counts once (its first place)."""
     blocks, slots = [], []
+    seen = set()
     for j in np.asarray(ids_row).tolist():
-        if j < 0:
+        if j < 0 or j in seen:
             continue
+        seen.add(j)
         last = min(PAGE - 1, pos - PAGE * j)          # causal cut inside the page
         if last < 0:
             continue

@@ -123,6 +123,32 @@ def pin_id_order_and_skips():
     return None
 
 
+def pin_repeated_id_counts_once():
+    """The visible set is a union of pages: an id listed twice for a row
+    gives the brute force's answer over the set of pages, and the same
+    output as the list with the repeat replaced by -1."""
+    q, kc, vc, table, req, pos, ids, G = _case(8)
+    scale = 128 ** -0.5
+    ids2 = ids.copy()
+    for t in range(ids.shape[0]):
+        for h in range(ids.shape[1]):
+            row = ids[t, h]
+            valid = row[row >= 0]
+            if valid.size >= 2 and (row < 0).any():
+                ids2[t, h, np.nonzero(row < 0)[0][0]] = valid[valid.size // 2]   # a repeat in a free slot
+    if np.array_equal(ids2, ids):
+        return "the case has no row with a free slot for a repeated id"
+    o, _ = oat.attend(q, kc, vc, table, req, pos, ids, G, scale)
+    o2, _ = oat.attend(q, kc, vc, table, req, pos, ids2, G, scale)
+    if np.max(np.abs(o - o2)) > 1e-12:
+        return "a repeated id changed the output"
+    t, hq = 0, 0
+    want = brute.attend_one(q[t, hq], kc, vc, table[req[t]], int(pos[t]), ids2[t, hq // G], hq // G, scale)
+    if np.max(np.abs(o2[t, hq] - np.array(want))) > 1e-12:
+        return "a row with a repeated id differs from the brute force"
+    return None
+
+
 def _fp32_online(q, kc, vc, table, req, pos, ids, G, scale):
     """fp32 evaluation the way a kernel does it: page by page (ids order),
     per page the scores, a running max, rescaling of the accumulators, sums
@@ -171,7 +197,7 @@ def pin_fp32_bound_covers_and_detects_a_dropped_token():
 
 
 PINS = [pin_brute_force, pin_one_visible_token_is_its_v, pin_zero_query_is_mean, pin_causal_cut_and_empty_rows,
-        pin_id_order_and_skips, pin_fp32_bound_covers_and_detects_a_dropped_token]
+        pin_id_order_and_skips, pin_repeated_id_counts_once, pin_fp32_bound_covers_and_detects_a_dropped_token]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -198,6 +224,20 @@ def _visible_first_id_skipped(ids_row, table_row, pos):
     return _orig_visible(r, table_row, pos)
 
 
+def _visible_repeats_counted(ids_row, table_row, pos):
+    # every listed id read, a repeated one twice (a multiset instead of the union)
+    b, s = [], []
+    for j in np.asarray(ids_row).tolist():
+        if j < 0:
+            continue
+        bb, ss = _orig_visible(np.array([j]), table_row, pos)
+        b.append(bb)
+        s.append(ss)
+    if not b:
+        return np.zeros(0, np.int64), np.zeros(0, np.int64)
+    return np.concatenate(b), np.concatenate(s)
+
+
 def _attend_no_scale(q, kc, vc, table, req, pos, ids, G, scale):
     return _orig_attend(q, kc, vc, table, req, pos, ids, G, 1.0)
 
@@ -217,6 +257,7 @@ MUTATIONS = [
      ["pin_brute_force", "pin_one_visible_token_is_its_v"]),
     ("first id skipped", "visible_tokens", _visible_first_id_skipped,
      ["pin_brute_force", "pin_one_visible_token_is_its_v"]),
+    ("repeated id counted twice", "visible_tokens", _visible_repeats_counted, ["pin_repeated_id_counts_once"]),
     ("scale ignored", "attend", _attend_no_scale, ["pin_brute_force"]),
     ("query head grouped with the wrong KV head", "attend", _attend_wrong_head_group, ["pin_brute_force"]),
 ]
