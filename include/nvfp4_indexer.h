@@ -360,8 +360,9 @@ int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages, int num_bl
  * describe the attend; this library reads it as the usual paged sparse
  * attention: per row t and KV head hk (one per index head), query heads
  * hk*G .. hk*G+G-1 attend over the tokens of the pages ids[t][hk][0..15]
- * (-1 skipped) whose position is at most the row's (causal cut inside the
- * local page): o = sum_s softmax_s(scale * q.k_s) v_s, in fp32 (bf16
+ * (-1 skipped; the pages form a set, so an id listed twice counts once)
+ * whose position is at most the row's (causal cut inside the local
+ * page): o = sum_s softmax_s(scale * q.k_s) v_s, in fp32 (bf16
  * products exact, exp2f on log2e-scaled scores, online softmax page by
  * page); a row with no visible token gets o = 0.
  *   q          bf16 [num_rows][num_kv_heads * q_per_kv][128], 16-byte aligned

@@ -117,12 +117,12 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
   __shared__ float mq_all[kAttSplit][G];               // CTA 0: every CTA's running maximum
   __shared__ int page_s[16];
   __shared__ int npages_s;
+  const int64_t unit = blockIdx.x / kAttSplit;
+  const int t = (int)(unit / p.H), hk = (int)(unit % p.H);
   cluster_arrive_relaxed();                            // this CTA runs: its shared memory may be written
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
-  const int64_t unit = blockIdx.x / kAttSplit;
-  const int t = (int)(unit / p.H), hk = (int)(unit % p.H);
   const int HQ = p.H * G;
   const int r = __ldg(p.row_req + t), pos = __ldg(p.row_pos + t);
 
@@ -146,6 +146,9 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
       for (int k = 0; k < 16; ++k) {
         const int j = __ldg(p.ids + ((int64_t)t * p.H + hk) * 16 + k);
         if (j < 0 || (int64_t)j * kPage > pos) continue;
+        bool dup = false;                              // a page is attended once (a set of pages)
+        for (int u = 0; u < n; ++u) dup |= page_s[u] == j;
+        if (dup) continue;
         if (j >= p.pt_stride) {
           bad = kStatusBadTable;
           break;

@@ -167,3 +167,61 @@ def test_attend_long_mixed_decode_rows_sampled():
     got, (q, req, pos, ids) = _run(w, 1, 45, rows=rows, launch_rows=nd)
     o, b, _ = _oracle(w, 1, 45, q, req, pos, ids)
     _assert_close(got, o, b, "long_mixed decode rows, sampled")
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_attend_row_groups_repeats_and_bad_row(G):
+    """Consecutive rows of one request (they share a row-group unit of up to
+    8 / G rows), cut where the request changes and at multiples of 8 / G;
+    ids shuffled, with a repeated id (counted once: a set of pages); then
+    one row of a group with a page outside the cache: that row is zeros with
+    a status bit, the group's other rows still match the oracle."""
+    import torch
+    import sparse_attention_block_nvfp4_gb300 as idx
+    w = workloads.config(1, small=True)
+    H = w.num_heads
+    seq = w.dec_seq_lens.astype(np.int64)
+    req = np.array([1, 1, 1, 1, 1, 0, 0, 1, 1, 1, 3, 3], np.int32)
+    back = np.array([1, 3, 129, 200, 7, 1, 64, 2, 1, 300, 1, 5])
+    pos = (seq[req] - back).astype(np.int32)
+    T = req.size
+    rng = np.random.Generator(np.random.PCG64(77))
+    ids = np.full((T, H, 16), -1, np.int32)
+    for t in range(T):
+        L = int(pos[t]) // 128
+        for h in range(H):
+            hist = rng.permutation(L)[: min(L, 12)]
+            row = list(hist) + [L]
+            if len(row) >= 2:
+                row.append(row[len(row) // 2])              # a repeat
+            row = row + [-1] * (16 - len(row))
+            ids[t, h] = np.array(row, np.int32)[rng.permutation(16)]
+    # page X of request 1: selected by row 2 only (every head), read nowhere else
+    X = int(pos[2]) // 128 - 1
+    for t in range(T):
+        if req[t] == 1 and t != 2:
+            ids[t][ids[t] == X] = -1
+    for h in range(H):
+        if X not in ids[2, h]:
+            ids[2, h, int(np.nonzero(ids[2, h] == -1)[0][0])] = X
+    q = workloads.attend_q(T, H * G, rng)
+    kc = workloads.attend_kv_fill(78, 0, w.num_blocks, H, torch_dev())
+    vc = workloads.attend_kv_fill(78, 1, w.num_blocks, H, torch_dev())
+    status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+
+    def call(table):
+        status.zero_()
+        return idx.sparse_attend(up(q.view(np.int16)), kc, vc, up(table), up(req), up(pos), up(ids), SCALE,
+                                 status=status).cpu().numpy().astype(np.float64)
+
+    out = call(w.page_table)
+    assert int(status.item()) == 0
+    o, b, _ = _oracle(w, G, 78, q, req, pos, ids)
+    _assert_close(out, o, b, f"row groups G={G}")
+    table = w.page_table.copy()
+    table[1, X] = w.num_blocks + 3
+    out_bad = call(table)
+    assert int(status.item()) == idx.STATUS_BAD_PAGE
+    assert np.all(out_bad[2] == 0)
+    keep = np.arange(T) != 2
+    _assert_close(out_bad[keep], o[keep], b[keep], f"row groups G={G}, one bad row")
