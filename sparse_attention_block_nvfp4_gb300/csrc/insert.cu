@@ -45,6 +45,20 @@ __global__ void __launch_bounds__(256) nvfp4_insert_kernel(const uint16_t* __res
   const int64_t tok = tid >> 2;
   const int j = (int)(tid & 3);
   const bool live = tok < n;
+  // the key's quarter and the slot load independently (one memory latency,
+  // not two); a skipped token's key is read and dropped
+  uint32_t w[16];
+  if (live) {
+    const uint4* src = reinterpret_cast<const uint4*>(k + tok * 128 + j * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(src + i);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+  }
   int64_t slot = live ? __ldg(slots + tok) : -1;
   if (slot >= num_slots) {
     if (j == 0 && status) atomicOr(status, (int32_t)kStatusBadSlot);
@@ -54,16 +68,6 @@ __global__ void __launch_bounds__(256) nvfp4_insert_kernel(const uint16_t* __res
   uint32_t sc2 = 0;                  // scale bytes 2j (low) and 2j + 1
   uint32_t cw[4] = {0, 0, 0, 0};     // codes of elements 32j .. 32j + 31
   if (slot >= 0) {
-    const uint4* src = reinterpret_cast<const uint4*>(k + tok * 128 + j * 32);
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldg(src + i);
-      w[4 * i] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
-    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {   // group 2j + h, widened to fp32 only now
       uint32_t m = w[8 * h];
@@ -375,16 +379,9 @@ __global__ void __launch_bounds__(256) mxfp4_insert_kernel(const uint16_t* __res
   const int j = (int)(tid & 3);
   const unsigned lane = threadIdx.x & 31u;
   const bool live = tok < n;
-  int64_t slot = live ? __ldg(slots + tok) : -1;
-  if (slot >= num_slots) {
-    if (j == 0 && status) atomicOr(status, (int32_t)kStatusBadSlot);
-    slot = -1;
-  }
-  uint32_t scale_byte = 0;
-  uint32_t cw[4] = {0, 0, 0, 0};
-  if (slot >= 0) {
+  uint32_t w[16];                    // loaded independently of the slot, as in the NVFP4 insert
+  if (live) {
     const uint4* src = reinterpret_cast<const uint4*>(k + tok * 128 + j * 32);
-    uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint4 v = __ldg(src + i);
@@ -393,6 +390,15 @@ __global__ void __launch_bounds__(256) mxfp4_insert_kernel(const uint16_t* __res
       w[4 * i + 2] = v.z;
       w[4 * i + 3] = v.w;
     }
+  }
+  int64_t slot = live ? __ldg(slots + tok) : -1;
+  if (slot >= num_slots) {
+    if (j == 0 && status) atomicOr(status, (int32_t)kStatusBadSlot);
+    slot = -1;
+  }
+  uint32_t scale_byte = 0;
+  uint32_t cw[4] = {0, 0, 0, 0};
+  if (slot >= 0) {
     uint32_t m = w[0];
 #pragma unroll
     for (int i = 1; i < 16; ++i) m = bf16x2_max_abs(m, w[i]);
