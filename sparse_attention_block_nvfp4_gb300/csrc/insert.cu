@@ -148,14 +148,10 @@ __device__ __forceinline__ float norm_rope_sumsq(float tA, float tB) {
   }
 }
 
-// One 16-element group of a token: load (bf16 -> fp32), the group sum of
-// squares t = e + o (even / odd running sums, one rounding per step).
-__device__ __forceinline__ float norm_rope_load_group(const uint16_t* kg, bool act, float (&x)[16]) {
-  uint4 v[2] = {};
-  if (act) {
-    v[0] = __ldg(reinterpret_cast<const uint4*>(kg));
-    v[1] = __ldg(reinterpret_cast<const uint4*>(kg) + 1);
-  }
+// One 16-element group of a token (two 16-byte words of bf16, loaded at
+// entry) widened to fp32, and the group sum of squares t = e + o (even / odd
+// running sums, one rounding per step).
+__device__ __forceinline__ float norm_rope_widen_group(const uint4 (&v)[2], float (&x)[16]) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -222,7 +218,8 @@ __device__ __forceinline__ uint32_t norm_rope_encode_group(float (&x)[16], uint3
 // NeoX pair (i, i + rd/2) sits in one thread (rd 64 or 128); GPT-J pairs
 // (2i, 2i + 1) stay inside a thread anyway.  At entry each thread starts an
 // asynchronous copy of its 16 cosines and 16 sines into shared memory, so the
-// table's latency hides behind the key loads and the norm.  HBM-bound: 256 B
+// table's latency hides behind the norm; the key loads are issued first,
+// independently of the slot and the position.  HBM-bound: 256 B
 // key + 8 B slot + 8 B position + 72 B row per token, plus the table rows.
 template <int kMode>
 __global__ void __launch_bounds__(256) nvfp4_insert_norm_rope_kernel(const NormRopeArgs a) {
@@ -233,22 +230,30 @@ __global__ void __launch_bounds__(256) nvfp4_insert_norm_rope_kernel(const NormR
   const int64_t tok = tid >> 2;
   const int j = (int)(tid & 3);
   const bool live = tok < a.n;
+  int gA, gB;
+  norm_rope_groups<kMode>(j, gA, gB);
+  // the key's two groups, the slot and the position load independently (a
+  // skipped token's key is read and dropped)
+  uint4 ka[2] = {}, kb[2] = {};
+  if (live) {
+    const uint4* kt = reinterpret_cast<const uint4*>(a.k + tok * 128);
+    ka[0] = __ldg(kt + 2 * gA);
+    ka[1] = __ldg(kt + 2 * gA + 1);
+    kb[0] = __ldg(kt + 2 * gB);
+    kb[1] = __ldg(kt + 2 * gB + 1);
+  }
   int64_t slot = live ? __ldg(a.slots + tok) : -1;
+  int64_t pos = (kMode != kNormOnly && live) ? __ldg(a.positions + tok) : 0;
   if (slot >= a.num_slots) {
     if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadSlot);
     slot = -1;
   }
-  int64_t pos = 0;
-  if (kMode != kNormOnly && slot >= 0) {
-    pos = __ldg(a.positions + tok);
-    if (pos < 0 || pos >= a.max_pos) {
-      if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadPosition);
-      slot = -1;
-    }
+  if (kMode != kNormOnly && slot >= 0 && (pos < 0 || pos >= a.max_pos)) {
+    if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadPosition);
+    slot = -1;
   }
+  if (slot < 0) pos = 0;                           // the table is read only for a kept token
   const bool act = slot >= 0;
-  int gA, gB;
-  norm_rope_groups<kMode>(j, gA, gB);
 
   // table slice: pairs p0 .. p0 + 15 (those below rd/2), cosines and sines
   const int h = a.rotary_dim >> 1, p0 = 16 * j;
@@ -269,9 +274,8 @@ __global__ void __launch_bounds__(256) nvfp4_insert_norm_rope_kernel(const NormR
   cp_async_commit();
 
   float xa[16], xb[16];
-  const uint16_t* kt = a.k + tok * 128;
-  const float tA = norm_rope_load_group(kt + 16 * gA, act, xa);
-  const float tB = norm_rope_load_group(kt + 16 * gB, act, xb);
+  const float tA = norm_rope_widen_group(ka, xa);
+  const float tB = norm_rope_widen_group(kb, xb);
   const float ss = norm_rope_sumsq<kMode>(tA, tB);
   const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
   norm_rope_scale_group(a.weight + 16 * gA, rs, xa);
