@@ -136,34 +136,37 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
     q_s[g][2 * d2] = bf16_lo(w) * qscale;
     q_s[g][2 * d2 + 1] = bf16_hi(w) * qscale;
   }
-  // ---- the selected pages with visible tokens, in id order; an unreadable
-  // one (outside the page table or the cache) empties the unit's output
-  if (tid == 0) {
-    int n = 0, bad = 0;
-    if (r < 0 || r >= p.num_reqs) {
-      bad = kStatusBadTable;
-    } else {
-      for (int k = 0; k < 16; ++k) {
-        const int j = __ldg(p.ids + ((int64_t)t * p.H + hk) * 16 + k);
-        if (j < 0 || (int64_t)j * kPage > pos) continue;
-        bool dup = false;                              // a page is attended once (a set of pages)
-        for (int u = 0; u < n; ++u) dup |= page_s[u] == j;
-        if (dup) continue;
+  // ---- the selected pages with visible tokens, in id order (a repeated id
+  // once, at its first place); an unreadable one (outside the page table or
+  // the cache) empties the unit's output.  Lanes 0..15 of warp 0 take one id
+  // each, so the id and page-table loads of the 16 ids are in flight together.
+  if (warp == 0) {
+    const bool req_ok = r >= 0 && r < p.num_reqs;
+    int j = -1, bad = 0;
+    bool vis = false;
+    if (lane < 16 && req_ok) {
+      j = __ldg(p.ids + ((int64_t)t * p.H + hk) * 16 + lane);
+      vis = j >= 0 && (int64_t)j * kPage <= pos;
+      if (vis) {
         if (j >= p.pt_stride) {
           bad = kStatusBadTable;
-          break;
+        } else {
+          const int phys = __ldg(p.page_table + (int64_t)r * p.pt_stride + j);
+          if (phys < 0 || phys >= p.num_blocks) bad = kStatusBadPage;
         }
-        const int phys = __ldg(p.page_table + (int64_t)r * p.pt_stride + j);
-        if (phys < 0 || phys >= p.num_blocks) {
-          bad = kStatusBadPage;
-          break;
-        }
-        page_s[n] = j;
-        ++n;
       }
     }
-    npages_s = bad ? 0 : n;
-    if (bad && p.status && rank == 0) atomicOr(p.status, bad);
+    if (lane == 0 && !req_ok) bad = kStatusBadTable;
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    // equal visible ids: only the lowest lane's is kept
+    const uint32_t same = __match_any_sync(0xffffffffu, vis ? j : -1 - lane);
+    const bool keep = vis && (same & ((1u << lane) - 1u)) == 0;
+    const uint32_t kept = __ballot_sync(0xffffffffu, keep);
+    if (keep) page_s[__popc(kept & ((1u << lane) - 1u))] = j;
+    if (lane == 0) {
+      npages_s = bad ? 0 : __popc(kept);
+      if (bad && p.status && rank == 0) atomicOr(p.status, bad);
+    }
   }
   __syncthreads();
   const int npages = npages_s;
