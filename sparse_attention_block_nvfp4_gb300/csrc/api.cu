@@ -2,6 +2,7 @@
 // object and its device scratch, launches on the caller's stream.
 #include <cmath>
 #include <cstdarg>
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <string>
@@ -48,8 +49,8 @@ struct indexer_plan_s {
   int max_prefill_tokens = 0, max_prefill_reqs = 0;
   int decode_grid = 0;
   uint64_t wait_ns = kWaitLimitNs;   // limit of each bounded wait inside the kernels
-  float2* cand = nullptr;      // [(decode_grid + max_reqs)][<= 64 rows][15]
-  int32_t* slot_bad = nullptr; // [decode_grid + max_reqs]
+  float2* cand = nullptr;      // [(split units + max_reqs) slots][R rows][15]
+  int32_t* slot_bad = nullptr; // [16 * decode_grid + max_reqs]
   int2* req_info = nullptr;    // [max_reqs]
   int32_t* status = nullptr;   // 1 word
   float2* pcand = nullptr;     // [2 * num_sms][2][128][15]: prefill units cut by a CTA boundary
@@ -231,13 +232,17 @@ int indexer_plan(indexer_plan_t* plan, int num_heads, int max_reqs, int max_quer
   pl->max_prefill_tokens = max_prefill_tokens;
   pl->max_prefill_reqs = max_prefill_reqs;
   pl->decode_grid = pl->num_sms;   // one decode CTA per SM
+  // candidate slots = split units + requests: CTAs of the quad kernel (up to
+  // 64 rows each), or warps of the small-row kernel (up to 8 rows each)
   const size_t slots = (size_t)pl->decode_grid + (size_t)max_reqs;
-  e = cudaMalloc(&pl->cand, slots * kMaxRows * kHistK * sizeof(float2));
-  if (e == cudaSuccess) e = cudaMalloc(&pl->slot_bad, slots * sizeof(int32_t));
+  const size_t bad_slots = (size_t)decode_split_units(1, kPagesNvfp4, pl->decode_grid) + (size_t)max_reqs;
+  const size_t cand_rows = std::max(slots * kMaxRows, bad_slots * 8);
+  e = cudaMalloc(&pl->cand, cand_rows * kHistK * sizeof(float2));
+  if (e == cudaSuccess) e = cudaMalloc(&pl->slot_bad, bad_slots * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&pl->req_info, (size_t)(max_reqs > 0 ? max_reqs : 1) * sizeof(int2));
   if (e == cudaSuccess) e = cudaMalloc(&pl->status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(pl->status, 0, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMemset(pl->slot_bad, 0, slots * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(pl->slot_bad, 0, bad_slots * sizeof(int32_t));
   if (e == cudaSuccess)
     e = cudaMalloc(&pl->pcand, (size_t)2 * pl->num_sms * 2 * 128 * kHistK * sizeof(float2));
   if (e == cudaSuccess) e = cudaMalloc(&pl->pslot, (size_t)2 * pl->num_sms * kPreSlotInts * sizeof(int32_t));

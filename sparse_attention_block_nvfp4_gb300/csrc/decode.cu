@@ -699,11 +699,15 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
 
 // One warp per (request, row): merge the per-segment top-15 lists of split
 // requests; write rows of requests with no history page or an unreadable one.
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+// Lane k holds lists k and k + 32 (up to 64 segments; beyond that each of
+// the two is the top-15 of lists k, k + 64, ... / k + 32, k + 96, ...), and
+// 15 warp-wide rounds take the best head (score desc, id asc) of all of them.
+constexpr int kMergeWarps = 4;
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
   griddep_wait();                                    // the scoring grid's candidates are written
-  __shared__ float2 lists[8][32][kHistK];
+  __shared__ float2 lists[kMergeWarps][64][kHistK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t)blockIdx.x * 8 + warp;
+  const int64_t gw = (int64_t)blockIdx.x * kMergeWarps + warp;
   if (gw >= (int64_t)p.num_reqs * p.R) return;
   const int r = (int)(gw / p.R), n = (int)(gw % p.R);
   const int seq = __ldg(p.seq_lens + r);
@@ -739,46 +743,55 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     if (lane == 0) finish(zs, none, true);
     return;
   }
-  // lane-local sorted list: list `lane` when nseg <= 32, else a top-15 of
-  // lists lane, lane+32, ... (visited in ascending page order)
-  float2(&mine)[kHistK] = lists[warp][lane];
-  if (nseg <= 32) {
-    if (lane < nseg) {
-      const float2* src = p.cand + ((int64_t)(slot0 + lane) * p.R + n) * kHistK;
 #pragma unroll
-      for (int k = 0; k < kHistK; ++k) mine[k] = src[k];
+  for (int hh = 0; hh < 2; ++hh) {
+    const int li = lane + 32 * hh;
+    float2(&mine)[kHistK] = lists[warp][li];
+    if (nseg <= 64) {
+      if (li < nseg) {
+        const float2* src = p.cand + ((int64_t)(slot0 + li) * p.R + n) * kHistK;
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) mine[k] = src[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(0.0f, __int_as_float(-1));
+      }
     } else {
+      // lists li, li + 64, ... cover ascending page ranges: inserted in that
+      // order, an equal score always comes with a higher id
+      TopK15 t;
+      t.reset();
+      for (int k = li; k < nseg; k += 64) {
+        const float2* src = p.cand + ((int64_t)(slot0 + k) * p.R + n) * kHistK;
+        float2 e[kHistK];
 #pragma unroll
-      for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(0.0f, __int_as_float(-1));
+        for (int i = 0; i < kHistK; ++i) e[i] = src[i];
+#pragma unroll
+        for (int i = 0; i < kHistK; ++i)
+          if (__float_as_int(e[i].y) >= 0) t.insert(e[i].x, __float_as_int(e[i].y));
+      }
+#pragma unroll
+      for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(t.s[k], __int_as_float(t.id[k]));
     }
-  } else {
-    TopK15 t;
-    t.reset();
-    for (int k = lane; k < nseg; k += 32) {
-      const float2* src = p.cand + ((int64_t)(slot0 + k) * p.R + n) * kHistK;
-      float2 e[kHistK];
-#pragma unroll
-      for (int i = 0; i < kHistK; ++i) e[i] = src[i];
-#pragma unroll
-      for (int i = 0; i < kHistK; ++i)
-        if (__float_as_int(e[i].y) >= 0) t.insert(e[i].x, __float_as_int(e[i].y));
-    }
-#pragma unroll
-    for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(t.s[k], __int_as_float(t.id[k]));
   }
   __syncwarp();
   int res[kHistK];
   float rs[kHistK];
-  int cur = 0;
+  int h0 = 0, h1 = 0;                         // heads of lists lane and lane + 32
 #pragma unroll
   for (int k = 0; k < kHistK; ++k) {
-    float2 e = make_float2(0.0f, __int_as_float(-1));
-    if (cur < kHistK) e = lists[warp][lane][cur];
-    const int id = __float_as_int(e.y);
-    const uint32_t key = id >= 0 ? order_key(e.x) : 0u;
+    const float2 e0 = h0 < kHistK ? lists[warp][lane][h0] : make_float2(0.0f, __int_as_float(-1));
+    const float2 e1 = h1 < kHistK ? lists[warp][lane + 32][h1] : make_float2(0.0f, __int_as_float(-1));
+    const int id0 = __float_as_int(e0.y), id1 = __float_as_int(e1.y);
+    const uint32_t k0 = id0 >= 0 ? order_key(e0.x) : 0u, k1 = id1 >= 0 ? order_key(e1.x) : 0u;
+    const bool take1 = k1 > k0 || (k1 == k0 && k1 != 0u && id1 < id0);
+    const uint32_t key = take1 ? k1 : k0;
+    const int id = take1 ? id1 : id0;
     const uint32_t kmax = warp_max_u32(key);
     const uint32_t idmin = warp_min_u32(key == kmax && kmax != 0u ? (uint32_t)id : 0xFFFFFFFFu);
-    if (kmax != 0u && key == kmax && (uint32_t)id == idmin) ++cur;
+    if (kmax != 0u && key == kmax && (uint32_t)id == idmin) {
+      if (take1) ++h1; else ++h0;
+    }
     res[k] = kmax != 0u ? (int)idmin : -1;
     rs[k] = kmax != 0u ? key_to_float(kmax) : 0.0f;
   }
@@ -847,6 +860,308 @@ cudaError_t launch_cp_merge(const float2* cand_all, int world, int num_reqs, int
   return cudaGetLastError();
 }
 
+// ============================================================ small-R decode
+// Requests of at most 8 rows (query_len x heads <= 8: decode_batch's 4, a
+// single query of 1..8 heads) on NVFP4 pages.  The quad kernel above pays a
+// chain of tensor-memory hand-offs per slice whatever the row count; here
+// the contraction is small enough for the warp-level mma.sync tensor path
+// (m16n8k16, f16 operands, f32 accumulation: the same exact products and
+// fp32 sums), so every warp streams its own pages with no hand-off at all.
+//   * the split unit is a warp: the T history pages are cut into G = min(16 x
+//     grid, T) contiguous ranges, warp u of the grid takes range u, walks it
+//     as segments (one per request) and keeps each row's top-15 in lane n
+//     (n < R); a request inside one range is finalised by its warp, the
+//     others leave 15 candidates per row in slot u + r for the merge kernel
+//     (the same slots, request info and merge as the quad kernel, with warps
+//     in place of CTAs), so no barrier joins the warps of a CTA;
+//   * half pages (64 tokens) go through a 2-stage ring per warp (bulk
+//     copies; lane 0 issues the copy of the half after next as soon as a
+//     stage is read), 16 warps per CTA;
+//   * per page 8 token tiles x 8 K steps of mma.sync, M = 16 tokens, N = 8
+//     query rows (row n in lane group n, rows >= R zero), K = 16 dimensions
+//     = one NVFP4 group: lane (g, c) dequantises its A fragment straight
+//     from the raw page, the two code bytes 8kk + 2c, 8kk + 2c + 1 of tokens
+//     g and g + 8 times the group's E4M3 scale (exact in f16).  The K order
+//     inside a group is permuted alike for A and the query fragment B
+//     (fragment columns 2c, 2c+1, 2c+8, 2c+9 <- dimensions 4c .. 4c+3), which
+//     leaves every dot product unchanged;
+//   * the row maxima over the 128 tokens: per lane over its two tokens of
+//     each tile, then over the 8 lane groups by shuffles.
+// Every wait is bounded; a wait that runs out gives the quad kernel's
+// failure rows (-1 rows or a bad slot) and the copies in flight are drained.
+constexpr int kSmWarps = 16, kSmStages = 2, kSmRows = 8;
+constexpr uint32_t kSmHalf = 64 * 72;                 // a stage holds 64 tokens (half a page)
+constexpr uint32_t kSmPageOff = 0;
+constexpr uint32_t kSmPreOff = kSmWarps * kSmStages * kSmHalf;
+static_assert(kSmPreOff + (kMaxDecodeReqs + 1) * 4 + 128 <= 227 * 1024, "small decode shared memory");
+
+// Bytes 0 and 1 of w (two E2M1 codes each, low nibble first) -> two f16x2.
+__device__ __forceinline__ void e2m1x4_lo2_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+__device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Split units of the decode launch: CTAs of the quad kernel, or warps of the
+// small-row kernel (the candidate slots are indexed by unit + request).
+int decode_split_units(int R, int page_format, int grid) {
+  return (page_format != kPagesMxfp4 && R <= kSmRows) ? grid * kSmWarps : grid;
+}
+
+__global__ void __launch_bounds__(kSmWarps * 32, 1) decode_small_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t pg_full[kSmWarps][kSmStages];
+  __shared__ volatile int abort_s;
+  __shared__ int warp_sum[kSmWarps];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lg = lane >> 2, lc = lane & 3;            // mma fragment lane group / index in group
+  const uint64_t lim = p.wait_ns;
+  griddep_launch_dependents();                       // the merge kernel may be scheduled
+  uint8_t* const base = sm_raw + ((128u - (smem_u32(sm_raw) & 127u)) & 127u);
+  int32_t* const pre = reinterpret_cast<int32_t*>(base + kSmPreOff);
+  const int NR = p.num_reqs, R = p.R;
+  constexpr int kThreads = kSmWarps * 32;
+
+  // ---- history pages per request -> exclusive prefix sums in smem
+  {
+    const int per = (NR + kThreads - 1) / kThreads;
+    const int r0 = tid * per, r1 = min(NR, r0 + per);
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) sum += req_pages(p, r);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int off = 0;
+    for (int w = 0; w < warp; ++w) off += warp_sum[w];
+    int run = off + incl - sum;
+    for (int r = r0; r < r1; ++r) {
+      pre[r] = run;
+      run += req_pages(p, r);
+    }
+    if (tid == kThreads - 1) {
+      int tot = 0;
+      for (int w = 0; w < kSmWarps; ++w) tot += warp_sum[w];
+      pre[NR] = tot;
+    }
+    if (tid == 0) {
+      for (int w = 0; w < kSmWarps; ++w)
+        for (int st = 0; st < kSmStages; ++st) mbar_init(smem_u32(&pg_full[w][st]), 1);
+      abort_s = 0;
+      fence_mbar_init();
+    }
+    __syncthreads();
+  }
+  const int64_t T = pre[NR];
+  const int G = (int)min((int64_t)gridDim.x * kSmWarps, T);
+  if (blockIdx.x == 0) {
+    for (int r = tid; r < NR; r += kThreads) {
+      const int h = pre[r + 1] - pre[r];
+      int2 info = make_int2(0, 0);
+      if (h > 0) {
+        const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+        info = make_int2(cf, cl - cf + 1);
+      }
+      p.req_info[r] = info;
+    }
+  }
+  const int u = blockIdx.x * kSmWarps + warp;        // this warp's split unit
+  if (u >= G) return;
+  const int64_t x0 = (int64_t)u * T / G, x1 = (int64_t)(u + 1) * T / G;
+
+  int r_start;
+  {
+    int lo = 0, hi = NR - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= x0) lo = mid; else hi = mid - 1;
+    }
+    r_start = lo;
+    while (pre[r_start + 1] - pre[r_start] == 0) ++r_start;
+  }
+  SegWalk walk{pre, NR, x1 - x0, 0, r_start, req_lo(p, r_start) + (int)(x0 - pre[r_start])};
+  uint8_t* const ring = base + kSmPageOff + (uint32_t)warp * kSmStages * kSmHalf;
+  int64_t kw = 0;                                    // pages of this warp so far (ring position)
+  int64_t last_k[kSmStages] = {-1, -1};              // the last page issued into each stage
+  bool ok = true;                                    // uniform within the warp
+
+  while (walk.more()) {
+    const int je = walk.seg_end(p);
+    const int r = walk.r, js = walk.j;
+    const int seq_r = __ldg(p.seq_lens + r);
+    const int32_t* const pt_row = p.page_table + (int64_t)r * p.pt_stride;
+    const int npw = je - js;                          // this segment's pages, all this warp's
+    const int nh = 2 * npw;                           // and their halves: half h of page i is item 2i + h
+    const int64_t k0 = kw;
+    // the copy of item x (page js + x / 2, tokens 64 (x % 2) ..) into stage
+    // (k0 + x) % 2; false: unreadable page
+    auto issue = [&](int x) {
+      const int64_t k = k0 + x;
+      const int st = (int)(k & 1);
+      int phys = 0;
+      if (lane == 0) phys = __ldg(pt_row + js + (x >> 1));
+      phys = __shfl_sync(0xffffffffu, phys, 0);
+      const bool good = phys >= 0 && phys < p.num_blocks;
+      if (lane == 0) {
+        const uint32_t fb = smem_u32(&pg_full[warp][st]);
+        if (good) {
+          mbar_arrive_expect_tx(fb, kSmHalf);
+          bulk_g2s(smem_u32(ring + st * kSmHalf), p.kv + (int64_t)phys * 9216 + (x & 1) * kSmHalf, kSmHalf, fb);
+        } else {
+          if (!(x & 1)) atomicOr(p.status, kStatusBadPage);
+          mbar_arrive(fb);                           // nothing to copy: the stage's phase completes empty
+        }
+      }
+      last_k[st] = k;
+      return good;
+    };
+    bool good0 = true, good1 = true;                 // the item in stage 0 / 1 was readable
+    for (int x = 0; ok && x < nh && x < kSmStages; ++x) {
+      const bool gd = issue(x);
+      if ((k0 + x) & 1) good1 = gd; else good0 = gd;
+    }
+    // the request's queries as mma B fragments: row n = lg, dimensions
+    // 16kk + 4lc .. 16kk + 4lc + 3 (rows >= R zero)
+    uint32_t bq[8][2];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t w4 = 0;
+      if (lg < R) w4 = __ldg(reinterpret_cast<const uint32_t*>(p.q + ((int64_t)r * R + lg) * 128 + 16 * kk + 4 * lc));
+      bq[kk][0] = e4m3x2_to_f16x2(w4 & 0xFFFFu);
+      bq[kk][1] = e4m3x2_to_f16x2(w4 >> 16);
+    }
+    const int pos = seq_r - p.qlen + lane / p.H;       // row `lane` (lanes < R)
+    const int L = pos >= 0 ? (pos >> 7) : -1;
+    TopK15 top;
+    top.reset();
+    int seg_bad = 0;
+    float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;  // rows 2lc, 2lc + 1, over the page's items so far
+    for (int x = 0; x < nh; ++x) {
+      const int64_t k = k0 + x;
+      const int st = (int)(k & 1);
+      const int j = js + (x >> 1);
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&pg_full[warp][st]), (uint32_t)((k >> 1) & 1),
+                                                        &abort_s, lim));
+        if (!ok && lane == 0 && !abort_s) {
+          abort_s = 1;
+          atomicOr(p.status, kStatusTimeout);
+        }
+      }
+      const bool good = st ? good1 : good0;
+      seg_bad |= good ? 0 : 1;
+      if (ok && good) {
+        const uint8_t* const pg = ring + st * kSmHalf;
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+          const uint8_t* const t0 = pg + (16 * mt + lg) * 72;
+          const uint8_t* const t1 = t0 + 8 * 72;
+          // the two tokens' 8 scales, f16x2 pairs {group 2i, group 2i + 1}
+          const uint2 sa = *reinterpret_cast<const uint2*>(t0 + 64);
+          const uint2 sb = *reinterpret_cast<const uint2*>(t1 + 64);
+          const uint32_t sca[4] = {e4m3x2_to_f16x2(sa.x & 0xFFFFu), e4m3x2_to_f16x2(sa.x >> 16),
+                                   e4m3x2_to_f16x2(sa.y & 0xFFFFu), e4m3x2_to_f16x2(sa.y >> 16)};
+          const uint32_t scb[4] = {e4m3x2_to_f16x2(sb.x & 0xFFFFu), e4m3x2_to_f16x2(sb.x >> 16),
+                                   e4m3x2_to_f16x2(sb.y & 0xFFFFu), e4m3x2_to_f16x2(sb.y >> 16)};
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // the code bytes 8kk + 2lc, 8kk + 2lc + 1 of the two tokens
+            const uint32_t wa = *reinterpret_cast<const uint16_t*>(t0 + 8 * kk + 2 * lc);
+            const uint32_t wb = *reinterpret_cast<const uint16_t*>(t1 + 8 * kk + 2 * lc);
+            const uint32_t s2a = (kk & 1) ? f16x2_bcast_hi(sca[kk >> 1]) : f16x2_bcast_lo(sca[kk >> 1]);
+            const uint32_t s2b = (kk & 1) ? f16x2_bcast_hi(scb[kk >> 1]) : f16x2_bcast_lo(scb[kk >> 1]);
+            uint32_t ca0, ca2, cb0, cb2;
+            e2m1x4_lo2_to_f16x2(wa, ca0, ca2);
+            e2m1x4_lo2_to_f16x2(wb, cb0, cb2);
+            mma_m16n8k16_f16(d, hmul2_u32(ca0, s2a), hmul2_u32(cb0, s2b), hmul2_u32(ca2, s2a), hmul2_u32(cb2, s2b),
+                             bq[kk][0], bq[kk][1]);
+          }
+          rm0 = fmaxf(rm0, fmaxf(d[0], d[2]));
+          rm1 = fmaxf(rm1, fmaxf(d[1], d[3]));
+        }
+      }
+      // the stage is read: the item after next goes into it
+      if (ok && x + kSmStages < nh) {
+        __syncwarp();
+        fence_proxy_async_smem();
+        const bool gd = issue(x + kSmStages);
+        if (st) good1 = gd; else good0 = gd;
+      }
+      if (x & 1) {                                    // the page's second half: its score
+        if (ok && good) {
+          // over the 8 lane groups (tokens lg, lg + 8 of every tile)
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, o));
+            rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, o));
+          }
+          // row `lane`'s score sits in lane lane / 2 (rm0 for even rows, rm1 for odd)
+          const float v0 = __shfl_sync(0xffffffffu, rm0, (lane >> 1) & 3);
+          const float v1 = __shfl_sync(0xffffffffu, rm1, (lane >> 1) & 3);
+          const float m = canon_zero((lane & 1) ? v1 : v0);
+          if (lane < R && j < L) {
+            top.insert(m, j);
+            if (p.scores_dbg) p.scores_dbg[((int64_t)r * R + lane) * p.dbg_stride + j] = m;
+          }
+        }
+        rm0 = -CUDART_INF_F;
+        rm1 = -CUDART_INF_F;
+      }
+    }
+    kw = k0 + nh;
+
+    // ---- the segment's rows: final (a request inside this range) or candidates
+    const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+    const bool bad = __any_sync(0xffffffffu, seg_bad != 0);
+    if (ok && !abort_s) {
+      if (lane < R) {
+        const int pe = seq_r - p.qlen + lane / p.H;
+        if (cf == cl) {
+          if (p.cand_out) write_cand_row(p.cand_out + ((int64_t)r * R + lane) * kHistK, top.s, top.id, bad);
+          else write_out_row(p.out + ((int64_t)r * R + lane) * kTopK, top.id, pe >= 0 ? (pe >> 7) : -1, bad);
+        } else {
+          float2* dst = p.cand + ((int64_t)(u + r) * R + lane) * kHistK;
+#pragma unroll
+          for (int kq = 0; kq < kHistK; ++kq) dst[kq] = make_float2(top.s[kq], __int_as_float(top.id[kq]));
+        }
+      }
+      if (lane == 0 && cf != cl) p.slot_bad[u + r] = bad ? 1 : 0;
+    } else {
+      // a wait ran out: -1 rows for a request this warp finalises, else a bad slot
+      if (cf == cl && lane < R) {
+        const float zs[kHistK] = {};
+        const int none[kHistK] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+        if (p.cand_out) write_cand_row(p.cand_out + ((int64_t)r * R + lane) * kHistK, zs, none, true);
+        else write_out_row(p.out + ((int64_t)r * R + lane) * kTopK, none, -1, true);
+      }
+      if (lane == 0 && cf != cl) p.slot_bad[u + r] = 1;
+    }
+    walk.g += je - walk.j;
+    walk.j = je;
+    if (walk.more()) walk.next_request(p);
+  }
+  // copies still in flight (after a wait ran out) land before the warp leaves
+#pragma unroll
+  for (int st = 0; st < kSmStages; ++st)
+    if (last_k[st] >= 0) mbar_wait(smem_u32(&pg_full[warp][st]), (uint32_t)((last_k[st] >> 1) & 1));
+}
+
 template <int NQ, class PF>
 static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_t stream) {
   const size_t smem = DecLayout<NQ, PF>::bytes(p.num_reqs);
@@ -857,11 +1172,25 @@ static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;
-  return launch_dependent(decode_merge_kernel, (unsigned)((warps + 7) / 8), 256u, 0, stream, p);
+  return launch_dependent(decode_merge_kernel, (unsigned)((warps + kMergeWarps - 1) / kMergeWarps),
+                         (unsigned)(kMergeWarps * 32), 0, stream, p);
+}
+
+static cudaError_t launch_decode_small(const DecodeParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = 128 + kSmPreOff + (size_t)(p.num_reqs + 1) * 4;   // grid CTAs = 8 x grid split units
+  cudaError_t e = cudaFuncSetAttribute(decode_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_small_kernel<<<grid, kSmWarps * 32, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t warps = (int64_t)p.num_reqs * p.R;
+  return launch_dependent(decode_merge_kernel, (unsigned)((warps + kMergeWarps - 1) / kMergeWarps),
+                         (unsigned)(kMergeWarps * 32), 0, stream, p);
 }
 
 template <class PF>
 static cudaError_t launch_decode_pf(const DecodeParams& p, int grid, cudaStream_t stream) {
+  if (!PF::kBf16 && p.R <= kSmRows) return launch_decode_small(p, grid, stream);
   switch (decode_nq(p.R)) {
     case 16: return launch_decode_nq<16, PF>(p, grid, stream);
     case 32: return launch_decode_nq<32, PF>(p, grid, stream);

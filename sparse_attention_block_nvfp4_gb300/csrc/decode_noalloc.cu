@@ -113,7 +113,9 @@ extern "C" int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages,
   // carve the scratch: status | request info | per-slot bad flags | candidates
   const int R = query_len * num_heads;
   const int grid = slot.num_sms;        // one decode CTA per SM, as indexer_decode
-  const size_t slots = (size_t)grid + (size_t)num_reqs;
+  // candidate slots: one per split unit (a CTA, or a warp for requests of up
+  // to 8 rows) and per request
+  const size_t slots = (size_t)decode_split_units(R, kPagesNvfp4, grid) + (size_t)num_reqs;
   const size_t off_status = 0;
   const size_t off_info = align256(off_status + sizeof(int32_t));
   const size_t off_bad = align256(off_info + (size_t)num_reqs * sizeof(int2));

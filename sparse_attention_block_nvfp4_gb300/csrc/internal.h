@@ -34,9 +34,9 @@ struct DecodeParams {
   const int32_t* seq_lens;     // [num_reqs]
   int32_t* out;                // [rows][H][16]
   float* scores_dbg;           // nullable
-  float2* cand;                // [(grid + num_reqs) slots][R][15] (score, id bits)
-  int32_t* slot_bad;           // [(grid + num_reqs)]
-  int2* req_info;              // [num_reqs] (first CTA, number of segments)
+  float2* cand;                // [(split units + num_reqs) slots][R][15] (score, id bits)
+  int32_t* slot_bad;           // [(split units + num_reqs)]
+  int2* req_info;              // [num_reqs] (first split unit, number of segments)
   int32_t* status;
   int num_blocks, pt_stride, num_reqs, qlen, H, R, dbg_stride;
   int page_format;             // kPagesNvfp4 / kPagesMxfp4
@@ -131,6 +131,10 @@ struct NormRopeArgs {
 };
 cudaError_t launch_insert_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
+// Split units of a decode launch of `grid` CTAs (the candidate slots are
+// indexed by unit + request): the CTAs, or for requests of up to 8 rows on
+// NVFP4 pages the small-row kernel's 16 warps per CTA.
+int decode_split_units(int R, int page_format, int grid);
 // Merge the candidate lists of `world` context-parallel ranks ([world][rows][15],
 // rank-major) into final rows [rows][16].
 cudaError_t launch_cp_merge(const float2* cand_all, int world, int num_reqs, int query_len, int H,

@@ -49,11 +49,12 @@ def test_decode_heads_and_query_lengths(H, qlen):
     _check_workload(w)
 
 
-def test_decode_arbitrary_page_bytes():
+@pytest.mark.parametrize("H,qlen", [(8, 4), (4, 1), (2, 4)])
+def test_decode_arbitrary_page_bytes(H, qlen):
     """Pages of arbitrary bytes (all finite scales, subnormal scales included):
-    exercises the exact fp16 dequantisation beyond what the insert produces."""
-    rng = np.random.Generator(np.random.PCG64(31))
-    H, qlen = 8, 4
+    exercises the exact fp16 dequantisation beyond what the insert produces,
+    on the quad kernel (32 rows) and the small-row path (4 and 8 rows)."""
+    rng = np.random.Generator(np.random.PCG64(31 + H + qlen))
     seq = np.array([128 * 40 + 7, 128 * 3 + 1, 128 * 17], np.int32)
     nb = 70
     table = np.zeros((3, 41), np.int32)
