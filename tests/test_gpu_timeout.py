@@ -32,9 +32,16 @@ def _rows_exact_or_empty(got, ref, label):
     return got.shape[0] * got.shape[1] - empty, empty
 
 
-def test_decode_wait_limit_runs_out_then_recovers():
+@pytest.mark.parametrize("cfg,rows", [(4, 64), (2, 32), (1, 4)],
+                         ids=["quad_kernel_rows64", "quad_kernel_rows32", "small_row_kernel_rows4"])
+def test_decode_wait_limit_runs_out_then_recovers(cfg, rows):
+    """Decode with 1 ns waits: on the quad kernel (64 and 32 rows per
+    request, its waits are the hand-offs between roles) and on the small-row
+    kernel (4 rows per request, its waits are on the page copies of each
+    warp's ring)."""
     import sparse_attention_block_nvfp4_gb300 as idx
-    w = workloads.config(2, small=True)
+    w = workloads.config(cfg, small=True)
+    assert w.query_len * w.num_heads == rows
     kv = gpu_cache(w)
     ref = oidx.decode(w.q_decode, oracle_cache(w), w.dec_page_table, w.dec_seq_lens, w.query_len, w.num_heads)
     plan = make_plan(w)
