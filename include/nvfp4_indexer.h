@@ -330,10 +330,11 @@ int indexer_merge_candidates(const float* cand_all, int world, int num_reqs, int
  *   num_heads  H, one of 1, 2, 4, 8
  *   status     NULL, or a device int32 that gets IDX_STATUS_* bits OR-ed in
  *   (no scores_dbg output)
- * Limit: the call needs 256-byte-aligned pieces of roughly
- * 8*num_reqs + (SMs + num_reqs) * (4 + 120*query_len*num_heads) bytes; a
- * call that needs more than 4 MiB returns IDX_ENOSPACE and launches nothing
- * (about 390 requests at query_len*num_heads = 64 on a 152-SM GPU).
+ * Limit: with R = query_len*num_heads, the call needs 256-byte-aligned
+ * pieces of roughly 8*num_reqs + (U + num_reqs) * (4 + 120*R) bytes, where
+ * U = SMs, or 16*SMs for R <= 8 (the small-row kernel splits the pages over
+ * warps, not CTAs); a call that needs more than 4 MiB returns IDX_ENOSPACE
+ * and launches nothing (about 390 requests at R = 64 on a 152-SM GPU).
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (once per device, that device current) and checks
  * that the device is sm_103 (else IDX_EUNSUPPORTED): make that first call
