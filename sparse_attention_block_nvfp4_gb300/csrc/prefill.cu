@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           sw.next(w, pi.L_max);
           for (int j = ja; j < jb; ++j, ++g) {
             const int s = (int)(g % kPreStages);
-            if (!mbar_wait_or_abort(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
+            if (!mbar_wait_or_abort<true>(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
                                     &abort_s, lim)) {
               fail();
               break;
@@ -424,13 +424,13 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           sw.get<H>(p, sched, pi, w, ja, jb);
           sw.next(w, pi.L_max);
           if (jb <= ja) continue;                     // no pages of this unit here
-          if (!mbar_wait_or_abort(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s, lim)) { fail(); break; }
+          if (!mbar_wait_or_abort<true>(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s, lim)) { fail(); break; }
           bool ok = true;
           for (int j = ja; j < jb; ++j, ++g) {
             const int b = (int)(g & 1);
             const uint32_t par = (uint32_t)((g >> 1) & 1);
-            if (!mbar_wait_or_abort(smem_u32(&b_full[b]), par, &abort_s, lim) ||
-                !mbar_wait_or_abort(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s, lim)) {
+            if (!mbar_wait_or_abort<true>(smem_u32(&b_full[b]), par, &abort_s, lim) ||
+                !mbar_wait_or_abort<true>(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s, lim)) {
               fail();
               ok = false;
               break;
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       for (int j = ja; j < jb; ++j, ++g) {
         if ((int)(g & 1) != grp) continue;
         const int s = (int)(g % kPreStages);
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&raw_full[s]),
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort<true>(smem_u32(&raw_full[s]),
                                                          (uint32_t)((g / kPreStages) & 1), &abort_s, lim))) {
           fail();
           ok = false;
@@ -490,8 +490,8 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
         // phase needs this page)
         const uint32_t fpar = (uint32_t)((((g >> 1) - 1)) & 1);
         if (g >= 2 &&
-            !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[0][grp]), fpar, &abort_s, lim) &&
-                                         mbar_wait_or_abort(smem_u32(&d_full[1][grp]), fpar, &abort_s, lim))) {
+            !__all_sync(0xffffffffu, mbar_wait_or_abort<true>(smem_u32(&d_full[0][grp]), fpar, &abort_s, lim) &&
+                                         mbar_wait_or_abort<true>(smem_u32(&d_full[1][grp]), fpar, &abort_s, lim))) {
           fail();
           ok = false;
           break;
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       if (jb > ja) {
         // this tile's queries -> fp16 A tile, once the MMAs of the previous
         // unit are done with it
-        if (ok && ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&q_empty),
+        if (ok && ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort<true>(smem_u32(&q_empty),
                                                                     (uint32_t)((ip - 1) & 1), &abort_s, lim))) {
           fail();
           ok = false;
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       for (int j = ja; j < jb; ++j, ++g) {
         const int b = (int)(g & 1);
         if (!ok) continue;
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort<true>(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
                                                          &abort_s, lim))) {
           fail();
           ok = false;

@@ -52,14 +52,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// A thread in mbarrier.try_wait may be suspended until the phase completes
+// or a time limit passes.  kSleep asks for a limit of 1 ms, so that a long
+// wait costs almost no issue slots, at a later wake-up than the default
+// limit gives (the prefill kernel's roles gain, the decode kernel's short
+// hand-offs lose).
+constexpr uint32_t kTryWaitSleepNs = 1000000;
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kSleep) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kTryWaitSleepNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -112,12 +128,13 @@ __device__ __forceinline__ int named_bar_red_or(uint32_t id, uint32_t nthreads, 
 // Wait for the phase with the given parity; gives up (false) when *abort
 // becomes non-zero or after `limit_ns` of wall time (the caller's limit,
 // kWaitLimitNs unless the plan set another).
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
                                                    uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kSleep>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kSleep>(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
