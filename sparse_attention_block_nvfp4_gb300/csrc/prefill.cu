@@ -673,28 +673,52 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
 
 // Merge the sorted candidate list b (15 (score, id) entries from another
 // CTA, id < 0 = none) into the top 15 (s, id): the result is the first 15 of
-// both by (score descending, id ascending).  b is loaded in one go and its
-// entries go into the register list with insert_any (equal scores rank the
-// lower id first in any insertion order); the lists hold disjoint ids.
+// both by (score descending, id ascending); the lists hold disjoint ids and
+// their empty entries come last.  With both lists padded to 16 entries and
+// an empty entry keyed (-inf, INT_MAX), c_i = the better of a_i and b_(15-i)
+// holds the 16 best of both as a bitonic sequence (a descending, then b
+// ascending), which four rounds of compare-exchange, 8 / 4 / 2 / 1 apart,
+// sort (Batcher's bitonic merge): 48 compare-exchanges.
+__device__ __forceinline__ bool cand_better(float s1, int i1, float s2, int i2) {
+  return s1 > s2 || (s1 == s2 && i1 < i2);
+}
 __device__ __forceinline__ void merge_top15_list(float (&s)[kHistK], int (&id)[kHistK], const float2* b) {
+  constexpr int kNone = 0x7FFFFFFF;
   float2 bb[kHistK];
 #pragma unroll
   for (int k = 0; k < kHistK; ++k) bb[k] = b[k];
-  TopK15 t;
+  float cs[16];
+  int ci[16];
 #pragma unroll
-  for (int k = 0; k < kHistK; ++k) {
-    t.s[k] = id[k] >= 0 ? s[k] : -CUDART_INF_F;
-    t.id[k] = id[k];
+  for (int i = 0; i < 16; ++i) {
+    const float as = i < kHistK && id[i] >= 0 ? s[i] : -CUDART_INF_F;
+    const int ai = i < kHistK && id[i] >= 0 ? id[i] : kNone;
+    const int jb = 15 - i;                           // b_(15 - i); b_15 is the padding
+    const int bi0 = jb < kHistK ? __float_as_int(bb[jb < kHistK ? jb : 0].y) : -1;
+    const float bs = bi0 >= 0 ? bb[jb < kHistK ? jb : 0].x : -CUDART_INF_F;
+    const int bi = bi0 >= 0 ? bi0 : kNone;
+    const bool ta = cand_better(as, ai, bs, bi);
+    cs[i] = ta ? as : bs;
+    ci[i] = ta ? ai : bi;
+  }
+#pragma unroll
+  for (int d = 8; d >= 1; d >>= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & d) continue;
+      const bool sw = cand_better(cs[i + d], ci[i + d], cs[i], ci[i]);
+      const float ts = sw ? cs[i + d] : cs[i], us = sw ? cs[i] : cs[i + d];
+      const int ti = sw ? ci[i + d] : ci[i], ui = sw ? ci[i] : ci[i + d];
+      cs[i] = ts;
+      ci[i] = ti;
+      cs[i + d] = us;
+      ci[i + d] = ui;
+    }
   }
 #pragma unroll
   for (int k = 0; k < kHistK; ++k) {
-    const int bi = __float_as_int(bb[k].y);
-    if (bi >= 0) t.insert_any(bb[k].x, bi);
-  }
-#pragma unroll
-  for (int k = 0; k < kHistK; ++k) {
-    s[k] = t.s[k];
-    id[k] = t.id[k];
+    s[k] = ci[k] != kNone ? cs[k] : -CUDART_INF_F;
+    id[k] = ci[k] != kNone ? ci[k] : -1;
   }
 }
 
