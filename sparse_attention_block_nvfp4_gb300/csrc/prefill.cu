@@ -199,6 +199,11 @@ template <int H, class PF>
 __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillParams p) {
   using PreLayout = nvfp4idx::PreLayout<PF>;
   constexpr int TQ = 128 / H;     // tokens per tile
+  // Waits that sleep inside mbarrier.try_wait (up to 1 ms) leave their
+  // schedulers' issue slots to the dequant and epilogue warps: NVFP4 pages
+  // gain; MXFP4 pages, whose dequantisation costs 2.5 times the
+  // instructions, measured slower with them.
+  constexpr bool kSleep = !PF::kBf16;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kPreStages], raw_empty[kPreStages];
   // B tile h is free again once both tiles' MMAs of its last page are done,
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           sw.next(w, pi.L_max);
           for (int j = ja; j < jb; ++j, ++g) {
             const int s = (int)(g % kPreStages);
-            if (!mbar_wait_or_abort<true>(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
+            if (!mbar_wait_or_abort<kSleep>(smem_u32(&raw_empty[s]), (uint32_t)(((g / kPreStages) & 1) ^ 1),
                                     &abort_s, lim)) {
               fail();
               break;
@@ -424,13 +429,13 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
           sw.get<H>(p, sched, pi, w, ja, jb);
           sw.next(w, pi.L_max);
           if (jb <= ja) continue;                     // no pages of this unit here
-          if (!mbar_wait_or_abort<true>(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s, lim)) { fail(); break; }
+          if (!mbar_wait_or_abort<kSleep>(smem_u32(&q_full[x]), (uint32_t)(ip & 1), &abort_s, lim)) { fail(); break; }
           bool ok = true;
           for (int j = ja; j < jb; ++j, ++g) {
             const int b = (int)(g & 1);
             const uint32_t par = (uint32_t)((g >> 1) & 1);
-            if (!mbar_wait_or_abort<true>(smem_u32(&b_full[b]), par, &abort_s, lim) ||
-                !mbar_wait_or_abort<true>(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s, lim)) {
+            if (!mbar_wait_or_abort<kSleep>(smem_u32(&b_full[b]), par, &abort_s, lim) ||
+                !mbar_wait_or_abort<kSleep>(smem_u32(&d_empty[x][b]), par ^ 1u, &abort_s, lim)) {
               fail();
               ok = false;
               break;
@@ -546,7 +551,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       if (jb > ja) {
         // this tile's queries -> fp16 A tile, once the MMAs of the previous
         // unit are done with it
-        if (ok && ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort<true>(smem_u32(&q_empty),
+        if (ok && ip > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort<kSleep>(smem_u32(&q_empty),
                                                                     (uint32_t)((ip - 1) & 1), &abort_s, lim))) {
           fail();
           ok = false;
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kPreThreads, 1) prefill_kernel(const PrefillPa
       for (int j = ja; j < jb; ++j, ++g) {
         const int b = (int)(g & 1);
         if (!ok) continue;
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort<true>(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort<kSleep>(smem_u32(&d_full[x][b]), (uint32_t)((g >> 1) & 1),
                                                          &abort_s, lim))) {
           fail();
           ok = false;
