@@ -30,6 +30,8 @@
 //     4l .. 4l + 3 (8-byte loads of the V row, coalesced across the warp,
 //     eight tokens' loads in flight), a fresh per-page partial (at most 32
 //     terms), added to the running accumulator after its rescale by alpha;
+//     for G <= 2 a half warp takes a token (16-byte loads, 16 terms a
+//     partial, the halves added at the end);
 //   * at the end every CTA stores its maximum, its warps' weight sums and
 //     accumulators into the first CTA, which merges them in a fixed order:
 //     M the largest maximum, each CTA's sums scaled by exp(M_q - M), then
@@ -104,6 +106,11 @@ struct AttCfg {
   static constexpr int kKUnroll = G == 1 ? 16 : (G <= 4 ? 8 : 4);
   static constexpr int kMinBlocks = G == 1 ? 8 : (G == 2 ? 6 : (G == 4 ? 3 : 2));
   static constexpr int kSmemAcc = kAttSplit * 4 * G * kDim * 4;   // the leader's [CTA][warp][G][kDim]
+  // V rows by 16-byte loads: a half warp per token, lane l % 16 on dims
+  // 8 (l % 16) .. + 7, so a warp has twice the bytes in flight; the 8
+  // accumulators per head and lane fit the register budget for G <= 2
+  static constexpr bool kWideV = G <= 2;
+  static constexpr int kVC = kWideV ? 8 : 4;   // dims per lane
 };
 
 template <int G>
@@ -171,13 +178,14 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
   __syncthreads();
   const int npages = npages_s;
 
-  float m_run[G], l_thr[G], acc[G][4];
+  constexpr int VC = AttCfg<G>::kVC;
+  float m_run[G], l_thr[G], acc[G][VC];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m_run[g] = -CUDART_INF_F;
     l_thr[g] = 0.0f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[g][c] = 0.0f;
+    for (int c = 0; c < VC; ++c) acc[g][c] = 0.0f;
   }
 
   for (int pi = (int)rank; pi < npages; pi += kAttSplit) {
@@ -233,29 +241,49 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
       l_thr[g] = l_thr[g] * alpha[g] + pw;
     }
     __syncthreads();
-    // ---- weighted sum of the V rows: warp w, tokens w, w + 4, ...
-    float part[G][4];
+    // ---- weighted sum of the V rows
+    float part[G][VC];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) part[g][c] = 0.0f;
+      for (int c = 0; c < VC; ++c) part[g][c] = 0.0f;
+    if constexpr (AttCfg<G>::kWideV) {
+      // warp w, half h = lane / 16: tokens 2w + h, 2w + h + 8, ...
 #pragma unroll 8
-    for (int i = warp; i < n; i += 4) {
-      const uint2 vv = __ldg(reinterpret_cast<const uint2*>(p.v_cache + (base + (int64_t)i * p.H) * kDim) + lane);
-      const float v0 = bf16_lo(vv.x), v1 = bf16_hi(vv.x), v2 = bf16_lo(vv.y), v3 = bf16_hi(vv.y);
+      for (int i = 2 * warp + (lane >> 4); i < n; i += 8) {
+        const uint4 vv =
+            __ldg(reinterpret_cast<const uint4*>(p.v_cache + (base + (int64_t)i * p.H) * kDim) + (lane & 15));
+        const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pw = p_s[g][i];
-        part[g][0] = fmaf(pw, v0, part[g][0]);
-        part[g][1] = fmaf(pw, v1, part[g][1]);
-        part[g][2] = fmaf(pw, v2, part[g][2]);
-        part[g][3] = fmaf(pw, v3, part[g][3]);
+        for (int g = 0; g < G; ++g) {
+          const float pw = p_s[g][i];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            part[g][2 * c] = fmaf(pw, bf16_lo(w[c]), part[g][2 * c]);
+            part[g][2 * c + 1] = fmaf(pw, bf16_hi(w[c]), part[g][2 * c + 1]);
+          }
+        }
+      }
+    } else {
+      // warp w, tokens w, w + 4, ...; lane l on dims 4l .. 4l + 3
+#pragma unroll 8
+      for (int i = warp; i < n; i += 4) {
+        const uint2 vv = __ldg(reinterpret_cast<const uint2*>(p.v_cache + (base + (int64_t)i * p.H) * kDim) + lane);
+        const float v0 = bf16_lo(vv.x), v1 = bf16_hi(vv.x), v2 = bf16_lo(vv.y), v3 = bf16_hi(vv.y);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pw = p_s[g][i];
+          part[g][0] = fmaf(pw, v0, part[g][0]);
+          part[g][1] = fmaf(pw, v1, part[g][1]);
+          part[g][2] = fmaf(pw, v2, part[g][2]);
+          part[g][3] = fmaf(pw, v3, part[g][3]);
+        }
       }
     }
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[g][c] = fmaf(acc[g][c], alpha[g], part[g][c]);
+      for (int c = 0; c < VC; ++c) acc[g][c] = fmaf(acc[g][c], alpha[g], part[g][c]);
     __syncthreads();                                  // p_s and red_s are rewritten by the next page
   }
 
@@ -263,8 +291,19 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
   cluster_wait_acquire();                             // (the start barrier) every CTA of the cluster runs
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    st_cluster_v4(cluster_map(&acc_all[((rank * 4 + warp) * G + g) * kDim + 4 * lane], 0),
-                  make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]));
+    if constexpr (AttCfg<G>::kWideV) {
+      // the two half warps' sums of the same dimensions (one addition)
+#pragma unroll
+      for (int c = 0; c < VC; ++c) acc[g][c] += __shfl_xor_sync(0xffffffffu, acc[g][c], 16);
+      if (lane < 16) {
+        float* const dst = &acc_all[((rank * 4 + warp) * G + g) * kDim + 8 * lane];
+        st_cluster_v4(cluster_map(dst, 0), make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]));
+        st_cluster_v4(cluster_map(dst + 4, 0), make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]));
+      }
+    } else {
+      st_cluster_v4(cluster_map(&acc_all[((rank * 4 + warp) * G + g) * kDim + 4 * lane], 0),
+                    make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]));
+    }
     const float lw = warp_sum_f32(l_thr[g]);
     if (lane == 0) st_cluster_f32(cluster_map(&lq_all[rank][warp][g], 0), lw);
     if (tid == 0) st_cluster_f32(cluster_map(&mq_all[rank][g], 0), m_run[g]);
