@@ -31,7 +31,8 @@
 //     eight tokens' loads in flight), a fresh per-page partial (at most 32
 //     terms), added to the running accumulator after its rescale by alpha;
 //     for G <= 2 a half warp takes a token (16-byte loads, 16 terms a
-//     partial, the halves added at the end);
+//     partial, the halves added at the end); each thread prefetched its
+//     token's V row into L2 when the page's work began;
 //   * at the end every CTA stores its maximum, its warps' weight sums and
 //     accumulators into the first CTA, which merges them in a fixed order:
 //     M the largest maximum, each CTA's sums scaled by exp(M_q - M), then
@@ -193,6 +194,12 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
     const int phys = __ldg(p.page_table + (int64_t)r * p.pt_stride + j);
     const int n = min(kPage, pos - j * kPage + 1);                // visible tokens of the page
     const int64_t base = (int64_t)phys * kPage * p.H + hk;         // token row 0 of the page, head hk
+    // the page's V rows start their way into L2 now, behind the K loads
+    if (tid < n) {
+      const uint16_t* vrow = p.v_cache + (base + (int64_t)tid * p.H) * kDim;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + 64));
+    }
     // ---- scores: thread = token
     float s[G];
 #pragma unroll
