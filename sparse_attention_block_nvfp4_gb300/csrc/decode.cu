@@ -227,6 +227,21 @@ struct SegWalk {
   }
 };
 
+// The rows of a segment whose scores a run-out wait left incomplete: -1
+// rows for a request the CTA finalises, else a bad slot for the merge.  Out
+// of line, so that the epilogue's loop keeps its code and registers.
+__device__ __noinline__ void decode_segment_failed(const DecodeParams& p, const int32_t* pre, int64_t T, int G,
+                                                   int r, int c, int ep, int R) {
+  const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
+  if (cf == cl && ep < R) {
+    const float zs[kHistK] = {};
+    const int none[kHistK] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (p.cand_out) write_cand_row(p.cand_out + ((int64_t)r * R + ep) * kHistK, zs, none, true);
+    else write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, none, -1, true);
+  }
+  if (ep == 0 && cf != cl) p.slot_bad[c + r] = 1;
+}
+
 template <int NQ, class PF>
 __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel(const DecodeParams p) {
   using Lay = DecLayout<NQ, PF>;
@@ -313,20 +328,20 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
   if (tid == 0) {
     for (int s = 0; s < kDecStages; ++s) {
       mbar_init(smem_u32(&raw_full[s]), 1);
-      mbar_init(smem_u32(&raw_empty[s]), 1);    // one dequant warp reads a page (lane 0 arrives)
+      mbar_init(smem_u32(&raw_empty[s]), 32);   // one dequant warp reads a page
     }
-    // one arrival per warp: its lanes synchronise first (__syncwarp), then
-    // lane 0 arrives, which keeps the barrier's shared-memory atomics to one
-    // per warp instead of one per thread
+    // every thread of a role arrives for itself as soon as its own part is
+    // done (one arrival per warp after a __syncwarp measured 2.5 us slower
+    // per call on long_mixed)
     for (int b = 0; b < kDecSlices; ++b) {
-      mbar_init(smem_u32(&a_full[b]), 4);       // the quad's dequant warpgroup
+      mbar_init(smem_u32(&a_full[b]), 128);     // the quad's dequant warpgroup
       mbar_init(smem_u32(&d_full[0][b]), 1);    // MMA commit
       mbar_init(smem_u32(&d_full[1][b]), 1);
-      mbar_init(smem_u32(&d_empty[0][b]), Roles::kEpThreads / 32); // the epilogue warpgroup(s)
-      mbar_init(smem_u32(&d_empty[1][b]), Roles::kEpThreads / 32);
+      mbar_init(smem_u32(&d_empty[0][b]), Roles::kEpThreads);   // the epilogue warpgroup(s)
+      mbar_init(smem_u32(&d_empty[1][b]), Roles::kEpThreads);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&q_full[k]), 8);     // both dequant groups write the tile
+      mbar_init(smem_u32(&q_full[k]), 256);   // both dequant groups write the tile
       mbar_init(smem_u32(&q_empty[k]), 2);    // both MMA issuers commit
     }
     abort_s = 0;
@@ -516,7 +531,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         *reinterpret_cast<uint4*>(qt + (c8 >> 3) * (NQ * 128) + sw128_offset(row, c8 & 7)) = o;
       }
       fence_proxy_async_smem();
-      mbar_arrive_warp(smem_u32(&q_full[qs]));
+      mbar_arrive(smem_u32(&q_full[qs]));
       for (; walk.j < je && ok; ++kq) {
         const int npq = min(4, je - walk.j);
         walk.j += npq;
@@ -530,7 +545,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           ok = false;
           break;
         }
-        if (!has) mbar_arrive_warp(smem_u32(&raw_empty[st]));
+        if (!has) mbar_arrive(smem_u32(&raw_empty[st]));
         const uint8_t* const page = base + Lay::kStageOff + st * PF::kPageBytes;
 #pragma unroll 1
         for (int sl = 0; sl < kDecSlices; ++sl) {
@@ -538,7 +553,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
           if (has) {
             typename PF::Row row;
             PF::load(page, sl * 32 + lane, row);
-            if (sl == kDecSlices - 1) mbar_arrive_warp(smem_u32(&raw_empty[st]));
+            if (sl == kDecSlices - 1) mbar_arrive(smem_u32(&raw_empty[st]));
 #pragma unroll
             for (int g8 = 0; g8 < 8; ++g8) PF::chunk16(row, g8, a + 8 * g8);
           }
@@ -556,7 +571,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
             tmem_wait_st();
           }
           tc_fence_before();
-          mbar_arrive_warp(smem_u32(&a_full[sl]));
+          mbar_arrive(smem_u32(&a_full[sl]));
         }
       }
       ++sq;
@@ -634,7 +649,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
               }
             }
             tc_fence_before();
-            mbar_arrive_warp(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]));
+            mbar_arrive(smem_u32(&d_empty[DecD<NQ>::set(kq)][sl]));
           }
         }
         if (ok && has) {
@@ -675,14 +690,7 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
         // become -1 (a request this CTA finalises) or its slot is flagged
         // bad, so that the merge writes -1 rows instead of reading
         // candidates this call never wrote
-        const int cf = cta_of(pre[r], T, G), cl = cta_of(pre[r + 1] - 1, T, G);
-        if (cf == cl && ep < R) {
-          const float zs[kHistK] = {};
-          const int none[kHistK] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
-          if (p.cand_out) write_cand_row(p.cand_out + ((int64_t)r * R + ep) * kHistK, zs, none, true);
-          else write_out_row(p.out + ((int64_t)r * R + ep) * kTopK, none, -1, true);
-        }
-        if (ep == 0 && cf != cl) p.slot_bad[c + r] = 1;
+        decode_segment_failed(p, pre, T, G, r, c, ep, R);
       }
       named_bar_sync(2, Roles::kEpThreads);           // lists are read before the next reset
       if (walk.more()) walk.next_request(p);
@@ -699,15 +707,20 @@ __global__ void __launch_bounds__(DecRoles<NQ>::kThreads, 1) decode_score_kernel
 
 // One warp per (request, row): merge the per-segment top-15 lists of split
 // requests; write rows of requests with no history page or an unreadable one.
-// Lane k holds lists k and k + 32 (up to 64 segments; beyond that each of
-// the two is the top-15 of lists k, k + 64, ... / k + 32, k + 96, ...), and
-// 15 warp-wide rounds take the best head (score desc, id asc) of all of them.
-constexpr int kMergeWarps = 4;
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
+// W warps per CTA; lane k holds kHeads lists, k + 32h (h < kHeads), and with
+// more than 32 kHeads segments each of them is the top-15 of lists k + 32h,
+// k + 32h + 32 kHeads, ... (ascending page ranges).  15 warp-wide rounds then
+// take the best head (score desc, id asc) of all of them.  The quad kernel's
+// requests (a few segments each) take <8, 1>; the small-row kernel's warps
+// (dozens of segments per request) take <4, 2>.
+template <int W, int kHeads>
+__global__ void __launch_bounds__(W * 32) decode_merge_kernel(const DecodeParams p) {
+  static_assert(kHeads == 1 || kHeads == 2, "one or two lists per lane");
   griddep_wait();                                    // the scoring grid's candidates are written
-  __shared__ float2 lists[kMergeWarps][64][kHistK];
+  constexpr int kLists = 32 * kHeads;
+  __shared__ float2 lists[W][kLists][kHistK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t)blockIdx.x * kMergeWarps + warp;
+  const int64_t gw = (int64_t)blockIdx.x * W + warp;
   if (gw >= (int64_t)p.num_reqs * p.R) return;
   const int r = (int)(gw / p.R), n = (int)(gw % p.R);
   const int seq = __ldg(p.seq_lens + r);
@@ -744,10 +757,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
     return;
   }
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
+  for (int hh = 0; hh < kHeads; ++hh) {
     const int li = lane + 32 * hh;
     float2(&mine)[kHistK] = lists[warp][li];
-    if (nseg <= 64) {
+    if (nseg <= kLists) {
       if (li < nseg) {
         const float2* src = p.cand + ((int64_t)(slot0 + li) * p.R + n) * kHistK;
 #pragma unroll
@@ -757,11 +770,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
         for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(0.0f, __int_as_float(-1));
       }
     } else {
-      // lists li, li + 64, ... cover ascending page ranges: inserted in that
-      // order, an equal score always comes with a higher id
+      // lists li, li + kLists, ... cover ascending page ranges: inserted in
+      // that order, an equal score always comes with a higher id
       TopK15 t;
       t.reset();
-      for (int k = li; k < nseg; k += 64) {
+      for (int k = li; k < nseg; k += kLists) {
         const float2* src = p.cand + ((int64_t)(slot0 + k) * p.R + n) * kHistK;
         float2 e[kHistK];
 #pragma unroll
@@ -781,12 +794,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 #pragma unroll
   for (int k = 0; k < kHistK; ++k) {
     const float2 e0 = h0 < kHistK ? lists[warp][lane][h0] : make_float2(0.0f, __int_as_float(-1));
-    const float2 e1 = h1 < kHistK ? lists[warp][lane + 32][h1] : make_float2(0.0f, __int_as_float(-1));
-    const int id0 = __float_as_int(e0.y), id1 = __float_as_int(e1.y);
-    const uint32_t k0 = id0 >= 0 ? order_key(e0.x) : 0u, k1 = id1 >= 0 ? order_key(e1.x) : 0u;
-    const bool take1 = k1 > k0 || (k1 == k0 && k1 != 0u && id1 < id0);
-    const uint32_t key = take1 ? k1 : k0;
-    const int id = take1 ? id1 : id0;
+    const int id0 = __float_as_int(e0.y);
+    const uint32_t k0 = id0 >= 0 ? order_key(e0.x) : 0u;
+    uint32_t key = k0;
+    int id = id0;
+    bool take1 = false;
+    if constexpr (kHeads == 2) {
+      const float2 e1 = h1 < kHistK ? lists[warp][lane + 32][h1] : make_float2(0.0f, __int_as_float(-1));
+      const int id1 = __float_as_int(e1.y);
+      const uint32_t k1 = id1 >= 0 ? order_key(e1.x) : 0u;
+      take1 = k1 > k0 || (k1 == k0 && k1 != 0u && id1 < id0);
+      key = take1 ? k1 : k0;
+      id = take1 ? id1 : id0;
+    }
     const uint32_t kmax = warp_max_u32(key);
     const uint32_t idmin = warp_min_u32(key == kmax && kmax != 0u ? (uint32_t)id : 0xFFFFFFFFu);
     if (kmax != 0u && key == kmax && (uint32_t)id == idmin) {
@@ -1172,8 +1192,7 @@ static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;
-  return launch_dependent(decode_merge_kernel, (unsigned)((warps + kMergeWarps - 1) / kMergeWarps),
-                         (unsigned)(kMergeWarps * 32), 0, stream, p);
+  return launch_dependent(decode_merge_kernel<8, 1>, (unsigned)((warps + 7) / 8), 256u, 0, stream, p);
 }
 
 static cudaError_t launch_decode_small(const DecodeParams& p, int grid, cudaStream_t stream) {
@@ -1184,8 +1203,7 @@ static cudaError_t launch_decode_small(const DecodeParams& p, int grid, cudaStre
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;
-  return launch_dependent(decode_merge_kernel, (unsigned)((warps + kMergeWarps - 1) / kMergeWarps),
-                         (unsigned)(kMergeWarps * 32), 0, stream, p);
+  return launch_dependent(decode_merge_kernel<4, 2>, (unsigned)((warps + 3) / 4), 128u, 0, stream, p);
 }
 
 template <class PF>

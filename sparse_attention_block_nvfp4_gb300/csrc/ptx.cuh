@@ -38,14 +38,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
                : "memory");
 }
 
-// One arrival for the whole warp: every lane must call it (convergent); the
-// lanes' earlier writes are ordered before lane 0's arrival by the warp
-// barrier.
-__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                "r"(bytes)
