@@ -135,7 +135,7 @@ def _score_rows(q_rows_bytes, K, H):
 
 
 def _run(q, kv_pages, page_table, seq_lens, qlens, H, rows_wanted, page_format="nvfp4"):
-    """Shared driver: requests r with qlens[r] rows each, right-aligned."""
+    """Shared body of decode and prefill: requests r with qlens[r] rows each, right-aligned."""
     kv_pages = np.asarray(kv_pages, dtype=np.uint8)
     page_table = np.asarray(page_table)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
