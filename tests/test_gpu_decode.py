@@ -73,11 +73,13 @@ def test_decode_arbitrary_page_bytes(H, qlen):
     _check_workload(w, kv_gpu=up(kv), kv_ref=kv)
 
 
-def test_decode_ties_take_lowest_ids_across_splits():
+@pytest.mark.parametrize("H,qlen", [(4, 2), (8, 4), (8, 8)])
+def test_decode_ties_take_lowest_ids_across_splits(H, qlen):
     """Identical pages: every score ties, so every row must be [0..14, L]
-    exactly, also when a long request is split across many CTAs."""
+    exactly, also when a long request is split across many split units
+    (warps of the small-row kernel for 8 rows, CTAs of the quad kernel for
+    32 and 64)."""
     rng = np.random.Generator(np.random.PCG64(32))
-    H, qlen = 4, 2
     seq = np.array([128 * 3000 + 77, 128 * 20 + 1, 128 * 900], np.int32)
     pages = (seq + 127) // 128
     nb = int(pages.sum())
@@ -100,11 +102,16 @@ def test_decode_ties_take_lowest_ids_across_splits():
             assert np.all(out[r * qlen + i] == np.array(want, np.int32)), (r, i, out[r * qlen + i])
 
 
-def test_decode_one_long_request_many_splits():
-    """One request spread over every CTA (more than 32 segments per request)."""
+@pytest.mark.parametrize("H,qlen", [(8, 8), (4, 1), (8, 1)])
+def test_decode_one_long_request_many_splits(H, qlen):
+    """One request spread over every split unit: more than 32 CTAs of the
+    quad kernel (64 rows), or more than 64 warps of the small-row kernel (4
+    and 8 rows: about one page a warp, so the merge folds the lists beyond
+    the 64 a warp holds)."""
     rng = np.random.Generator(np.random.PCG64(33))
-    w = workloads.make_workload(name="one_long", seed=33, rng=rng, num_heads=8, dec_seq_lens=[128 * 1500 + 9],
-                                query_len=8, outlier_channels=4, page_scale_spread=6.0)
+    w = workloads.make_workload(name=f"one_long_H{H}_q{qlen}", seed=33, rng=rng, num_heads=H,
+                                dec_seq_lens=[128 * 1500 + 9], query_len=qlen, outlier_channels=4,
+                                page_scale_spread=6.0)
     _check_workload(w)
 
 
