@@ -932,13 +932,28 @@ __device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                  uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Split units of the decode launch: CTAs of the quad kernel, or warps of the
 // small-row kernel (the candidate slots are indexed by unit + request).
 int decode_split_units(int R, int page_format, int grid) {
-  return (page_format != kPagesMxfp4 && R <= kSmRows) ? grid * kSmWarps : grid;
+  (void)page_format;                                 // both page formats
+  return R <= kSmRows ? grid * kSmWarps : grid;
 }
 
+template <class PF>
 __global__ void __launch_bounds__(kSmWarps * 32, 1) decode_small_kernel(const DecodeParams p) {
+  // a stage: NVFP4, 64 token rows of 72 bytes; MXFP4, 64 rows of 64 code
+  // bytes, then their 64 x 4 E8M0 scale bytes
+  constexpr uint32_t kRow = PF::kBf16 ? 64u : 72u;
+  constexpr uint32_t kStageBytes = PF::kBf16 ? 64u * 64u + 64u * 4u : kSmHalf;
   extern __shared__ __align__(128) uint8_t sm_raw[];
   __shared__ __align__(8) uint64_t pg_full[kSmWarps][kSmStages];
   __shared__ volatile int abort_s;
@@ -1040,8 +1055,14 @@ __global__ void __launch_bounds__(kSmWarps * 32, 1) decode_small_kernel(const De
       if (lane == 0) {
         const uint32_t fb = smem_u32(&pg_full[warp][st]);
         if (good) {
-          mbar_arrive_expect_tx(fb, kSmHalf);
-          bulk_g2s(smem_u32(ring + st * kSmHalf), p.kv + (int64_t)phys * 9216 + (x & 1) * kSmHalf, kSmHalf, fb);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint8_t* const page = p.kv + (int64_t)phys * PF::kPageBytes;
+          if constexpr (PF::kBf16) {
+            bulk_g2s(smem_u32(ring + st * kSmHalf), page + (x & 1) * 4096, 4096u, fb);
+            bulk_g2s(smem_u32(ring + st * kSmHalf + 4096), page + 8192 + (x & 1) * 256, 256u, fb);
+          } else {
+            bulk_g2s(smem_u32(ring + st * kSmHalf), page + (x & 1) * kSmHalf, kSmHalf, fb);
+          }
         } else {
           if (!(x & 1)) atomicOr(p.status, kStatusBadPage);
           mbar_arrive(fb);                           // nothing to copy: the stage's phase completes empty
@@ -1062,8 +1083,8 @@ __global__ void __launch_bounds__(kSmWarps * 32, 1) decode_small_kernel(const De
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t w4 = 0;
       if (lg < R) w4 = __ldg(reinterpret_cast<const uint32_t*>(p.q + ((int64_t)r * R + lg) * 128 + 16 * kk + 4 * lc));
-      bq[kk][0] = e4m3x2_to_f16x2(w4 & 0xFFFFu);
-      bq[kk][1] = e4m3x2_to_f16x2(w4 >> 16);
+      bq[kk][0] = PF::widen_q(w4 & 0xFFFFu);
+      bq[kk][1] = PF::widen_q(w4 >> 16);
     }
     const int pos = seq_r - p.qlen + lane / p.H;       // row `lane` (lanes < R)
     const int L = pos >= 0 ? (pos >> 7) : -1;
@@ -1089,28 +1110,54 @@ __global__ void __launch_bounds__(kSmWarps * 32, 1) decode_small_kernel(const De
         const uint8_t* const pg = ring + st * kSmHalf;
 #pragma unroll 1
         for (int mt = 0; mt < 4; ++mt) {
-          const uint8_t* const t0 = pg + (16 * mt + lg) * 72;
-          const uint8_t* const t1 = t0 + 8 * 72;
-          // the two tokens' 8 scales, f16x2 pairs {group 2i, group 2i + 1}
-          const uint2 sa = *reinterpret_cast<const uint2*>(t0 + 64);
-          const uint2 sb = *reinterpret_cast<const uint2*>(t1 + 64);
-          const uint32_t sca[4] = {e4m3x2_to_f16x2(sa.x & 0xFFFFu), e4m3x2_to_f16x2(sa.x >> 16),
-                                   e4m3x2_to_f16x2(sa.y & 0xFFFFu), e4m3x2_to_f16x2(sa.y >> 16)};
-          const uint32_t scb[4] = {e4m3x2_to_f16x2(sb.x & 0xFFFFu), e4m3x2_to_f16x2(sb.x >> 16),
-                                   e4m3x2_to_f16x2(sb.y & 0xFFFFu), e4m3x2_to_f16x2(sb.y >> 16)};
+          const uint8_t* const t0 = pg + (16 * mt + lg) * kRow;
+          const uint8_t* const t1 = t0 + 8 * kRow;
           float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if constexpr (PF::kBf16) {
+            // the two tokens' 4 E8M0 scales, one per 32 dimensions = K steps
+            // 2j, 2j + 1, as bf16x2 broadcasts
+            const uint32_t sa = *reinterpret_cast<const uint32_t*>(pg + 4096 + (16 * mt + lg) * 4);
+            const uint32_t sb = *reinterpret_cast<const uint32_t*>(pg + 4096 + (16 * mt + lg + 8) * 4);
+            uint32_t s2a[4], s2b[4];
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // the code bytes 8kk + 2lc, 8kk + 2lc + 1 of the two tokens
-            const uint32_t wa = *reinterpret_cast<const uint16_t*>(t0 + 8 * kk + 2 * lc);
-            const uint32_t wb = *reinterpret_cast<const uint16_t*>(t1 + 8 * kk + 2 * lc);
-            const uint32_t s2a = (kk & 1) ? f16x2_bcast_hi(sca[kk >> 1]) : f16x2_bcast_lo(sca[kk >> 1]);
-            const uint32_t s2b = (kk & 1) ? f16x2_bcast_hi(scb[kk >> 1]) : f16x2_bcast_lo(scb[kk >> 1]);
-            uint32_t ca0, ca2, cb0, cb2;
-            e2m1x4_lo2_to_f16x2(wa, ca0, ca2);
-            e2m1x4_lo2_to_f16x2(wb, cb0, cb2);
-            mma_m16n8k16_f16(d, hmul2_u32(ca0, s2a), hmul2_u32(cb0, s2b), hmul2_u32(ca2, s2a), hmul2_u32(cb2, s2b),
-                             bq[kk][0], bq[kk][1]);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t ba = (sa >> (8 * j)) & 0xFFu, bb = (sb >> (8 * j)) & 0xFFu;
+              s2a[j] = e8m0x2_to_bf16x2(ba | (ba << 8));
+              s2b[j] = e8m0x2_to_bf16x2(bb | (bb << 8));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t wa = *reinterpret_cast<const uint16_t*>(t0 + 8 * kk + 2 * lc);
+              const uint32_t wb = *reinterpret_cast<const uint16_t*>(t1 + 8 * kk + 2 * lc);
+              uint32_t ca0, ca2, cb0, cb2;
+              e2m1x4_lo2_to_f16x2(wa, ca0, ca2);
+              e2m1x4_lo2_to_f16x2(wb, cb0, cb2);
+              const uint32_t sA = s2a[kk >> 1], sB = s2b[kk >> 1];
+              mma_m16n8k16_bf16(d, bmul2_u32(f16x2_to_bf16x2(ca0), sA), bmul2_u32(f16x2_to_bf16x2(cb0), sB),
+                                bmul2_u32(f16x2_to_bf16x2(ca2), sA), bmul2_u32(f16x2_to_bf16x2(cb2), sB),
+                                bq[kk][0], bq[kk][1]);
+            }
+          } else {
+            // the two tokens' 8 scales, f16x2 pairs {group 2i, group 2i + 1}
+            const uint2 sa = *reinterpret_cast<const uint2*>(t0 + 64);
+            const uint2 sb = *reinterpret_cast<const uint2*>(t1 + 64);
+            const uint32_t sca[4] = {e4m3x2_to_f16x2(sa.x & 0xFFFFu), e4m3x2_to_f16x2(sa.x >> 16),
+                                     e4m3x2_to_f16x2(sa.y & 0xFFFFu), e4m3x2_to_f16x2(sa.y >> 16)};
+            const uint32_t scb[4] = {e4m3x2_to_f16x2(sb.x & 0xFFFFu), e4m3x2_to_f16x2(sb.x >> 16),
+                                     e4m3x2_to_f16x2(sb.y & 0xFFFFu), e4m3x2_to_f16x2(sb.y >> 16)};
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // the code bytes 8kk + 2lc, 8kk + 2lc + 1 of the two tokens
+              const uint32_t wa = *reinterpret_cast<const uint16_t*>(t0 + 8 * kk + 2 * lc);
+              const uint32_t wb = *reinterpret_cast<const uint16_t*>(t1 + 8 * kk + 2 * lc);
+              const uint32_t s2a = (kk & 1) ? f16x2_bcast_hi(sca[kk >> 1]) : f16x2_bcast_lo(sca[kk >> 1]);
+              const uint32_t s2b = (kk & 1) ? f16x2_bcast_hi(scb[kk >> 1]) : f16x2_bcast_lo(scb[kk >> 1]);
+              uint32_t ca0, ca2, cb0, cb2;
+              e2m1x4_lo2_to_f16x2(wa, ca0, ca2);
+              e2m1x4_lo2_to_f16x2(wb, cb0, cb2);
+              mma_m16n8k16_f16(d, hmul2_u32(ca0, s2a), hmul2_u32(cb0, s2b), hmul2_u32(ca2, s2a),
+                               hmul2_u32(cb2, s2b), bq[kk][0], bq[kk][1]);
+            }
           }
           rm0 = fmaxf(rm0, fmaxf(d[0], d[2]));
           rm1 = fmaxf(rm1, fmaxf(d[1], d[3]));
@@ -1195,11 +1242,13 @@ static cudaError_t launch_decode_nq(const DecodeParams& p, int grid, cudaStream_
   return launch_dependent(decode_merge_kernel<8, 1>, (unsigned)((warps + 7) / 8), 256u, 0, stream, p);
 }
 
+template <class PF>
 static cudaError_t launch_decode_small(const DecodeParams& p, int grid, cudaStream_t stream) {
   const size_t smem = 128 + kSmPreOff + (size_t)(p.num_reqs + 1) * 4;   // grid CTAs = 8 x grid split units
-  cudaError_t e = cudaFuncSetAttribute(decode_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_small_kernel<PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_small_kernel<<<grid, kSmWarps * 32, smem, stream>>>(p);
+  decode_small_kernel<PF><<<grid, kSmWarps * 32, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)p.num_reqs * p.R;
@@ -1208,7 +1257,7 @@ static cudaError_t launch_decode_small(const DecodeParams& p, int grid, cudaStre
 
 template <class PF>
 static cudaError_t launch_decode_pf(const DecodeParams& p, int grid, cudaStream_t stream) {
-  if (!PF::kBf16 && p.R <= kSmRows) return launch_decode_small(p, grid, stream);
+  if (p.R <= kSmRows) return launch_decode_small<PF>(p, grid, stream);
   switch (decode_nq(p.R)) {
     case 16: return launch_decode_nq<16, PF>(p, grid, stream);
     case 32: return launch_decode_nq<32, PF>(p, grid, stream);
