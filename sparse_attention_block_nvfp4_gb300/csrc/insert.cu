@@ -9,6 +9,7 @@
 // quotient rounded so that ties fall exactly (nvfp4_ratio), the scales from
 // the E4M3 conversion of a 12-bit rounding of amax / 6 (e4m3_scale_of_amax).
 // HBM-bound: 256 B read + 8 B slot + 72 B written per token.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -148,58 +149,162 @@ __device__ __forceinline__ float norm_rope_sumsq(float tA, float tB) {
   }
 }
 
-// One 16-element group of a token (two 16-byte words of bf16, loaded at
-// entry) widened to fp32, and the group sum of squares t = e + o (even / odd
-// running sums, one rounding per step).
-__device__ __forceinline__ float norm_rope_widen_group(const uint4 (&v)[2], float (&x)[16]) {
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      x[8 * i + 2 * h] = __uint_as_float(w[h] << 16);
-      x[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
-    }
-  }
-  float e = 0.0f, o = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    e = __fmaf_rn(x[2 * i], x[2 * i], e);
-    o = __fmaf_rn(x[2 * i + 1], x[2 * i + 1], o);
-  }
-  return __fadd_rn(e, o);
+// Two fp32 values in one 64-bit register (element 2i in the low word,
+// 2i + 1 in the high word) and the packed fp32 instructions of sm_100-family
+// GPUs, whose lanes each round as the scalar instruction does (round to
+// nearest even, subnormals kept): the same results as scalar code, bit for
+// bit, from half the instructions.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// The two bf16 halves of a word as an exact fp32 pair.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+  return ((uint64_t)(w & 0xFFFF0000u) << 32) | (uint32_t)(w << 16);
 }
 
-// y = (x * rs) * w for one group (w: the group's 16 bf16 weights).
-__device__ __forceinline__ void norm_rope_scale_group(const uint16_t* wg, float rs, float (&x)[16]) {
+// One 16-element group of a token (two 16-byte words of bf16, loaded at
+// entry) widened to 8 fp32 pairs, and the group sum of squares t = e + o
+// (running sums of the even / odd elements' squares, one rounding per step:
+// the two lanes of one packed fused multiply-add).
+__device__ __forceinline__ float norm_rope_widen_group(const uint4 (&v)[2], uint64_t (&x)[8]) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wg) + i);
-    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+    x[4 * i] = bf16x2_to_f2(v[i].x);
+    x[4 * i + 1] = bf16x2_to_f2(v[i].y);
+    x[4 * i + 2] = bf16x2_to_f2(v[i].z);
+    x[4 * i + 3] = bf16x2_to_f2(v[i].w);
+  }
+  uint64_t eo = 0;
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      x[8 * i + 2 * h] = __fmul_rn(__fmul_rn(x[8 * i + 2 * h], rs), __uint_as_float(w[h] << 16));
-      x[8 * i + 2 * h + 1] = __fmul_rn(__fmul_rn(x[8 * i + 2 * h + 1], rs), __uint_as_float(w[h] & 0xFFFF0000u));
-    }
+  for (int i = 0; i < 8; ++i) eo = f2_fma(x[i], x[i], eo);
+  return __fadd_rn(f2_lo(eo), f2_hi(eo));
+}
+
+// y = (x * rs) * w for one group (wg: the group's 16 bf16 weights; the
+// loads do not depend on the token, so they stay out of the token loop).
+__device__ __forceinline__ void norm_rope_scale_group(const uint16_t* wg, uint64_t rs2, uint64_t (&x)[8]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(wg) + i);
+    x[4 * i] = f2_mul(f2_mul(x[4 * i], rs2), bf16x2_to_f2(w.x));
+    x[4 * i + 1] = f2_mul(f2_mul(x[4 * i + 1], rs2), bf16x2_to_f2(w.y));
+    x[4 * i + 2] = f2_mul(f2_mul(x[4 * i + 2], rs2), bf16x2_to_f2(w.z));
+    x[4 * i + 3] = f2_mul(f2_mul(x[4 * i + 3], rs2), bf16x2_to_f2(w.w));
   }
 }
 
 // bf16 rounding of one group, its amax from the bf16 words, the NVFP4
-// codes (c0, c1) and the returned scale byte.
-__device__ __forceinline__ uint32_t norm_rope_encode_group(float (&x)[16], uint32_t& c0, uint32_t& c1) {
+// codes (c0, c1) and the returned scale byte.  The quotients are those of
+// nvfp4_ratio taken on the signed value: x r + 3 * 2^10 lies in
+// (2^11, 2^12) for |x r| < 2^10, where the ulp is 2^-12 as above 3 * 2^10,
+// and round-to-nearest-even on that grid is symmetric about 3 * 2^10 (an
+// even multiple of 2^-12), so the difference is minus the rounding of
+// |x| r; the sign of x is put back for the quotients that round to zero.
+__device__ __forceinline__ uint32_t norm_rope_encode_group(const uint64_t (&x)[8], uint32_t& c0, uint32_t& c1) {
   uint32_t R[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(R[i]) : "f"(x[2 * i + 1]), "f"(x[2 * i]));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(R[i]) : "f"(f2_hi(x[i])), "f"(f2_lo(x[i])));
   uint32_t mx = R[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) mx = bf16x2_max_abs(mx, R[i]);
+  const uint32_t sb = e4m3_scale_of_amax(bf16x2_amax_f32(mx));
+  const float s = e4m3_to_f32(sb);
+  float q[16];
+  if (s > 0.0f) {
+    const float r = rcp_approx(s);
+    const uint64_t r2 = f2_pack(r, r), k2 = f2_pack(3072.0f, 3072.0f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = __uint_as_float(R[i] << 16);
-    x[2 * i + 1] = __uint_as_float(R[i] & 0xFFFF0000u);
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t g = f2_sub(f2_fma(bf16x2_to_f2(R[i]), r2, k2), k2);
+      q[2 * i] = __uint_as_float(__float_as_uint(f2_lo(g)) | ((R[i] << 16) & 0x80000000u));
+      q[2 * i + 1] = __uint_as_float(__float_as_uint(f2_hi(g)) | (R[i] & 0x80000000u));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      q[2 * i] = __uint_as_float((R[i] << 16) & 0x80000000u);
+      q[2 * i + 1] = __uint_as_float(R[i] & 0x80000000u);
+    }
   }
-  return nvfp4_encode16(x, bf16x2_amax_f32(mx), c0, c1);
+  c0 = f32x8_to_e2m1x8(q);
+  c1 = f32x8_to_e2m1x8(q + 8);
+  return sb;
+}
+
+// One token's two key groups, slot and position, loaded independently (a
+// skipped token's key is read and dropped; past the end nothing is read).
+template <int kMode>
+__device__ __forceinline__ void norm_rope_load(const NormRopeArgs& a, int64_t tok, int gA, int gB,
+                                               uint4 (&ka)[2], uint4 (&kb)[2], int64_t& slot,
+                                               int64_t& pos) {
+  const bool live = tok < a.n;
+  ka[0] = ka[1] = kb[0] = kb[1] = make_uint4(0u, 0u, 0u, 0u);
+  if (live) {
+    const uint4* kt = reinterpret_cast<const uint4*>(a.k + tok * 128);
+    ka[0] = __ldg(kt + 2 * gA);
+    ka[1] = __ldg(kt + 2 * gA + 1);
+    kb[0] = __ldg(kt + 2 * gB);
+    kb[1] = __ldg(kt + 2 * gB + 1);
+  }
+  slot = live ? __ldg(a.slots + tok) : -1;
+  pos = (kMode != kNormOnly && live) ? __ldg(a.positions + tok) : 0;
+}
+
+// A token's slot and position checked (an out-of-range one flags the status
+// word and skips the token; the table is read only for a kept token), and
+// the asynchronous copy of its table row started: the row's 16-byte chunks
+// (rd/2 cosines, then rd/2 sines) go round the token's 4 lanes, lane j
+// taking chunks j, j + 4, ..., so that each copy instruction of a warp reads
+// 64 contiguous bytes per token.  Chunk c lands at row[c + c / 8] (one pad
+// chunk per 8), which puts the chunks 4j + v that lane j reads back on four
+// different bank quads.
+template <int kMode>
+__device__ __forceinline__ bool norm_rope_accept(const NormRopeArgs& a, int j, int64_t& slot, int64_t& pos,
+                                                 float4* row) {
+  if (slot >= a.num_slots) {
+    if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadSlot);
+    slot = -1;
+  }
+  if (kMode != kNormOnly && slot >= 0 && (pos < 0 || pos >= a.max_pos)) {
+    if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadPosition);
+    slot = -1;
+  }
+  if (slot < 0) pos = 0;
+  const bool vec = kMode == kNeox128 || kMode == kNeox64 || (a.rotary_dim & 7) == 0;
+  if (kMode != kNormOnly && slot >= 0 && vec) {
+    const float* cs = a.cos_sin + pos * a.rotary_dim;
+    const int nc = kMode == kNeox128 ? 32 : kMode == kNeox64 ? 16 : a.rotary_dim >> 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = 4 * i + j;
+      if (c < nc) cp_async16(row + c + (c >> 3), cs + 4 * c);
+    }
+  }
+  cp_async_commit();
+  return slot >= 0;
 }
 
 // qk-norm + RoPE + NVFP4 quantise-and-scatter: the fused insert that writes
@@ -216,148 +321,162 @@ __device__ __forceinline__ uint32_t norm_rope_encode_group(float (&x)[16], uint3
 // y2 c + y1 s) with every product and sum rounded (no fused multiply-add).
 // Four threads per token, each holding two whole groups, chosen so that a
 // NeoX pair (i, i + rd/2) sits in one thread (rd 64 or 128); GPT-J pairs
-// (2i, 2i + 1) stay inside a thread anyway.  At entry each thread starts an
-// asynchronous copy of its 16 cosines and 16 sines into shared memory, so the
-// table's latency hides behind the norm; the key loads are issued first,
-// independently of the slot and the position.  HBM-bound: 256 B
-// key + 8 B slot + 8 B position + 72 B row per token, plus the table rows.
+// (2i, 2i + 1) stay inside a thread anyway.  The element-wise steps run on
+// packed fp32 pairs.  The grid is persistent (as many CTAs as fit at once),
+// each group of 4 threads stepping through the tokens with the grid's
+// stride, and the loads run one token ahead: the key groups, slot and
+// position of the next token are issued before the current one is
+// computed, and the asynchronous copy of the next token's table row into
+// shared memory when the current one is written.  The CTAs have 128 threads
+// and up to 96 registers (5 per SM): with the loads one token ahead the
+// kernel is limited by the L1 load pipe, not by the warps in flight.
+// HBM-bound: 256 B key + 8 B slot + 8 B position + 72 B row per token, plus
+// the table rows.
 template <int kMode>
-__global__ void __launch_bounds__(256) nvfp4_insert_norm_rope_kernel(const NormRopeArgs a) {
-  // per thread: 16 cosines, 16 sines; rows padded to 36 floats so that the
-  // 16-byte reads of 8 consecutive lanes fall on 8 different bank quads
-  __shared__ __align__(16) float tab_s[256][36];
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t tok = tid >> 2;
-  const int j = (int)(tid & 3);
-  const bool live = tok < a.n;
+__global__ void __launch_bounds__(128, 5) nvfp4_insert_norm_rope_kernel(const NormRopeArgs a) {
+  // per token: its table row in 16-byte chunks at c + c / 8, rows 42 chunks
+  // apart, so that the two tokens of a quarter warp read different bank quads
+  __shared__ __align__(16) float4 row_s[32][42];
+  float4* row = row_s[threadIdx.x >> 2];
+  const int j = (int)(threadIdx.x & 3);
   int gA, gB;
   norm_rope_groups<kMode>(j, gA, gB);
-  // the key's two groups, the slot and the position load independently (a
-  // skipped token's key is read and dropped)
-  uint4 ka[2] = {}, kb[2] = {};
-  if (live) {
-    const uint4* kt = reinterpret_cast<const uint4*>(a.k + tok * 128);
-    ka[0] = __ldg(kt + 2 * gA);
-    ka[1] = __ldg(kt + 2 * gA + 1);
-    kb[0] = __ldg(kt + 2 * gB);
-    kb[1] = __ldg(kt + 2 * gB + 1);
-  }
-  int64_t slot = live ? __ldg(a.slots + tok) : -1;
-  int64_t pos = (kMode != kNormOnly && live) ? __ldg(a.positions + tok) : 0;
-  if (slot >= a.num_slots) {
-    if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadSlot);
-    slot = -1;
-  }
-  if (kMode != kNormOnly && slot >= 0 && (pos < 0 || pos >= a.max_pos)) {
-    if (j == 0 && a.status) atomicOr(a.status, (int32_t)kStatusBadPosition);
-    slot = -1;
-  }
-  if (slot < 0) pos = 0;                           // the table is read only for a kept token
-  const bool act = slot >= 0;
-
-  // table slice: pairs p0 .. p0 + 15 (those below rd/2), cosines and sines
   const int h = a.rotary_dim >> 1, p0 = 16 * j;
-  const bool rot = kMode != kNormOnly && act && p0 < h;
   const bool vec = kMode == kNeox128 || kMode == kNeox64 || (a.rotary_dim & 7) == 0;
-  const float* cs = a.cos_sin + pos * a.rotary_dim;
-  float* tab = tab_s[threadIdx.x];
-  if (rot && vec) {
-    const int nchunk = min(4, (h - p0) >> 2);      // h - p0 is a multiple of 4 here
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      if (v < nchunk) {
-        cp_async16(tab + 4 * v, cs + p0 + 4 * v);
-        cp_async16(tab + 16 + 4 * v, cs + h + p0 + 4 * v);
-      }
-    }
-  }
-  cp_async_commit();
+  const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 2);
+  const int64_t tok0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 2;
+  const int lane_tok = (int)((threadIdx.x & 31) >> 2);   // the warp steps while its first token is live
 
-  float xa[16], xb[16];
-  const float tA = norm_rope_widen_group(ka, xa);
-  const float tB = norm_rope_widen_group(kb, xb);
-  const float ss = norm_rope_sumsq<kMode>(tA, tB);
-  const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
-  norm_rope_scale_group(a.weight + 16 * gA, rs, xa);
-  norm_rope_scale_group(a.weight + 16 * gB, rs, xb);
+  uint4 ka[2], kb[2];
+  int64_t slot, pos;
+  norm_rope_load<kMode>(a, tok0, gA, gB, ka, kb, slot, pos);
+  bool act = norm_rope_accept<kMode>(a, j, slot, pos, row);
+  for (int64_t tok = tok0; tok - lane_tok < a.n; tok += stride) {
+    uint4 na[2], nb[2];
+    int64_t nslot, npos;
+    norm_rope_load<kMode>(a, tok + stride, gA, gB, na, nb, nslot, npos);
 
-  cp_async_wait_all();
-  if constexpr (kMode == kNeox128 || kMode == kNeox64) {
-    if (rot) {                       // element i of gA pairs with element i of gB (pair p0 + i)
+    uint64_t xa[8], xb[8];
+    const float tA = norm_rope_widen_group(ka, xa);
+    const float tB = norm_rope_widen_group(kb, xb);
+    const float ss = norm_rope_sumsq<kMode>(tA, tB);
+    const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
+    const uint64_t rs2 = f2_pack(rs, rs);
+    norm_rope_scale_group(a.weight + 16 * gA, rs2, xa);
+    norm_rope_scale_group(a.weight + 16 * gB, rs2, xb);
+
+    const bool rot = kMode != kNormOnly && act && p0 < h;
+    cp_async_wait_all();
+    __syncwarp();                    // the row, copied by the token's 4 lanes
+    if constexpr (kMode == kNeox128 || kMode == kNeox64) {
+      if (rot) {                       // element i of gA pairs with element i of gB (pair p0 + i)
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const float4 c4 = *reinterpret_cast<const float4*>(tab + 4 * v);
-        const float4 s4 = *reinterpret_cast<const float4*>(tab + 16 + 4 * v);
-        const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+        for (int v = 0; v < 4; ++v) {
+          const int c = 4 * j + v, sn_c = (h >> 2) + 4 * j + v;
+          const ulonglong2 c4 = *reinterpret_cast<const ulonglong2*>(row + c + (c >> 3));
+          const ulonglong2 s4 = *reinterpret_cast<const ulonglong2*>(row + sn_c + (sn_c >> 3));
+          const uint64_t cc[2] = {c4.x, c4.y}, sn[2] = {s4.x, s4.y};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 4 * v + u;
-          const float y1 = xa[i], y2 = xb[i];
-          xa[i] = __fsub_rn(__fmul_rn(y1, cc[u]), __fmul_rn(y2, sn[u]));
-          xb[i] = __fadd_rn(__fmul_rn(y2, cc[u]), __fmul_rn(y1, sn[u]));
+          for (int u = 0; u < 2; ++u) {
+            const int i = 2 * v + u;
+            const uint64_t y1 = xa[i], y2 = xb[i];
+            xa[i] = f2_sub(f2_mul(y1, cc[u]), f2_mul(y2, sn[u]));
+            xb[i] = f2_add(f2_mul(y2, cc[u]), f2_mul(y1, sn[u]));
+          }
         }
       }
-    }
-  } else if constexpr (kMode == kGptj) {
-    if (rot) {                       // pair p0 + q = elements 32j + 2q, 32j + 2q + 1
+    } else if constexpr (kMode == kGptj) {
+      if (rot) {                       // pair p0 + q = elements 32j + 2q, 32j + 2q + 1
+        const float* cs = a.cos_sin + pos * a.rotary_dim;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        float cc[4], sn[4];
-        if (vec) {
-          const float4 c4 = *reinterpret_cast<const float4*>(tab + 4 * v);
-          const float4 s4 = *reinterpret_cast<const float4*>(tab + 16 + 4 * v);
-          cc[0] = c4.x; cc[1] = c4.y; cc[2] = c4.z; cc[3] = c4.w;
-          sn[0] = s4.x; sn[1] = s4.y; sn[2] = s4.z; sn[3] = s4.w;
-        } else {
+        for (int v = 0; v < 4; ++v) {
+          float cc[4], sn[4];
+          if (vec) {
+            const int c = 4 * j + v, sn_c = (h >> 2) + 4 * j + v;
+            const float4 c4 = row[c + (c >> 3)];
+            const float4 s4 = row[sn_c + (sn_c >> 3)];
+            cc[0] = c4.x; cc[1] = c4.y; cc[2] = c4.z; cc[3] = c4.w;
+            sn[0] = s4.x; sn[1] = s4.y; sn[2] = s4.z; sn[3] = s4.w;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const bool in = p0 + 4 * v + u < h;
+              cc[u] = in ? __ldg(cs + p0 + 4 * v + u) : 0.0f;
+              sn[u] = in ? __ldg(cs + h + p0 + 4 * v + u) : 0.0f;
+            }
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const bool in = p0 + 4 * v + u < h;
-            cc[u] = in ? __ldg(cs + p0 + 4 * v + u) : 0.0f;
-            sn[u] = in ? __ldg(cs + h + p0 + 4 * v + u) : 0.0f;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int q = 4 * v + u;
-          if (p0 + q < h) {
-            float* xs = q < 8 ? xa : xb;
-            const int e = 2 * (q & 7);
-            const float y1 = xs[e], y2 = xs[e + 1];
-            xs[e] = __fsub_rn(__fmul_rn(y1, cc[u]), __fmul_rn(y2, sn[u]));
-            xs[e + 1] = __fadd_rn(__fmul_rn(y2, cc[u]), __fmul_rn(y1, sn[u]));
+            const int q = 4 * v + u;
+            if (p0 + q < h) {
+              uint64_t& xs = q < 8 ? xa[q] : xb[q - 8];
+              const float y1 = f2_lo(xs), y2 = f2_hi(xs);
+              xs = f2_pack(__fsub_rn(__fmul_rn(y1, cc[u]), __fmul_rn(y2, sn[u])),
+                           __fadd_rn(__fmul_rn(y2, cc[u]), __fmul_rn(y1, sn[u])));
+            }
           }
         }
       }
     }
-  }
 
-  uint32_t ca0, ca1, cb0, cb1;
-  const uint32_t sbA = norm_rope_encode_group(xa, ca0, ca1);
-  const uint32_t sbB = norm_rope_encode_group(xb, cb0, cb1);
-  // the token's 8 scale bytes, byte g from the lane holding group g
-  uint32_t lo = (gA < 4 ? sbA << (8 * gA) : 0u) | (gB < 4 ? sbB << (8 * gB) : 0u);
-  uint32_t hi = (gA >= 4 ? sbA << (8 * (gA - 4)) : 0u) | (gB >= 4 ? sbB << (8 * (gB - 4)) : 0u);
-  lo |= __shfl_xor_sync(0xffffffffu, lo, 1);
-  hi |= __shfl_xor_sync(0xffffffffu, hi, 1);
-  lo |= __shfl_xor_sync(0xffffffffu, lo, 2);
-  hi |= __shfl_xor_sync(0xffffffffu, hi, 2);
-  if (act) {
-    uint8_t* row = a.pages + slot * 72;
-    *reinterpret_cast<uint2*>(row + 8 * gA) = make_uint2(ca0, ca1);
-    *reinterpret_cast<uint2*>(row + 8 * gB) = make_uint2(cb0, cb1);
-    if (j == 0) *reinterpret_cast<uint2*>(row + 64) = make_uint2(lo, hi);
+    uint32_t ca0, ca1, cb0, cb1;
+    const uint32_t sbA = norm_rope_encode_group(xa, ca0, ca1);
+    const uint32_t sbB = norm_rope_encode_group(xb, cb0, cb1);
+    // the token's 8 scale bytes, byte g from the lane holding group g
+    uint32_t lo = (gA < 4 ? sbA << (8 * gA) : 0u) | (gB < 4 ? sbB << (8 * gB) : 0u);
+    uint32_t hi = (gA >= 4 ? sbA << (8 * (gA - 4)) : 0u) | (gB >= 4 ? sbB << (8 * (gB - 4)) : 0u);
+    lo |= __shfl_xor_sync(0xffffffffu, lo, 1);
+    hi |= __shfl_xor_sync(0xffffffffu, hi, 1);
+    lo |= __shfl_xor_sync(0xffffffffu, lo, 2);
+    hi |= __shfl_xor_sync(0xffffffffu, hi, 2);
+    if (act) {
+      uint8_t* row = a.pages + slot * 72;
+      *reinterpret_cast<uint2*>(row + 8 * gA) = make_uint2(ca0, ca1);
+      *reinterpret_cast<uint2*>(row + 8 * gB) = make_uint2(cb0, cb1);
+      if (j == 0) *reinterpret_cast<uint2*>(row + 64) = make_uint2(lo, hi);
+    }
+
+    // the next token becomes the current one; its table row is copied once
+    // every lane has read this token's
+    ka[0] = na[0];
+    ka[1] = na[1];
+    kb[0] = nb[0];
+    kb[1] = nb[1];
+    slot = nslot;
+    pos = npos;
+    __syncwarp();                    // every lane is done with the row
+    act = norm_rope_accept<kMode>(a, j, slot, pos, row);
   }
+  cp_async_wait_all();
+}
+
+// CTAs of the persistent fused insert that fit on the device at once.
+template <int kMode>
+static int norm_rope_grid(int64_t n) {
+  static int per_sm = 0, sms = 0;
+  if (per_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nvfp4_insert_norm_rope_kernel<kMode>, 128, 0) !=
+            cudaSuccess || per_sm < 1)
+      per_sm = 1, sms = sms > 0 ? sms : 1;
+  }
+  const int64_t need = (n * 4 + 127) / 128;
+  return (int)std::min<int64_t>(need, (int64_t)per_sm * sms);
 }
 
 cudaError_t launch_insert_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   if (a.n <= 0) return cudaSuccess;
-  const int64_t threads = (int64_t)a.n * 4;
-  const int block = 256;
-  const unsigned grid = (unsigned)((threads + block - 1) / block);
-  if (a.rotary_dim == 0) nvfp4_insert_norm_rope_kernel<kNormOnly><<<grid, block, 0, stream>>>(a);
-  else if (a.is_neox && a.rotary_dim == 128) nvfp4_insert_norm_rope_kernel<kNeox128><<<grid, block, 0, stream>>>(a);
-  else if (a.is_neox) nvfp4_insert_norm_rope_kernel<kNeox64><<<grid, block, 0, stream>>>(a);
-  else nvfp4_insert_norm_rope_kernel<kGptj><<<grid, block, 0, stream>>>(a);
+  const int block = 128;
+  if (a.rotary_dim == 0)
+    nvfp4_insert_norm_rope_kernel<kNormOnly><<<norm_rope_grid<kNormOnly>(a.n), block, 0, stream>>>(a);
+  else if (a.is_neox && a.rotary_dim == 128)
+    nvfp4_insert_norm_rope_kernel<kNeox128><<<norm_rope_grid<kNeox128>(a.n), block, 0, stream>>>(a);
+  else if (a.is_neox)
+    nvfp4_insert_norm_rope_kernel<kNeox64><<<norm_rope_grid<kNeox64>(a.n), block, 0, stream>>>(a);
+  else
+    nvfp4_insert_norm_rope_kernel<kGptj><<<norm_rope_grid<kGptj>(a.n), block, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
