@@ -254,9 +254,19 @@ __device__ __forceinline__ uint32_t norm_rope_encode_group(const uint64_t (&x)[8
   return sb;
 }
 
+// 32 bytes from a 32-byte aligned address of read-only global memory in one
+// load (the 256-bit form of sm_100-family GPUs): both 16-byte halves of a
+// sector in one request.
+__device__ __forceinline__ void ldg_32B(const uint4* p, uint4& lo, uint4& hi) {
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+      : "l"(p));
+}
+
 // One token's two key groups, slot and position, loaded independently (a
 // skipped token's key is read and dropped; past the end nothing is read).
-template <int kMode>
+// kWide: the keys are 32-byte aligned and each group comes in one load.
+template <int kMode, bool kWide>
 __device__ __forceinline__ void norm_rope_load(const NormRopeArgs& a, int64_t tok, int gA, int gB,
                                                uint4 (&ka)[2], uint4 (&kb)[2], int64_t& slot,
                                                int64_t& pos) {
@@ -264,10 +274,15 @@ __device__ __forceinline__ void norm_rope_load(const NormRopeArgs& a, int64_t to
   ka[0] = ka[1] = kb[0] = kb[1] = make_uint4(0u, 0u, 0u, 0u);
   if (live) {
     const uint4* kt = reinterpret_cast<const uint4*>(a.k + tok * 128);
-    ka[0] = __ldg(kt + 2 * gA);
-    ka[1] = __ldg(kt + 2 * gA + 1);
-    kb[0] = __ldg(kt + 2 * gB);
-    kb[1] = __ldg(kt + 2 * gB + 1);
+    if constexpr (kWide) {
+      ldg_32B(kt + 2 * gA, ka[0], ka[1]);
+      ldg_32B(kt + 2 * gB, kb[0], kb[1]);
+    } else {
+      ka[0] = __ldg(kt + 2 * gA);
+      ka[1] = __ldg(kt + 2 * gA + 1);
+      kb[0] = __ldg(kt + 2 * gB);
+      kb[1] = __ldg(kt + 2 * gB + 1);
+    }
   }
   slot = live ? __ldg(a.slots + tok) : -1;
   pos = (kMode != kNormOnly && live) ? __ldg(a.positions + tok) : 0;
@@ -332,7 +347,7 @@ __device__ __forceinline__ bool norm_rope_accept(const NormRopeArgs& a, int j, i
 // kernel is limited by the L1 load pipe, not by the warps in flight.
 // HBM-bound: 256 B key + 8 B slot + 8 B position + 72 B row per token, plus
 // the table rows.
-template <int kMode>
+template <int kMode, bool kWide>
 __global__ void __launch_bounds__(128, 5) nvfp4_insert_norm_rope_kernel(const NormRopeArgs a) {
   // per token: its table row in 16-byte chunks at c + c / 8, rows 42 chunks
   // apart, so that the two tokens of a quarter warp read different bank quads
@@ -349,12 +364,12 @@ __global__ void __launch_bounds__(128, 5) nvfp4_insert_norm_rope_kernel(const No
 
   uint4 ka[2], kb[2];
   int64_t slot, pos;
-  norm_rope_load<kMode>(a, tok0, gA, gB, ka, kb, slot, pos);
+  norm_rope_load<kMode, kWide>(a, tok0, gA, gB, ka, kb, slot, pos);
   bool act = norm_rope_accept<kMode>(a, j, slot, pos, row);
   for (int64_t tok = tok0; tok - lane_tok < a.n; tok += stride) {
     uint4 na[2], nb[2];
     int64_t nslot, npos;
-    norm_rope_load<kMode>(a, tok + stride, gA, gB, na, nb, nslot, npos);
+    norm_rope_load<kMode, kWide>(a, tok + stride, gA, gB, na, nb, nslot, npos);
 
     uint64_t xa[8], xb[8];
     const float tA = norm_rope_widen_group(ka, xa);
@@ -451,32 +466,36 @@ __global__ void __launch_bounds__(128, 5) nvfp4_insert_norm_rope_kernel(const No
 }
 
 // CTAs of the persistent fused insert that fit on the device at once.
-template <int kMode>
+template <int kMode, bool kWide>
 static int norm_rope_grid(int64_t n) {
   static int per_sm = 0, sms = 0;
   if (per_sm == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nvfp4_insert_norm_rope_kernel<kMode>, 128, 0) !=
-            cudaSuccess || per_sm < 1)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nvfp4_insert_norm_rope_kernel<kMode, kWide>, 128,
+                                                      0) != cudaSuccess ||
+        per_sm < 1)
       per_sm = 1, sms = sms > 0 ? sms : 1;
   }
   const int64_t need = (n * 4 + 127) / 128;
   return (int)std::min<int64_t>(need, (int64_t)per_sm * sms);
 }
 
+template <int kMode>
+static void launch_norm_rope_mode(const NormRopeArgs& a, cudaStream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(a.k) & 31u) == 0)
+    nvfp4_insert_norm_rope_kernel<kMode, true><<<norm_rope_grid<kMode, true>(a.n), 128, 0, stream>>>(a);
+  else
+    nvfp4_insert_norm_rope_kernel<kMode, false><<<norm_rope_grid<kMode, false>(a.n), 128, 0, stream>>>(a);
+}
+
 cudaError_t launch_insert_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   if (a.n <= 0) return cudaSuccess;
-  const int block = 128;
-  if (a.rotary_dim == 0)
-    nvfp4_insert_norm_rope_kernel<kNormOnly><<<norm_rope_grid<kNormOnly>(a.n), block, 0, stream>>>(a);
-  else if (a.is_neox && a.rotary_dim == 128)
-    nvfp4_insert_norm_rope_kernel<kNeox128><<<norm_rope_grid<kNeox128>(a.n), block, 0, stream>>>(a);
-  else if (a.is_neox)
-    nvfp4_insert_norm_rope_kernel<kNeox64><<<norm_rope_grid<kNeox64>(a.n), block, 0, stream>>>(a);
-  else
-    nvfp4_insert_norm_rope_kernel<kGptj><<<norm_rope_grid<kGptj>(a.n), block, 0, stream>>>(a);
+  if (a.rotary_dim == 0) launch_norm_rope_mode<kNormOnly>(a, stream);
+  else if (a.is_neox && a.rotary_dim == 128) launch_norm_rope_mode<kNeox128>(a, stream);
+  else if (a.is_neox) launch_norm_rope_mode<kNeox64>(a, stream);
+  else launch_norm_rope_mode<kGptj>(a, stream);
   return cudaGetLastError();
 }
 

@@ -154,6 +154,36 @@ def test_norm_rope_insert_bad_positions_and_slots():
         run_gpu(k, pos, slots, w, -1.0, table, 128, True, 1)
 
 
+@pytest.mark.parametrize("rd,neox", [(128, True), (64, True), (40, False), (6, False), (0, True)])
+def test_norm_rope_insert_keys_16_byte_aligned(rd, neox):
+    """Keys at an address that is 16-byte but not 32-byte aligned (the
+    kernel then loads each group in two 16-byte halves instead of one
+    32-byte load): the same rows as from 32-byte aligned keys, and within
+    the oracle's check."""
+    import torch
+    import sparse_attention_block_nvfp4_gb300 as idx
+    n = 3000
+    k, w, pos = case(n, 90 + rd + neox)
+    nb = (n + 127) // 128 + 1
+    slots = np.arange(n, dtype=np.int64)[::-1].copy()
+    slots[::7] = -1
+    table = rope_table(4096, rd) if rd else None
+    outs = []
+    for off in (0, 8):                            # int16 elements: 0 or 16 bytes
+        buf = torch.zeros(n * 128 + 16, dtype=torch.int16, device=torch_dev())
+        kd = buf[off:off + n * 128].view(n, 128)
+        kd.copy_(up(k.view(np.int16)))
+        assert (kd.data_ptr() % 32 == 0) == (off == 0) and kd.data_ptr() % 16 == 0
+        kv = torch.full((nb, 128, 72), 0x21, dtype=torch.uint8, device=torch_dev())
+        status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+        idx.insert_norm_rope(kd, up(pos), up(slots), up(w.view(np.int16)), 1e-6,
+                             up(table) if table is not None else None, rd, neox, kv, status=status)
+        assert int(status.item()) == 0
+        outs.append(kv.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    assert_rows(outs[1], k, pos, slots, w, 1e-6, table, rd, neox, 0x21, f"16-byte aligned keys, rd {rd}")
+
+
 def test_norm_rope_insert_full_cache_sampled():
     """The long mixed workload's whole cache (2.24 M keys, each request's
     tokens at positions 0 .. seq_len - 1), in the launch configuration the
