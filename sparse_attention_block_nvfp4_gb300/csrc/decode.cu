@@ -724,6 +724,7 @@ __global__ void __launch_bounds__(W * 32) decode_merge_kernel(const DecodeParams
   if (gw >= (int64_t)p.num_reqs * p.R) return;
   const int r = (int)(gw / p.R), n = (int)(gw % p.R);
   const int seq = __ldg(p.seq_lens + r);
+  const int2 info = p.req_info[r];                   // loaded with seq, not after it
   const int pos = seq - p.qlen + n / p.H;
   const int L = pos >= 0 ? (pos >> 7) : -1;
   const int hist = seq >= 1 ? (seq - 1) >> 7 : 0;
@@ -742,7 +743,6 @@ __global__ void __launch_bounds__(W * 32) decode_merge_kernel(const DecodeParams
     }
     return;
   }
-  const int2 info = p.req_info[r];
   const int nseg = info.y;
   if (nseg == 1) return;                      // finalised by the scoring kernel
   if (nseg == 0) {                            // no history page (in the share): local page only
@@ -750,6 +750,23 @@ __global__ void __launch_bounds__(W * 32) decode_merge_kernel(const DecodeParams
     return;
   }
   const int slot0 = info.x + r;
+  // up to kLists lists: loaded into registers together with the segments'
+  // bad flags (one memory latency, not two; dropped if a flag is set)
+  float2 e[kHeads][kHistK];
+  if (nseg <= kLists) {
+#pragma unroll
+    for (int hh = 0; hh < kHeads; ++hh) {
+      const int li = lane + 32 * hh;
+      if (li < nseg) {
+        const float2* src = p.cand + ((int64_t)(slot0 + li) * p.R + n) * kHistK;
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) e[hh][k] = src[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < kHistK; ++k) e[hh][k] = make_float2(0.0f, __int_as_float(-1));
+      }
+    }
+  }
   int bad = 0;
   for (int k = lane; k < nseg; k += 32) bad |= p.slot_bad[slot0 + k];
   if (__any_sync(0xffffffffu, bad)) {
@@ -761,14 +778,8 @@ __global__ void __launch_bounds__(W * 32) decode_merge_kernel(const DecodeParams
     const int li = lane + 32 * hh;
     float2(&mine)[kHistK] = lists[warp][li];
     if (nseg <= kLists) {
-      if (li < nseg) {
-        const float2* src = p.cand + ((int64_t)(slot0 + li) * p.R + n) * kHistK;
 #pragma unroll
-        for (int k = 0; k < kHistK; ++k) mine[k] = src[k];
-      } else {
-#pragma unroll
-        for (int k = 0; k < kHistK; ++k) mine[k] = make_float2(0.0f, __int_as_float(-1));
-      }
+      for (int k = 0; k < kHistK; ++k) mine[k] = e[hh][k];
     } else {
       // lists li, li + kLists, ... cover ascending page ranges: inserted in
       // that order, an equal score always comes with a higher id
