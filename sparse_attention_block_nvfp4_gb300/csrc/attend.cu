@@ -100,11 +100,20 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// 32 bytes from a 32-byte aligned address of read-only global memory in one
+// load (the 256-bit form of sm_100-family GPUs).
+__device__ __forceinline__ void att_ldg_32B(const uint4* p, uint4& lo, uint4& hi) {
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+      : "l"(p));
+}
+
 // Registers grow with G (accumulators, scores): fewer K loads in flight and
 // fewer resident CTAs for the larger groups.
 template <int G>
 struct AttCfg {
   static constexpr int kKUnroll = G == 1 ? 16 : (G <= 4 ? 8 : 4);
+  static constexpr int kKUnroll32 = kKUnroll / 2;   // the same bytes in flight with 32-byte loads
   static constexpr int kMinBlocks = G == 1 ? 8 : (G == 2 ? 6 : (G == 4 ? 3 : 2));
   static constexpr int kSmemAcc = kAttSplit * 4 * G * kDim * 4;   // the leader's [CTA][warp][G][kDim]
   // V rows by 16-byte loads: a half warp per token, lane l % 16 on dims
@@ -114,7 +123,32 @@ struct AttCfg {
   static constexpr int kVC = kWideV ? 8 : 4;   // dims per lane
 };
 
+// One 16-byte chunk c of a token's K row (dims 8c .. 8c + 7) into the G
+// heads' dot products with the scaled queries.
 template <int G>
+__device__ __forceinline__ void att_dot8(float (&s)[G], const uint4 kv, const float (&q_s)[G][kDim], int c) {
+  const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float4 qa = *reinterpret_cast<const float4*>(&q_s[g][8 * c]);
+    const float4 qb = *reinterpret_cast<const float4*>(&q_s[g][8 * c + 4]);
+    float a = s[g];
+    a = fmaf(qa.x, bf16_lo(w[0]), a);
+    a = fmaf(qa.y, bf16_hi(w[0]), a);
+    a = fmaf(qa.z, bf16_lo(w[1]), a);
+    a = fmaf(qa.w, bf16_hi(w[1]), a);
+    a = fmaf(qb.x, bf16_lo(w[2]), a);
+    a = fmaf(qb.y, bf16_hi(w[2]), a);
+    a = fmaf(qb.z, bf16_lo(w[3]), a);
+    a = fmaf(qb.w, bf16_hi(w[3]), a);
+    s[g] = a;
+  }
+}
+
+// kWideK: the K cache is 32-byte aligned and each thread reads its token's
+// K row in eight 32-byte loads (whole sectors) instead of sixteen 16-byte
+// ones.
+template <int G, bool kWideK>
 __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads, AttCfg<G>::kMinBlocks)
     sparse_attend_kernel(const AttendParams p) {
   extern __shared__ __align__(16) float acc_all[];     // [kAttSplit * 4 warps][G][kDim], used in CTA 0
@@ -208,25 +242,17 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
       const uint4* krow = reinterpret_cast<const uint4*>(p.k_cache + (base + (int64_t)tid * p.H) * kDim);
 #pragma unroll
       for (int g = 0; g < G; ++g) s[g] = 0.0f;
-#pragma unroll AttCfg<G>::kKUnroll
-      for (int c = 0; c < kDim / 8; ++c) {
-        const uint4 kv = __ldg(krow + c);
-        const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4*>(&q_s[g][8 * c]);
-          const float4 qb = *reinterpret_cast<const float4*>(&q_s[g][8 * c + 4]);
-          float a = s[g];
-          a = fmaf(qa.x, bf16_lo(w[0]), a);
-          a = fmaf(qa.y, bf16_hi(w[0]), a);
-          a = fmaf(qa.z, bf16_lo(w[1]), a);
-          a = fmaf(qa.w, bf16_hi(w[1]), a);
-          a = fmaf(qb.x, bf16_lo(w[2]), a);
-          a = fmaf(qb.y, bf16_hi(w[2]), a);
-          a = fmaf(qb.z, bf16_lo(w[3]), a);
-          a = fmaf(qb.w, bf16_hi(w[3]), a);
-          s[g] = a;
+      if constexpr (kWideK) {
+#pragma unroll AttCfg<G>::kKUnroll32
+        for (int c2 = 0; c2 < kDim / 16; ++c2) {
+          uint4 k0, k1;
+          att_ldg_32B(krow + 2 * c2, k0, k1);
+          att_dot8<G>(s, k0, q_s, 2 * c2);
+          att_dot8<G>(s, k1, q_s, 2 * c2 + 1);
         }
+      } else {
+#pragma unroll AttCfg<G>::kKUnroll
+        for (int c = 0; c < kDim / 8; ++c) att_dot8<G>(s, __ldg(krow + c), q_s, c);
       }
     }
     // ---- the page's maximum per head, the new running maximum
@@ -337,13 +363,19 @@ __global__ void __cluster_dims__(kAttSplit, 1, 1) __launch_bounds__(kAttThreads,
   }
 }
 
+template <int G, bool kWideK>
+static cudaError_t launch_attend_gk(const AttendParams& p, int64_t units, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(sparse_attend_kernel<G, kWideK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, AttCfg<G>::kSmemAcc);
+  if (e != cudaSuccess) return e;
+  sparse_attend_kernel<G, kWideK><<<(unsigned)(units * kAttSplit), kAttThreads, AttCfg<G>::kSmemAcc, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int G>
 static cudaError_t launch_attend_g(const AttendParams& p, int64_t units, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(sparse_attend_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       AttCfg<G>::kSmemAcc);
-  if (e != cudaSuccess) return e;
-  sparse_attend_kernel<G><<<(unsigned)(units * kAttSplit), kAttThreads, AttCfg<G>::kSmemAcc, stream>>>(p);
-  return cudaGetLastError();
+  return (reinterpret_cast<uintptr_t>(p.k_cache) & 31u) == 0 ? launch_attend_gk<G, true>(p, units, stream)
+                                                              : launch_attend_gk<G, false>(p, units, stream);
 }
 
 cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream) {

@@ -41,10 +41,22 @@ def _ids(w, kv):
     return torch.cat(parts).contiguous()
 
 
-def _run(w, G, seed, rows=None, launch_rows=None):
+def _shift16(t):
+    """The same tensor at an address that is 16-byte but not 32-byte aligned."""
+    import torch
+    buf = torch.empty(t.numel() + 16, dtype=t.dtype, device=t.device)
+    assert buf.data_ptr() % 32 == 0 and t.element_size() == 2
+    out = buf[8:8 + t.numel()].view(t.shape)
+    out.copy_(t)
+    assert out.data_ptr() % 32 == 16
+    return out
+
+
+def _run(w, G, seed, rows=None, launch_rows=None, k_shift16=False):
     """Attend over the workload's rows on the GPU (all of them, or the first
     ``launch_rows``); returns the outputs of the listed rows and the oracle's
-    inputs for them."""
+    inputs for them.  k_shift16: the K cache at a 16-byte (not 32-byte)
+    aligned address."""
     import torch
     import sparse_attention_block_nvfp4_gb300 as idx
     kv = gpu_cache(w)
@@ -56,6 +68,8 @@ def _run(w, G, seed, rows=None, launch_rows=None):
     rng = np.random.Generator(np.random.PCG64(seed))
     q_np = workloads.attend_q(nl, H * G, rng)
     kc = workloads.attend_kv_fill(seed, 0, w.num_blocks, H, torch_dev())
+    if k_shift16:
+        kc = _shift16(kc)
     vc = workloads.attend_kv_fill(seed, 1, w.num_blocks, H, torch_dev())
     status = torch.zeros(1, dtype=torch.int32, device=torch_dev())
     out = idx.sparse_attend(up(q_np.view(np.int16)), kc, vc, up(w.page_table), up(req), up(pos), ids_t, SCALE,
@@ -105,6 +119,21 @@ def test_attend_matches_oracle_small(cfg, G):
     o, b, n = _oracle(w, G, seed, q, req, pos, ids)
     _assert_close(got, o, b, f"{w.name} G={G}")
     assert np.all(got[n == 0] == 0)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_attend_k_cache_16_byte_aligned(G):
+    """A K cache at an address that is 16-byte but not 32-byte aligned (the
+    kernel then reads each K row in sixteen 16-byte loads instead of eight
+    32-byte ones, in the same order): the same outputs, bit for bit, as from
+    the 32-byte aligned cache, and within the oracle's bound."""
+    w = workloads.config(0)
+    seed = 520
+    got, (q, req, pos, ids) = _run(w, G, seed)
+    got16, _ = _run(w, G, seed, k_shift16=True)
+    assert np.array_equal(got, got16)
+    o, b, n = _oracle(w, G, seed, q, req, pos, ids)
+    _assert_close(got16, o, b, f"{w.name} G={G}, K cache 16-byte aligned")
 
 
 def test_attend_edge_rows():
