@@ -101,3 +101,28 @@ def test_traffic_needs_current_kernel_hash(tmp_path, monkeypatch):
     # a shared header voids both
     (tmp_path / "sparse_attention_block_nvfp4_gb300" / "csrc" / "ptx.cuh").write_text("changed")
     assert bench.recorded_traffic("decode", "long_mixed") is None
+
+
+def test_kernel_deps_cover_every_included_header():
+    """Each timed kernel's hash covers its .cu and every header it includes
+    (directly or through another header), so that a change to any of them
+    voids the kernel's committed DRAM-traffic record."""
+    import re
+    base = os.path.join(bench.ROOT, "sparse_attention_block_nvfp4_gb300")
+
+    def closure(rel):
+        seen, todo = set(), [rel]
+        while todo:
+            r = todo.pop()
+            if r in seen:
+                continue
+            seen.add(r)
+            text = open(os.path.join(base, r)).read()
+            for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', text, re.M):
+                todo.append(os.path.normpath(os.path.join(os.path.dirname(r), inc)))
+        return seen
+
+    for kernel, deps in bench.KERNEL_DEPS.items():
+        assert deps[0].endswith(".cu"), kernel
+        missing = closure(deps[0]) - set(deps)
+        assert not missing, f"{kernel}: {sorted(missing)} not in its hashed sources"
