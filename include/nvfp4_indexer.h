@@ -203,7 +203,8 @@ int nvfp4_insert(const uint16_t* k_bf16, const int64_t* slot_mapping, int n, uin
  * therefore those of the exact RMSNorm + RoPE up to that fp32 error (an
  * element whose exact value lies that close to a bf16 rounding boundary
  * may round to the other neighbour).
- *   k_bf16         [n][128] bf16 bit patterns, 16-byte aligned
+ *   k_bf16         [n][128] bf16 bit patterns, 16-byte aligned (32-byte
+ *                  aligned keys are read in 32-byte loads: the faster path)
  *   positions      int64 [n] (unused, may be NULL, when rotary_dim == 0)
  *   slot_mapping   int64 [n]: page * 128 + row; negative = skip
  *   norm_weight    bf16 [128], 16-byte aligned
@@ -368,7 +369,9 @@ int indexer_decode_noalloc(const uint8_t* q, const uint8_t* kv_pages, int num_bl
  * page); a row with no visible token gets o = 0.
  *   q          bf16 [num_rows][num_kv_heads * q_per_kv][128], 16-byte aligned
  *   k_cache    bf16 [num_blocks][128][num_kv_heads][128] (token-major pages,
- *              logical page j of request r = block page_table[r][j])
+ *              logical page j of request r = block page_table[r][j]);
+ *              16-byte aligned, and read in 32-byte loads (the faster path)
+ *              when 32-byte aligned
  *   v_cache    same layout as k_cache
  *   page_table int32 [num_reqs][pt_stride] (the indexer's table)
  *   row_req    int32 [num_rows]: the request of each row
